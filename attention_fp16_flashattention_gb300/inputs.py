@@ -1,0 +1,193 @@
+"""Seeded synthetic inputs for the attention workloads (numpy, host memory).
+
+This module only draws random numbers and lays them out; it holds none of the
+attention, bridge or selection arithmetic.  Tests, ``bench.py`` and
+``__graft_entry__.smoke()`` use it to feed both the CUDA library and the CPU
+oracle the same bytes.
+
+Workloads (shapes and value distributions of the pages' workloads: D128
+video-DiT heads, Hq6/Hkv1/D256 long prefill with 32-token E4M3 pages, VSA
+with 64-token cubes and top-k 64):
+
+  dense_small   B1 H2  S256   D128, Q/K/V ~ N(0,1)
+  causal_small  B1 Hq6 Hkv1 D256, Q=1024 after a 3072-token prefix (KV=4096)
+  dense_video   B1 H24 S32768 D128, Q/K = 0.5 N(0,1) + per-head mean offset
+                (each entry N(0, 0.2^2)), V ~ N(0,1)
+  vsa_video     B1 H24 S32768 D128 on an 8x64x64 latent grid split in 512
+                cubes of 4x4x4; Q/K = smooth low-frequency signal + N(0,1)
+  paged_e4m3    B1 Hq6 Hkv1 D256, Q=8192 at the tail of KV=131072, K/V as
+                E4M3 bytes uniform over the 254 finite codes in 32-token pages
+                behind a random page-table permutation; scales 1/16 and 1/8
+
+Every tensor is drawn from its own numpy PCG64 stream keyed by
+(seed, tensor tag), so shapes can be shrunk for tests without changing the
+recipe.
+"""
+
+import math
+
+import numpy as np
+
+TAGS = {"q": 1, "k": 2, "v": 3, "kpages": 4, "vpages": 5, "table": 6,
+        "qmean": 7, "kmean": 8, "qsig": 9, "ksig": 10, "rows": 11}
+
+
+def _rng(seed, tag):
+    return np.random.default_rng([int(seed), TAGS[tag]])
+
+
+def _normal_fp16(rng, shape, std=1.0):
+    """N(0, std^2) values rounded to FP16 (numpy's float32 -> float16 is RNE)."""
+    out = np.empty(shape, dtype=np.float16)
+    flat = out.reshape(-1)
+    step = 1 << 24
+    for i in range(0, flat.size, step):
+        n = min(step, flat.size - i)
+        x = rng.standard_normal(n, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        flat[i:i + n] = x.astype(np.float16)
+    return out
+
+
+def dense_inputs(B, H, S, D, seed, skv=None, video=False):
+    """Q [B][H][S][D], K/V [B][H][Skv][D] FP16.
+
+    video=False: all three i.i.d. N(0,1).
+    video=True : Q, K = 0.5 * N(0,1) + mu (mu: one vector per (tensor, head),
+                 entries N(0, 0.2^2)); V ~ N(0,1).
+    """
+    skv = S if skv is None else skv
+    if not video:
+        q = _normal_fp16(_rng(seed, "q"), (B, H, S, D))
+        k = _normal_fp16(_rng(seed, "k"), (B, H, skv, D))
+        v = _normal_fp16(_rng(seed, "v"), (B, H, skv, D))
+        return q, k, v
+    out = []
+    for name, mean_tag, n in (("q", "qmean", S), ("k", "kmean", skv)):
+        mu = (_rng(seed, mean_tag).standard_normal((B, H, 1, D)) * 0.2).astype(np.float32)
+        x = np.empty((B, H, n, D), dtype=np.float16)
+        rng = _rng(seed, name)
+        for b in range(B):
+            for h in range(H):
+                z = rng.standard_normal((n, D), dtype=np.float32) * np.float32(0.5)
+                x[b, h] = (z + mu[b, h]).astype(np.float16)
+        out.append(x)
+    v = _normal_fp16(_rng(seed, "v"), (B, H, skv, D))
+    return out[0], out[1], v
+
+
+def causal_inputs(B, Hq, Hkv, Q, KV, D, seed):
+    """Q [B][Hq][Q][D], K/V [B][Hkv][KV][D] FP16, all N(0,1)."""
+    q = _normal_fp16(_rng(seed, "q"), (B, Hq, Q, D))
+    k = _normal_fp16(_rng(seed, "k"), (B, Hkv, KV, D))
+    v = _normal_fp16(_rng(seed, "v"), (B, Hkv, KV, D))
+    return q, k, v
+
+
+def cube_major_permutation(grid, cube):
+    """Token permutation raster (t, y, x) -> cube-major order.
+
+    Returns perm with cube_major[i] = raster[perm[i]].  Cube index
+    c = ((t//ct) * (Y//cy) + y//cy) * (X//cx) + x//cx; inside a cube tokens go
+    in (t%ct, y%cy, x%cx) raster order.
+    """
+    T, Y, X = grid
+    ct, cy, cx = cube
+    t, y, x = np.meshgrid(np.arange(T), np.arange(Y), np.arange(X), indexing="ij")
+    c = ((t // ct) * (Y // cy) + y // cy) * (X // cx) + x // cx
+    inner = ((t % ct) * cy + y % cy) * cx + x % cx
+    pos = (c * (ct * cy * cx) + inner).reshape(-1)      # cube-major position of each raster token
+    perm = np.empty_like(pos)
+    perm[pos] = np.arange(pos.size)
+    return perm
+
+
+def _smooth_signal(rng, H, D, grid, n_terms=4):
+    """Per head, a sum of n_terms low-frequency plane waves on the grid.
+
+    signal[token, d] = sum_r a[r, d] * cos(2 pi (f_t t/T + f_y y/Y + f_x x/X) + phi[r, d]),
+    f in {0, 1, 2} per axis and term, a ~ N(0,1)/2, phi ~ U[0, 2 pi).
+    Returned in raster token order, float32 [H][T*Y*X][D].
+    """
+    T, Y, X = grid
+    t, y, x = np.meshgrid(np.arange(T), np.arange(Y), np.arange(X), indexing="ij")
+    t = t.reshape(-1)
+    y = y.reshape(-1)
+    x = x.reshape(-1)
+    out = np.empty((H, T * Y * X, D), dtype=np.float32)
+    for h in range(H):
+        f = rng.integers(0, 3, size=(n_terms, 3))
+        a = rng.standard_normal((n_terms, D)) / 2.0
+        phi = rng.uniform(0.0, 2.0 * math.pi, size=(n_terms, D))
+        theta = 2.0 * math.pi * (f[:, 0:1] * t[None] / T + f[:, 1:2] * y[None] / Y
+                                 + f[:, 2:3] * x[None] / X)            # [R][N]
+        basis = np.concatenate([np.cos(theta), np.sin(theta)], axis=0)   # [2R][N]
+        coef = np.concatenate([a * np.cos(phi), -a * np.sin(phi)], axis=0)  # [2R][D]
+        out[h] = (basis.T @ coef).astype(np.float32)
+    return out
+
+
+def vsa_inputs(B, H, D, seed, grid=(8, 64, 64), cube=(4, 4, 4)):
+    """Q, K, V [B][H][S][D] FP16 in cube-major token order, S = T*Y*X."""
+    S = grid[0] * grid[1] * grid[2]
+    perm = cube_major_permutation(grid, cube)
+    out = []
+    for name, sig_tag in (("q", "qsig"), ("k", "ksig")):
+        sig_rng = _rng(seed, sig_tag)
+        rng = _rng(seed, name)
+        x = np.empty((B, H, S, D), dtype=np.float16)
+        for b in range(B):
+            sig = _smooth_signal(sig_rng, H, D, grid)
+            for h in range(H):
+                z = rng.standard_normal((S, D), dtype=np.float32)
+                x[b, h] = (sig[h] + z)[perm].astype(np.float16)
+        out.append(x)
+    v = _normal_fp16(_rng(seed, "v"), (B, H, S, D))
+    return out[0], out[1], v
+
+
+FINITE_E4M3 = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+
+
+def paged_e4m3_inputs(Hkv, KV, D, seed, page_size=32, num_phys_pages=None):
+    """K/V E4M3 pages [P][page_size][Hkv][D] uint8 and an int32 page table.
+
+    Bytes are uniform over the 254 finite E4M3 codes; the page table is a
+    seeded permutation of the physical pages (logical page i -> table[i]).
+    """
+    n_log = -(-KV // page_size)
+    P = n_log if num_phys_pages is None else num_phys_pages
+    rk = _rng(seed, "kpages")
+    rv = _rng(seed, "vpages")
+    kp = FINITE_E4M3[rk.integers(0, FINITE_E4M3.size, size=(P, page_size, Hkv, D))]
+    vp = FINITE_E4M3[rv.integers(0, FINITE_E4M3.size, size=(P, page_size, Hkv, D))]
+    table = _rng(seed, "table").permutation(P)[:n_log].astype(np.int32)
+    return kp, vp, table
+
+
+def sample_rows(n_heads, n_rows, count, seed, row_limit=None):
+    """``count`` distinct seeded (head, row) pairs, sorted; rows < row_limit."""
+    lim = n_rows if row_limit is None else row_limit
+    total = n_heads * lim
+    rng = _rng(seed, "rows")
+    pick = rng.choice(total, size=min(count, total), replace=False)
+    pick.sort()
+    return np.stack([pick // lim, pick % lim], axis=1).astype(np.int64)
+
+
+# The five workloads, with their seeds (1000 + workload number).
+WORKLOADS = {
+    "dense_small": dict(kind="dense", B=1, H=2, S=256, D=128, seed=1001),
+    "causal_small": dict(kind="causal", B=1, Hq=6, Hkv=1, Q=1024, KV=4096, D=256, seed=1002),
+    "dense_video": dict(kind="dense", B=1, H=24, S=32768, D=128, seed=1003, video=True),
+    "vsa_video": dict(kind="vsa", B=1, H=24, D=128, grid=(8, 64, 64), cube=(4, 4, 4), topk=64,
+                      seed=1004),
+    "paged_e4m3": dict(kind="paged", B=1, Hq=6, Hkv=1, Q=8192, KV=131072, D=256, page_size=32,
+                       k_scale=0.0625, v_scale=0.125, seed=1005),
+}
+
+
+def softmax_scale(D):
+    """The FP32 scale 1/sqrt(D) (computed in double, stored as float)."""
+    return float(np.float32(1.0 / math.sqrt(D)))
