@@ -1,0 +1,236 @@
+"""Fused FP16 attention for one GB300 (sm_103a): Python binding of libgbattn.
+
+The CUDA library (``libgbattn.so``, built in-tree from ``csrc/`` by
+``build.py``) does all the work; this module only marshals arguments.  PyTorch
+supplies device memory and the current CUDA stream.  Every function has the
+name of the C entry point it calls (see ``include/gbattn.h``) and raises
+``GbattnError`` when that call returns a non-zero status.  There is no CPU
+path: if the library is missing, the first call raises.
+
+The library is loaded lazily, so the seeded input generators in ``inputs``
+can be imported on a machine without a GPU.
+"""
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgbattn.so")
+
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "gbattn_version": (_i, []),
+    "gbattn_status_string": (ctypes.c_char_p, [_i]),
+    "gbattn_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "gbattn_set_wait_limit_ns": (_i, [ctypes.c_uint64]),
+    "gbattn_launch_count": (ctypes.c_uint64, []),
+    "attn_dense_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "attn_causal_prefill_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "attn_causal_prefill_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
+                                     _vp, _sz, _vp]),
+    "e4m3_paged_to_fp16": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _vp, _vp, _vp]),
+    "vsa_select_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "vsa_select_blocks": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "vsa_sparse_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
+}
+
+DEV_WAIT_TIMEOUT = 1
+DEV_BAD_PAGE = 2
+DEV_BAD_INDEX = 4
+
+
+class GbattnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def load():
+    """Load libgbattn.so (once) and declare its C signatures."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_string(status):
+    return load().gbattn_status_string(int(status)).decode()
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise GbattnError(fn, rc)
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+def _scale(scale, D):
+    return float(1.0 / D ** 0.5) if scale is None else float(scale)
+
+
+def version():
+    return load().gbattn_version()
+
+
+def launch_count():
+    """Kernels launched by the library since it was loaded."""
+    return int(load().gbattn_launch_count())
+
+
+def set_wait_limit_ns(ns):
+    _check("gbattn_set_wait_limit_ns", load().gbattn_set_wait_limit_ns(int(ns)))
+
+
+def device_status(stream=None):
+    """Read and clear the device status word (gbattn_device_flag bits)."""
+    out = ctypes.c_uint32(0)
+    _check("gbattn_device_status", load().gbattn_device_status(_stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def attn_dense_fwd(q, k, v, o=None, lse=None, scale=None, stream=None):
+    """Dense non-causal attention. q [B,H,Sq,D], k/v [B,H,Skv,D] FP16 -> o [B,H,Sq,D]."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.float16, 4)
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    if tuple(k.shape) != (B, H, Skv, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, H, Skv, D] matching q")
+    o = torch.empty_like(q) if o is None else o
+    _need(o, "o", torch.float16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    rc = load().attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Skv, D,
+                               _scale(scale, D), _stream(stream))
+    _check("attn_dense_fwd", rc)
+    return o
+
+
+def attn_causal_prefill_workspace_size(B, Hq, Q_pad, KV, D):
+    return int(load().attn_causal_prefill_workspace_size(B, Hq, Q_pad, KV, D))
+
+
+def attn_causal_prefill_fwd(q, k, v, q_real=None, o=None, lse=None, scale=None, workspace=None,
+                            stream=None):
+    """Causal prefill with shared-KV heads. q [B,Hq,Q_pad,D], k/v [B,Hkv,KV,D] FP16."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.float16, 4)
+    B, Hq, Qp, D = q.shape
+    Hkv, KV = k.shape[1], k.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, KV, D] matching q")
+    q_real = Qp if q_real is None else int(q_real)
+    o = torch.empty_like(q) if o is None else o
+    _need(o, "o", torch.float16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    if workspace is None:
+        nbytes = attn_causal_prefill_workspace_size(B, Hq, Qp, KV, D)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    rc = load().attn_causal_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                        Qp, q_real, KV, D, _scale(scale, D), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream))
+    _check("attn_causal_prefill_fwd", rc)
+    return o
+
+
+def e4m3_paged_to_fp16(k_pages, v_pages, page_table, kv_len, k_scale, v_scale, k_out=None,
+                       v_out=None, stream=None):
+    """Paged E4M3 bytes [P, page, Hkv, D] -> FP16 [Hkv, kv_len, D] for K and V."""
+    import torch
+    _need(k_pages, "k_pages", torch.uint8, 4)
+    _need(v_pages, "v_pages", torch.uint8, 4)
+    _need(page_table, "page_table", torch.int32, 1)
+    P, ps, Hkv, D = k_pages.shape
+    if tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages and v_pages must have the same shape")
+    if k_out is None:
+        k_out = torch.empty((Hkv, kv_len, D), dtype=torch.float16, device=k_pages.device)
+    if v_out is None:
+        v_out = torch.empty((Hkv, kv_len, D), dtype=torch.float16, device=k_pages.device)
+    _need(k_out, "k_out", torch.float16)
+    _need(v_out, "v_out", torch.float16)
+    rc = load().e4m3_paged_to_fp16(_ptr(k_pages), _ptr(v_pages), _ptr(page_table), P, ps,
+                                   int(kv_len), Hkv, D, float(k_scale), float(v_scale),
+                                   _ptr(k_out), _ptr(v_out), _stream(stream))
+    _check("e4m3_paged_to_fp16", rc)
+    return k_out, v_out
+
+
+def vsa_select_workspace_size(B, H, S, D, block):
+    return int(load().vsa_select_workspace_size(B, H, S, D, block))
+
+
+def vsa_select_blocks(q, k, topk, block=64, idx=None, workspace=None, stream=None):
+    """Top-k key cubes per query cube. q, k [B,H,S,D] FP16 -> idx int32 [B,H,S/block,topk]."""
+    import torch
+    _need(q, "q", torch.float16, 4)
+    _need(k, "k", torch.float16, 4)
+    B, H, S, D = q.shape
+    if tuple(k.shape) != tuple(q.shape):
+        raise ValueError("q and k must have the same shape")
+    nc = S // block
+    if idx is None:
+        idx = torch.empty((B, H, nc, topk), dtype=torch.int32, device=q.device)
+    _need(idx, "idx", torch.int32)
+    if workspace is None:
+        workspace = torch.empty(max(vsa_select_workspace_size(B, H, S, D, block), 16),
+                                dtype=torch.uint8, device=q.device)
+    rc = load().vsa_select_blocks(_ptr(q), _ptr(k), B, H, S, D, block, int(topk), _ptr(idx),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    _check("vsa_select_blocks", rc)
+    return idx
+
+
+def vsa_sparse_fwd(q, k, v, idx, block=64, o=None, lse=None, scale=None, stream=None):
+    """Block-sparse attention over the cubes in idx. q/k/v [B,H,S,D] FP16 cube-major."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.float16, 4)
+    _need(idx, "idx", torch.int32, 4)
+    B, H, S, D = q.shape
+    topk = idx.shape[3]
+    o = torch.empty_like(q) if o is None else o
+    _need(o, "o", torch.float16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    rc = load().vsa_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse), B, H, S,
+                               D, block, topk, _scale(scale, D), _stream(stream))
+    _check("vsa_sparse_fwd", rc)
+    return o

@@ -1,0 +1,789 @@
+// Fused forward attention on sm_103a: O = softmax(scale * Q K^T + mask) V with
+// FP16 Q/K/V/P/O, FP32 accumulation in tensor memory and an FP32 online softmax
+// ("Integrate FP32 v37 prefill and exact E4M3 bridge", Implementation: FP32
+// QK/PV accumulation, FP32 prefix/tail state and final merge, FP16
+// probabilities and output).
+//
+// One CTA owns a 128-row query tile and walks a list of 128-key tiles.  Each
+// key tile is two 64-key halves; for dense and causal attention the halves are
+// adjacent, for VSA they are two selected 64-token cubes (the two-query-half x
+// two-key-half blocks with a 4-bit quadrant mask of block_lists.py in the
+// FastVideo compare view).
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q once, then K and V tiles through an NS-slot ring
+//               in the order the MMA warp consumes them (K0, K1, V0, K2, V1, ...).
+//   warp 1      allocates tensor memory; one lane issues every tcgen05.mma:
+//               S = Q K_j^T (SMEM x SMEM), then O += P_j V_j (P from TMEM).
+//               S_{j+1} is computed while the softmax warps work on tile j.
+//   warps 2..5  softmax: one query row per thread (TMEM lane = row); row max,
+//               exp2, row sum, P -> FP16 into TMEM; lazy O rescaling (only when
+//               the running max grows by more than 2^8); epilogue O / l.
+// Tensor memory (512 columns): S [0,128) FP32, P double buffer [128,192) and
+// [192,256) (FP16 pairs), O [256, 256 + D) FP32.
+//
+// Every wait is bounded in time (see WaitCtl): a wait that runs out records
+// GBATTN_DEV_WAIT_TIMEOUT in the device status word, the CTA stops, waits a
+// bounded time for its copies and MMAs in flight, frees tensor memory and exits.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "host.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+constexpr int BM = 128;             // query rows per CTA
+constexpr int BN = 128;             // keys per tile (two halves of 64)
+constexpr int kThreads = 192;
+constexpr int kMaxSparseTiles = 512;
+constexpr int kMaxTopk = 512;
+constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s for draining after an abort
+
+enum Mode { kDense = 0, kCausal = 1, kSparse = 2 };
+
+struct AttnArgs {
+    int seq_q;          // query rows per head
+    int seq_k;          // keys per KV head
+    int heads_q;        // B * Hq (rows of the grid)
+    int hq;             // query heads per batch entry
+    int hkv;            // KV heads per batch entry
+    int group;          // Hq / Hkv
+    int q_real;         // causal: real queries
+    int kv_prefix;      // causal: KV - Q_real
+    int n_chunks;       // causal: key-range chunks per query tile
+    int n_cubes;        // sparse: S / 64
+    int topk;           // sparse
+    float scale_log2;   // scale * log2(e)
+    __half* o;
+    float* lse;         // optional natural-log LSE
+    float* part_o;      // causal, n_chunks > 1: [C][heads_q][seq_q][D] FP32, normalised
+    float* part_lse;    // causal, n_chunks > 1: [C][heads_q][seq_q] log2-sum-exp2
+    const int32_t* idx; // sparse: [heads][n_cubes][topk]
+    uint32_t* status;
+    uint64_t wait_limit;
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int NS = D == 128 ? 4 : 2;          // K/V ring slots
+    static constexpr int CHUNK = 128 * 128;               // 128 rows x 64 FP16 columns
+    static constexpr int HALF = 64 * 128;                 // 64 rows x 64 columns
+    static constexpr int KCH = D / 64;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int SLOT_BYTES = BN * D * 2;
+    static constexpr uint32_t T_S = 0, T_P0 = 128, T_P1 = 192, T_O = 256;
+    static constexpr uint32_t IDESC_QK = idesc_f16(BM, BN, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_f16(BM, D, false, true);
+};
+
+struct Ctrl {
+    uint64_t q_full;
+    uint64_t full[4];
+    uint64_t empty[4];
+    uint64_t s_full, s_free;
+    uint64_t p_full[2];
+    uint64_t pv_done[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int n_tiles;
+};
+
+struct SparseTiles {
+    int list_a[kMaxTopk];
+    int list_b[kMaxTopk];
+    int key0[kMaxSparseTiles];
+    int key1[kMaxSparseTiles];
+    uint8_t mask[kMaxSparseTiles];
+};
+
+template <int D, int MODE>
+constexpr int smem_bytes() {
+    return 1024 + Cfg<D>::Q_BYTES + Cfg<D>::NS * Cfg<D>::SLOT_BYTES + 256 +
+           (MODE == kSparse ? static_cast<int>(sizeof(SparseTiles)) : 0);
+}
+
+// Bounded wait that ignores the abort flag (used only to drain after an abort).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kDrainNs) return;
+    }
+}
+
+// Item order of the K/V ring: K0, then (K_j, V_{j-1}) for j = 1..n-1, then V_{n-1}.
+__device__ __forceinline__ void ring_item(int it, int n, int& tile, bool& is_v) {
+    if (it == 0) { tile = 0; is_v = false; return; }
+    if (it == 2 * n - 1) { tile = n - 1; is_v = true; return; }
+    if (it & 1) { tile = (it + 1) >> 1; is_v = false; }
+    else { tile = (it >> 1) - 1; is_v = true; }
+}
+
+// Merge two strictly ascending cube lists into the tile list of a query-cube
+// pair.  Entries that are out of range or not ascending are skipped and flagged.
+__device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& a, int bh,
+                                   int pair) {
+    const int lane = threadIdx.x & 31;
+    const int ca = 2 * pair, cb = 2 * pair + 1;
+    const int na = a.topk;
+    const int nb = cb < a.n_cubes ? a.topk : 0;
+    const int32_t* la = a.idx + (static_cast<long long>(bh) * a.n_cubes + ca) * a.topk;
+    const int32_t* lb = la + a.topk;
+    for (int i = lane; i < na; i += 32) st->list_a[i] = la[i];
+    for (int i = lane; i < nb; i += 32) st->list_b[i] = lb[i];
+    __syncwarp();
+    if (lane != 0) return;
+    int ia = 0, ib = 0, pa = -1, pb = -1, nu = 0, nt = 0, pend = -1, pend_f = 0;
+    bool bad = false;
+    constexpr int INF = 0x7fffffff;
+    while (true) {
+        int va = INF, vb = INF;
+        while (ia < na) {
+            const int v = st->list_a[ia];
+            if (v > pa && v < a.n_cubes) { va = v; break; }
+            bad = true;
+            ++ia;
+        }
+        while (ib < nb) {
+            const int v = st->list_b[ib];
+            if (v > pb && v < a.n_cubes) { vb = v; break; }
+            bad = true;
+            ++ib;
+        }
+        if (va == INF && vb == INF) break;
+        const int c = min(va, vb);
+        const int f = (va == c ? 1 : 0) | (vb == c ? 2 : 0);
+        if (va == c) { pa = va; ++ia; }
+        if (vb == c) { pb = vb; ++ib; }
+        if (pend < 0) {
+            pend = c;
+            pend_f = f;
+        } else {
+            st->key0[nt] = pend * 64;
+            st->key1[nt] = c * 64;
+            st->mask[nt] = static_cast<uint8_t>((pend_f & 1) | ((f & 1) << 1) |
+                                                ((pend_f >> 1) << 2) | ((f >> 1) << 3));
+            ++nt;
+            pend = -1;
+        }
+        ++nu;
+    }
+    if (pend >= 0) {   // odd union: the second half repeats the cube, fully masked
+        st->key0[nt] = pend * 64;
+        st->key1[nt] = pend * 64;
+        st->mask[nt] = static_cast<uint8_t>((pend_f & 1) | ((pend_f >> 1) << 2));
+        ++nt;
+    }
+    if (bad) atomicOr(a.status, kDevBadIndex);
+    ctrl->n_tiles = nt;
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sKV = smem + C::Q_BYTES;
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(sKV + C::NS * C::SLOT_BYTES);
+    SparseTiles* st = reinterpret_cast<SparseTiles*>(reinterpret_cast<uint8_t*>(ctrl) + 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y;
+
+    // ---- work decode
+    int q_row0, kv_bh, n_tiles = 0, tile0 = 0, chunk = 0;
+    if (MODE == kCausal) {
+        const int qt = blockIdx.x / a.n_chunks;
+        chunk = blockIdx.x - qt * a.n_chunks;
+        q_row0 = qt * BM;
+        const int b = bh / a.hq, h = bh - b * a.hq;
+        kv_bh = b * a.hkv + h / a.group;
+        const long long kend = min(static_cast<long long>(a.seq_k),
+                                   static_cast<long long>(a.kv_prefix) + q_row0 + BM);
+        const int T = static_cast<int>((kend + BN - 1) / BN);
+        tile0 = static_cast<int>(static_cast<long long>(chunk) * T / a.n_chunks);
+        n_tiles = static_cast<int>(static_cast<long long>(chunk + 1) * T / a.n_chunks) - tile0;
+    } else {
+        q_row0 = blockIdx.x * BM;
+        kv_bh = bh;
+        if (MODE == kDense) n_tiles = (a.seq_k + BN - 1) / BN;
+    }
+
+    // ---- prologue
+    if (threadIdx.x == 0) {
+        mbar_init(&ctrl->q_full, 1);
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(&ctrl->full[i], 1);
+            mbar_init(&ctrl->empty[i], 1);
+        }
+        mbar_init(&ctrl->s_full, 1);
+        mbar_init(&ctrl->s_free, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctrl->p_full[i], 128);
+            mbar_init(&ctrl->pv_done[i], 1);
+        }
+        mbar_init(&ctrl->drain, 1);
+        ctrl->abort = 0;
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
+        if (MODE == kSparse) build_sparse_tiles(st, ctrl, a, bh, blockIdx.x);
+        __syncwarp();
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctrl->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    if (MODE == kSparse) n_tiles = ctrl->n_tiles;
+    const WaitCtl w{a.wait_limit, a.status, &ctrl->abort};
+
+    auto tile_keys = [&](int t, int& k0, int& k1) {
+        if (MODE == kSparse) {
+            k0 = st->key0[t];
+            k1 = st->key1[t];
+        } else {
+            k0 = (tile0 + t) * BN;
+            k1 = k0 + 64;
+        }
+    };
+
+    if (warp == 0) {
+        // ================= TMA producer
+        if (lane == 0 && n_tiles > 0) {
+            int last_it[4] = {-1, -1, -1, -1};
+            mbar_arrive_expect_tx(&ctrl->q_full, C::Q_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+                tma_load_3d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, bh);
+            bool ok = true;
+            for (int it = 0; it < 2 * n_tiles; ++it) {
+                const int slot = it % C::NS;
+                const uint32_t ph = (it / C::NS) & 1;
+                if (!wait_one(&ctrl->empty[slot], ph ^ 1u, w)) { ok = false; break; }
+                int t;
+                bool is_v;
+                ring_item(it, n_tiles, t, is_v);
+                int k0, k1;
+                tile_keys(t, k0, k1);
+                const CUtensorMap* m = is_v ? &tmV : &tmK;
+                uint8_t* dst = sKV + slot * C::SLOT_BYTES;
+                mbar_arrive_expect_tx(&ctrl->full[slot], C::SLOT_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c) {
+                    tma_load_3d(dst + c * C::CHUNK, m, &ctrl->full[slot], c * 64, k0, kv_bh);
+                    tma_load_3d(dst + c * C::CHUNK + C::HALF, m, &ctrl->full[slot], c * 64, k1,
+                                kv_bh);
+                }
+                last_it[slot] = it;
+            }
+            if (!ok) {   // let copies in flight land before the CTA exits
+                drain_wait(&ctrl->q_full, 0);
+                for (int s = 0; s < C::NS; ++s)
+                    if (last_it[s] >= 0) drain_wait(&ctrl->full[s], (last_it[s] / C::NS) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            bool ok = wait_one(&ctrl->q_full, 0, w);
+            const uint32_t qa = smem_addr(sQ);
+            auto issue_qk = [&](int slot) {
+                const uint32_t ka = smem_addr(sKV + slot * C::SLOT_BYTES);
+#pragma unroll
+                for (int k16 = 0; k16 < D / 16; ++k16) {
+                    const uint32_t off = (k16 >> 2) * C::CHUNK + (k16 & 3) * 32;
+                    mma_ss(tmem + C::T_S, sdesc_sw128(qa + off, 16, 1024),
+                           sdesc_sw128(ka + off, 16, 1024), C::IDESC_QK, k16 > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int slot, int b, bool acc) {
+                const uint32_t va = smem_addr(sKV + slot * C::SLOT_BYTES);
+                const uint32_t pcol = tmem + (b ? C::T_P1 : C::T_P0);
+#pragma unroll
+                for (int k16 = 0; k16 < BN / 16; ++k16)
+                    mma_ts(tmem + C::T_O, pcol + k16 * 8, sdesc_sw128(va + k16 * 2048, C::CHUNK, 1024),
+                           C::IDESC_PV, (acc || k16 > 0) ? 1u : 0u);
+            };
+            int it = 0;
+            if (ok) ok = wait_one(&ctrl->full[0], 0, w);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(0);
+                mma_commit(&ctrl->s_full);
+                mma_commit(&ctrl->empty[0]);
+                it = 1;
+            }
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j + 1 < n_tiles) {
+                    const int slot = it % C::NS;
+                    ok = wait_one(&ctrl->full[slot], (it / C::NS) & 1, w) &&
+                         wait_one(&ctrl->s_free, j & 1, w);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(slot);
+                    mma_commit(&ctrl->s_full);
+                    mma_commit(&ctrl->empty[slot]);
+                    ++it;
+                }
+                const int b = j & 1;
+                const int slot = it % C::NS;
+                ok = wait_one(&ctrl->p_full[b], (j >> 1) & 1, w) &&
+                     wait_one(&ctrl->full[slot], (it / C::NS) & 1, w);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(slot, b, j > 0);
+                mma_commit(&ctrl->empty[slot]);
+                mma_commit(&ctrl->pv_done[b]);
+                ++it;
+            }
+            if (!ok) {   // wait for issued MMAs before tensor memory is freed
+                mma_commit(&ctrl->drain);
+                drain_wait(&ctrl->drain, 0);
+            }
+        }
+    } else {
+        // ================= softmax / correction / epilogue (warps 2..5)
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const long long row_g = static_cast<long long>(q_row0) + row;
+        const int row_half = row >> 6;
+        int lim = a.seq_k;   // keys >= lim are invisible to this row
+        if (MODE == kCausal)
+            lim = static_cast<int>(min(static_cast<long long>(a.seq_k), a.kv_prefix + row_g + 1));
+        const int lim0 = MODE == kCausal
+                             ? static_cast<int>(min(static_cast<long long>(a.seq_k),
+                                                    static_cast<long long>(a.kv_prefix) + q_row0 + 1))
+                             : a.seq_k;
+        const float sl2 = a.scale_log2;
+        float m_run = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            ok = wait_warp(&ctrl->s_full, j & 1, w);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t s[128];
+            tmem_ld32(tl + C::T_S, s);
+            tmem_ld32(tl + C::T_S + 32, s + 32);
+            tmem_ld32(tl + C::T_S + 64, s + 64);
+            tmem_ld32(tl + C::T_S + 96, s + 96);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&ctrl->s_free);
+
+            int k0, k1;
+            tile_keys(j, k0, k1);
+            if (MODE == kSparse) {
+                const uint32_t mk = st->mask[j];
+                if (mk != 0xFu) {
+                    const bool v0 = (mk >> (row_half * 2)) & 1u, v1 = (mk >> (row_half * 2 + 1)) & 1u;
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (!(c < 64 ? v0 : v1)) s[c] = __float_as_uint(-INFINITY);
+                }
+            } else if (k0 + BN > lim0) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (k0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+            const float m_new = fmaxf(m_run, mx * sl2);
+            const bool need = m_new > m_run + 8.0f;
+            float alpha = 1.0f;
+            if (need) {
+                alpha = fast_exp2(m_run - m_new);
+                m_run = m_new;
+            }
+            const bool warp_need = __any_sync(0xffffffffu, need);
+            const float m_use = m_run == -INFINITY ? 0.0f : m_run;
+            float rs0 = 0.0f, rs1 = 0.0f;
+            uint32_t p2[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(s[2 * i]), sl2, -m_use));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(s[2 * i + 1]), sl2, -m_use));
+                rs0 += p0;
+                rs1 += p1;
+                p2[i] = pack_half2(p0, p1);
+            }
+            l = l * alpha + (rs0 + rs1);
+            const int b = j & 1;
+            if (j >= 2) {   // PV_{j-2} must have finished reading this P buffer
+                ok = wait_warp(&ctrl->pv_done[b], ((j - 2) >> 1) & 1, w);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            const uint32_t pcol = tl + (b ? C::T_P1 : C::T_P0);
+            tmem_st32(pcol, p2);
+            tmem_st32(pcol + 32, p2 + 32);
+            tmem_st_wait();
+            if (warp_need && j > 0) {   // rescale O after PV_{j-1} has landed
+                ok = wait_warp(&ctrl->pv_done[b ^ 1], ((j - 1) >> 1) & 1, w);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tl + C::T_O + cc * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tl + C::T_O + cc * 32, o);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            mbar_arrive(&ctrl->p_full[b]);
+        }
+        if (ok && n_tiles > 0) {
+            ok = wait_warp(&ctrl->pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, w);
+            tc_fence_after();
+        }
+        if (ok) {
+            const bool row_ok = row_g < a.seq_q;
+            const bool zero_row = MODE == kCausal && row_g >= a.q_real;
+            const float inv_l = (l > 0.0f && !zero_row) ? 1.0f / l : 0.0f;
+            const float lse2 = (l > 0.0f && !zero_row) ? m_run + __log2f(l) : -INFINITY;
+            const bool partial = MODE == kCausal && a.n_chunks > 1;
+            const long long orow = static_cast<long long>(bh) * a.seq_q + row_g;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                if (n_tiles > 0) {
+                    tmem_ld32(tl + C::T_O + cc * 32, o);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                if (!row_ok) continue;
+                if (partial) {
+                    float4* dst = reinterpret_cast<float4*>(
+                        a.part_o + ((static_cast<long long>(chunk) * a.heads_q * a.seq_q + orow) * D +
+                                    cc * 32));
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l,
+                                             __uint_as_float(o[4 * e + 1]) * inv_l,
+                                             __uint_as_float(o[4 * e + 2]) * inv_l,
+                                             __uint_as_float(o[4 * e + 3]) * inv_l);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(a.o + orow * D + cc * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t hw[4];
+#pragma unroll
+                        for (int f = 0; f < 4; ++f)
+                            hw[f] = pack_half2(__uint_as_float(o[8 * e + 2 * f]) * inv_l,
+                                               __uint_as_float(o[8 * e + 2 * f + 1]) * inv_l);
+                        dst[e] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    }
+                }
+            }
+            if (row_ok) {
+                if (partial)
+                    a.part_lse[static_cast<long long>(chunk) * a.heads_q * a.seq_q + orow] = lse2;
+                else if (a.lse)
+                    a.lse[orow] = lse2 * 0.69314718055994531f;
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// Combine the per-chunk FP32 partials of the causal prefill (the final merge of
+// the FP32 prefix/tail states): with L_c = log2-sum-exp2 of chunk c,
+// L = log2(sum_c 2^L_c) and O = sum_c 2^(L_c - L) O_c.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict__ part_o,
+                                                         const float* __restrict__ part_lse,
+                                                         int n_chunks, long long rows, int seq_q,
+                                                         int q_real, __half* __restrict__ o,
+                                                         float* __restrict__ lse) {
+    const long long row = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int i = static_cast<int>(row % seq_q);
+    constexpr int PER = D / 32;   // elements per lane (contiguous)
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
+    float total = -INFINITY;
+    if (i < q_real) {
+        float mx = -INFINITY;
+        for (int c = 0; c < n_chunks; ++c) mx = fmaxf(mx, part_lse[c * rows + row]);
+        if (mx != -INFINITY) {
+            float wsum = 0.0f;
+            for (int c = 0; c < n_chunks; ++c) wsum += exp2f(part_lse[c * rows + row] - mx);
+            total = mx + log2f(wsum);
+            for (int c = 0; c < n_chunks; ++c) {
+                const float wc = exp2f(part_lse[c * rows + row] - total);
+                if (wc == 0.0f) continue;
+                const float4* src =
+                    reinterpret_cast<const float4*>(part_o + (c * rows + row) * D + lane * PER);
+#pragma unroll
+                for (int e = 0; e < PER / 4; ++e) {
+                    const float4 v = src[e];
+                    acc[4 * e] += wc * v.x;
+                    acc[4 * e + 1] += wc * v.y;
+                    acc[4 * e + 2] += wc * v.z;
+                    acc[4 * e + 3] += wc * v.w;
+                }
+            }
+        }
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(o + row * D + lane * PER);
+#pragma unroll
+    for (int e = 0; e < PER / 2; ++e) dst[e] = pack_half2(acc[2 * e], acc[2 * e + 1]);
+    if (lse && lane == 0) lse[row] = total * 0.69314718055994531f;
+}
+
+template <int D, int MODE>
+int set_smem_attr() {
+    static std::once_flag once[64];
+    static int rc[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBATTN_ERR_CUDA;
+    std::call_once(once[dev], [&] {
+        rc[dev] = cudaFuncSetAttribute(attn_fwd_kernel<D, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes<D, MODE>()) == cudaSuccess
+                      ? GBATTN_OK
+                      : GBATTN_ERR_CUDA;
+    });
+    return rc[dev];
+}
+
+template <int D, int MODE>
+int launch_attn(const void* q, const void* k, const void* v, int seq_q, int seq_k, int heads_q,
+                int heads_kv, dim3 grid, AttnArgs args, cudaStream_t stream) {
+    CUtensorMap tq, tk, tv;
+    if (encode_tmap_f16_3d(&tq, q, D, seq_q, heads_q, 64, BM) != GBATTN_OK ||
+        encode_tmap_f16_3d(&tk, k, D, seq_k, heads_kv, 64, 64) != GBATTN_OK ||
+        encode_tmap_f16_3d(&tv, v, D, seq_k, heads_kv, 64, 64) != GBATTN_OK)
+        return GBATTN_ERR_CUDA;
+    int rc = set_smem_attr<D, MODE>();
+    if (rc != GBATTN_OK) return rc;
+    attn_fwd_kernel<D, MODE><<<grid, kThreads, smem_bytes<D, MODE>(), stream>>>(tq, tk, tv, args);
+    count_launches(1);
+    return launch_status();
+}
+
+AttnArgs base_args(const DeviceState& dev, float scale) {
+    AttnArgs a{};
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.status = dev.status;
+    a.wait_limit = wait_limit_ns();
+    a.group = 1;
+    return a;
+}
+
+// Key-range chunks per causal query tile: minimise (waves of CTAs) / chunks
+// plus a small charge per chunk for the merge traffic, keeping at least two
+// key tiles per chunk.  The rule depends only on the padded query count, so
+// the workspace query and the call agree; real queries fewer than Q_pad only
+// lengthen the key ranges.
+int choose_chunks(int B, int Hq, int Q_pad, int KV, int nsm) {
+    const long long nqt = (Q_pad + BM - 1) / BM;
+    const long long units = static_cast<long long>(B) * Hq * nqt;
+    const long long q_real_max = std::min(Q_pad, KV);
+    const long long kend0 = std::min<long long>(KV, KV - q_real_max + BM);
+    const long long tmin = (kend0 + BN - 1) / BN;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int c = 1; c <= 8; ++c) {
+        if (c > 1 && tmin < 2LL * c) break;
+        const long long waves = (units * c + nsm - 1) / nsm;
+        const double cost = static_cast<double>(waves) / c + 0.01 * c;
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = c;
+        }
+    }
+    return best;
+}
+
+size_t causal_workspace(int chunks, int B, int Hq, int Q_pad, int D) {
+    if (chunks <= 1) return 0;
+    return static_cast<size_t>(chunks) * B * Hq * Q_pad * (static_cast<size_t>(D) + 1) *
+           sizeof(float);
+}
+
+int sm_count_or_default() {
+    DeviceState d;
+    return current_device(&d) == GBATTN_OK ? d.num_sms : 148;
+}
+
+}  // namespace
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" int attn_dense_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Sq, int Skv, int D, float scale, void* stream) {
+    if (!q || !k || !v || !o) return GBATTN_ERR_NULL;
+    if (B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0) return GBATTN_ERR_SHAPE;
+    if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
+    if (D != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return GBATTN_ERR_ALIGN;
+    const size_t qb = static_cast<size_t>(B) * H * Sq * D * 2;
+    const size_t kb = static_cast<size_t>(B) * H * Skv * D * 2;
+    const size_t lb = static_cast<size_t>(B) * H * Sq * 4;
+    if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kb) || overlaps(o, qb, v, kb) ||
+        overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
+        overlaps(lse, lb, o, qb))
+        return GBATTN_ERR_ALIAS;
+    DeviceState dev;
+    int rc = current_device(&dev);
+    if (rc != GBATTN_OK) return rc;
+    AttnArgs a = base_args(dev, scale);
+    a.seq_q = Sq;
+    a.seq_k = Skv;
+    a.heads_q = B * H;
+    a.hq = H;
+    a.hkv = H;
+    a.n_chunks = 1;
+    a.o = static_cast<__half*>(o);
+    a.lse = lse;
+    dim3 grid((Sq + BM - 1) / BM, B * H);
+    return launch_attn<128, kDense>(q, k, v, Sq, Skv, B * H, B * H, grid, a,
+                                    static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t attn_causal_prefill_workspace_size(int B, int Hq, int Q_pad, int KV, int D) {
+    if (B <= 0 || Hq <= 0 || Q_pad <= 0 || KV <= 0 || D <= 0) return 0;
+    return causal_workspace(choose_chunks(B, Hq, Q_pad, KV, sm_count_or_default()), B, Hq, Q_pad,
+                            D);
+}
+
+extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, int B, int Hq, int Hkv, int Q_pad, int Q_real,
+                                       int KV, int D, float scale, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !o) return GBATTN_ERR_NULL;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Q_pad <= 0 || KV <= 0) return GBATTN_ERR_SHAPE;
+    if (Hq % Hkv != 0 || Q_pad % 64 != 0 || Q_real < 1 || Q_real > Q_pad || Q_real > KV ||
+        KV % 32 != 0)
+        return GBATTN_ERR_SHAPE;
+    if (static_cast<long long>(B) * Hq > 65535) return GBATTN_ERR_SHAPE;
+    if (D != 256) return GBATTN_ERR_UNSUPPORTED;
+    if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return GBATTN_ERR_ALIGN;
+    const size_t qb = static_cast<size_t>(B) * Hq * Q_pad * D * 2;
+    const size_t kb = static_cast<size_t>(B) * Hkv * KV * D * 2;
+    const size_t lb = static_cast<size_t>(B) * Hq * Q_pad * 4;
+    if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kb) || overlaps(o, qb, v, kb) ||
+        overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
+        overlaps(lse, lb, o, qb))
+        return GBATTN_ERR_ALIAS;
+    DeviceState dev;
+    int rc = current_device(&dev);
+    if (rc != GBATTN_OK) return rc;
+    int chunks = choose_chunks(B, Hq, Q_pad, KV, dev.num_sms);
+    while (chunks > 1 && (!workspace || workspace_bytes < causal_workspace(chunks, B, Hq, Q_pad, D)))
+        --chunks;
+    const size_t wb = causal_workspace(chunks, B, Hq, Q_pad, D);
+    if (wb > 0 && (overlaps(workspace, wb, q, qb) || overlaps(workspace, wb, k, kb) ||
+                   overlaps(workspace, wb, v, kb) || overlaps(workspace, wb, o, qb) ||
+                   overlaps(workspace, wb, lse, lb)))
+        return GBATTN_ERR_ALIAS;
+    AttnArgs a = base_args(dev, scale);
+    a.seq_q = Q_pad;
+    a.seq_k = KV;
+    a.heads_q = B * Hq;
+    a.hq = Hq;
+    a.hkv = Hkv;
+    a.group = Hq / Hkv;
+    a.q_real = Q_real;
+    a.kv_prefix = KV - Q_real;
+    a.n_chunks = chunks;
+    a.o = static_cast<__half*>(o);
+    a.lse = lse;
+    const long long rows = static_cast<long long>(B) * Hq * Q_pad;
+    if (chunks > 1) {
+        a.part_o = static_cast<float*>(workspace);
+        a.part_lse = a.part_o + static_cast<size_t>(chunks) * rows * D;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    dim3 grid(((Q_pad + BM - 1) / BM) * chunks, B * Hq);
+    rc = launch_attn<256, kCausal>(q, k, v, Q_pad, KV, B * Hq, B * Hkv, grid, a, s);
+    if (rc != GBATTN_OK || chunks == 1) return rc;
+    const long long threads = rows * 32;
+    attn_merge_kernel<256><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
+        a.part_o, a.part_lse, chunks, rows, Q_pad, Q_real, a.o, lse);
+    count_launches(1);
+    return launch_status();
+}
+
+extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
+                              void* o, float* lse, int B, int H, int S, int D, int block, int topk,
+                              float scale, void* stream) {
+    if (!q || !k || !v || !idx || !o) return GBATTN_ERR_NULL;
+    if (B <= 0 || H <= 0 || S <= 0 || topk <= 0) return GBATTN_ERR_SHAPE;
+    if (D != 128 || block != 64) return GBATTN_ERR_UNSUPPORTED;
+    if (S % block != 0) return GBATTN_ERR_SHAPE;
+    const int nc = S / block;
+    if (topk > nc || topk > kMaxTopk) return GBATTN_ERR_SHAPE;
+    if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
+    if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return GBATTN_ERR_ALIGN;
+    const size_t xb = static_cast<size_t>(B) * H * S * D * 2;
+    const size_t ib = static_cast<size_t>(B) * H * nc * topk * 4;
+    const size_t lb = static_cast<size_t>(B) * H * S * 4;
+    if (overlaps(o, xb, q, xb) || overlaps(o, xb, k, xb) || overlaps(o, xb, v, xb) ||
+        overlaps(o, xb, idx, ib) || overlaps(lse, lb, q, xb) || overlaps(lse, lb, k, xb) ||
+        overlaps(lse, lb, v, xb) || overlaps(lse, lb, idx, ib) || overlaps(lse, lb, o, xb))
+        return GBATTN_ERR_ALIAS;
+    DeviceState dev;
+    int rc = current_device(&dev);
+    if (rc != GBATTN_OK) return rc;
+    AttnArgs a = base_args(dev, scale);
+    a.seq_q = S;
+    a.seq_k = S;
+    a.heads_q = B * H;
+    a.hq = H;
+    a.hkv = H;
+    a.n_chunks = 1;
+    a.n_cubes = nc;
+    a.topk = topk;
+    a.idx = idx;
+    a.o = static_cast<__half*>(o);
+    a.lse = lse;
+    dim3 grid((nc + 1) / 2, B * H);
+    return launch_attn<128, kSparse>(q, k, v, S, S, B * H, B * H, grid, a,
+                                     static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,167 @@
+// Paged FP8 E4M3 -> FP16 bridge ("Integrate FP32 v37 prefill and exact E4M3
+// bridge", Purpose and Implementation: exact E4M3 byte conversion with unit
+// and non-unit scales over the live length).
+//
+// Each thread turns 16 consecutive E4M3 bytes of one token into 16 FP16 values
+// (one 16-byte load, two 16-byte stores) for K and for V.  Decoding uses the
+// hardware e4m3x2 -> f16x2 conversion, which is exact (every finite E4M3 value
+// is an FP16 value).  The scaled result must be the FP16 value nearest to the
+// exact product, ties to even:
+//   * if the FP32 scale is itself an FP16 value, one IEEE FP16 multiply of two
+//     FP16 operands rounds the exact product once;
+//   * otherwise the product is formed in FP32 with round-to-odd (truncated
+//     product, sticky bit from the exact FMA residual) and rounded to FP16 once;
+//     FP32 carries 24 >= 11 + 2 significant bits, so the double rounding through
+//     round-to-odd equals a single rounding (Boldo and Melquiond, "Emulation of
+//     FMA and correctly rounded sums: proved algorithms using rounding to odd",
+//     IEEE Trans. Computers 57(4), 2008).
+#include <cuda_fp16.h>
+
+#include "host.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+    uint32_t out;
+    const uint16_t in = static_cast<uint16_t>(two_bytes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(in));
+    return out;
+}
+
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t h2, __half2 s2) {
+    __half2 x = *reinterpret_cast<__half2*>(&h2);
+    __half2 y = __hmul2(x, s2);
+    return *reinterpret_cast<uint32_t*>(&y);
+}
+
+__device__ __forceinline__ __half scale_round_to_odd(__half h, float s) {
+    const float x = __half2float(h);
+    float p = __fmul_rz(x, s);
+    const float r = __fmaf_rn(x, s, -p);
+    if (r != 0.0f) p = __uint_as_float(__float_as_uint(p) | 1u);
+    return __float2half_rn(p);
+}
+
+__device__ __forceinline__ uint32_t scale_f16x2_general(uint32_t h2, float s) {
+    __half2 x = *reinterpret_cast<__half2*>(&h2);
+    __half2 y = __halves2half2(scale_round_to_odd(__low2half(x), s),
+                               scale_round_to_odd(__high2half(x), s));
+    return *reinterpret_cast<uint32_t*>(&y);
+}
+
+template <bool kHalfScale>
+__device__ __forceinline__ void convert16(uint4 in, __half2 s2, float s, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+        o[2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        o[i] = kHalfScale ? scale_f16x2(o[i], s2) : scale_f16x2_general(o[i], s);
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <bool kHalfScale>
+__global__ void __launch_bounds__(256) e4m3_bridge_kernel(
+    const uint8_t* __restrict__ kp, const uint8_t* __restrict__ vp,
+    const int32_t* __restrict__ table, int num_phys, int page_size, int kv_len, int hkv, int D,
+    float ks, float vs, __half2 ks2, __half2 vs2, __half* __restrict__ ko,
+    __half* __restrict__ vo, uint32_t* status) {
+    const int chunks_per_row = D >> 4;                       // 16 bytes per chunk
+    const long long per_token = static_cast<long long>(hkv) * chunks_per_row;
+    const long long total = static_cast<long long>(kv_len) * per_token;
+    for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
+         g += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long t = g / per_token;
+        const int rem = static_cast<int>(g - t * per_token);
+        const int h = rem / chunks_per_row;
+        const int c = rem - h * chunks_per_row;
+        const int page = table[t / page_size];
+        const long long out_off =
+            (static_cast<long long>(h) * kv_len + t) * D + static_cast<long long>(c) * 16;
+        uint4 klo, khi, vlo, vhi;
+        if (page < 0 || page >= num_phys) {
+            if (c == 0 && h == 0 && (t % page_size) == 0) atomicOr(status, kDevBadPage);
+            klo = khi = vlo = vhi = make_uint4(0, 0, 0, 0);
+        } else {
+            const long long in_off =
+                ((static_cast<long long>(page) * page_size + (t % page_size)) * hkv + h) * D +
+                static_cast<long long>(c) * 16;
+            const uint4 kin = __ldcs(reinterpret_cast<const uint4*>(kp + in_off));
+            const uint4 vin = __ldcs(reinterpret_cast<const uint4*>(vp + in_off));
+            convert16<kHalfScale>(kin, ks2, ks, klo, khi);
+            convert16<kHalfScale>(vin, vs2, vs, vlo, vhi);
+        }
+        uint4* kdst = reinterpret_cast<uint4*>(ko + out_off);
+        uint4* vdst = reinterpret_cast<uint4*>(vo + out_off);
+        __stcs(kdst, klo);
+        __stcs(kdst + 1, khi);
+        __stcs(vdst, vlo);
+        __stcs(vdst + 1, vhi);
+    }
+}
+
+// True when the FP32 value s is exactly an FP16 value (normal or subnormal).
+bool is_fp16_value(float s) {
+    const __half h = __float2half_rn(s);
+    return __half2float(h) == s;
+}
+
+}  // namespace
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" int e4m3_paged_to_fp16(const uint8_t* k_pages, const uint8_t* v_pages,
+                                  const int32_t* page_table, int num_phys_pages, int page_size,
+                                  int kv_len, int Hkv, int D, float k_scale, float v_scale,
+                                  void* k_out, void* v_out, void* stream) {
+    if (!k_pages || !v_pages || !page_table || !k_out || !v_out) return GBATTN_ERR_NULL;
+    if (num_phys_pages <= 0 || page_size <= 0 || kv_len <= 0 || Hkv <= 0 || D <= 0)
+        return GBATTN_ERR_SHAPE;
+    if (D % 16 != 0) return GBATTN_ERR_UNSUPPORTED;
+    if (!finite_positive(k_scale) || !finite_positive(v_scale)) return GBATTN_ERR_SCALE;
+    if (!aligned16(k_pages) || !aligned16(v_pages) || !aligned16(k_out) || !aligned16(v_out) ||
+        (reinterpret_cast<uintptr_t>(page_table) & 3u))
+        return GBATTN_ERR_ALIGN;
+    const size_t in_bytes = static_cast<size_t>(num_phys_pages) * page_size * Hkv * D;
+    const size_t out_bytes = static_cast<size_t>(kv_len) * Hkv * D * 2;
+    const size_t tab_bytes = static_cast<size_t>((kv_len + page_size - 1) / page_size) * 4;
+    const void* outs[2] = {k_out, v_out};
+    for (const void* o : outs) {
+        if (overlaps(o, out_bytes, k_pages, in_bytes) || overlaps(o, out_bytes, v_pages, in_bytes) ||
+            overlaps(o, out_bytes, page_table, tab_bytes))
+            return GBATTN_ERR_ALIAS;
+    }
+    if (overlaps(k_out, out_bytes, v_out, out_bytes)) return GBATTN_ERR_ALIAS;
+
+    DeviceState dev;
+    int rc = current_device(&dev);
+    if (rc != GBATTN_OK) return rc;
+    const long long total = static_cast<long long>(kv_len) * Hkv * (D / 16);
+    const int threads = 256;
+    long long blocks = (total + threads - 1) / threads;
+    const long long cap = static_cast<long long>(dev.num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool half_scale = is_fp16_value(k_scale) && is_fp16_value(v_scale);
+    const __half2 ks2 = __float2half2_rn(k_scale), vs2 = __float2half2_rn(v_scale);
+    if (half_scale)
+        e4m3_bridge_kernel<true><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+            k_pages, v_pages, page_table, num_phys_pages, page_size, kv_len, Hkv, D, k_scale,
+            v_scale, ks2, vs2, static_cast<__half*>(k_out), static_cast<__half*>(v_out),
+            dev.status);
+    else
+        e4m3_bridge_kernel<false><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+            k_pages, v_pages, page_table, num_phys_pages, page_size, kv_len, Hkv, D, k_scale,
+            v_scale, ks2, vs2, static_cast<__half*>(k_out), static_cast<__half*>(v_out),
+            dev.status);
+    count_launches(1);
+    return launch_status();
+}

@@ -1,0 +1,196 @@
+// VSA key-cube selection ("Integrate H3 SM70 execution, metrics and VSA
+// diagnostics", Purpose: top-k = 64; FastVideo compare view,
+// minimax_h3_fusions/query_pool.py and key_quant.py: FP32 tile means = FP32 sum
+// divided by the token count).
+//
+// Two kernels:
+//  1. vsa_pool_kernel: FP32 cube means of Q and K.  Each thread owns 8
+//     consecutive channels of one cube and adds the cube's 64 tokens in token
+//     order with FP32 rounding after every addition, then divides by the count
+//     (correctly rounded).  HBM-bound: Q and K are read once with 16-byte loads.
+//  2. vsa_score_topk_kernel: one warp per query cube.  Scores against every key
+//     cube are FP32 sums over d = 0..D-1, in order, of FP32 products (no fused
+//     multiply-add, so both the product and the sum are rounded).  The k-th
+//     largest score is found with a 32-step bitwise search on order-preserving
+//     integer keys; equal scores at the threshold are taken from the lowest
+//     cube index up; the selection is written in ascending cube order.
+#include <cuda_fp16.h>
+
+#include "host.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+constexpr int kPoolThreads = 256;
+constexpr int kQueriesPerCta = 8;   // one warp per query cube
+constexpr int kKeyChunk = 32;       // key cubes staged in shared memory per step
+constexpr int kMaxChunks = 32;      // supports up to 1024 cubes per head
+
+__global__ void __launch_bounds__(kPoolThreads) vsa_pool_kernel(
+    const __half* __restrict__ q, const __half* __restrict__ k, long long n_cubes, int D,
+    int block, float* __restrict__ qm, float* __restrict__ km) {
+    const __half* x = blockIdx.y == 0 ? q : k;
+    float* out = blockIdx.y == 0 ? qm : km;
+    const int groups = D >> 3;   // 8 channels per thread
+    const long long gid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (gid >= n_cubes * groups) return;
+    const long long cube = gid / groups;
+    const int g = static_cast<int>(gid - cube * groups);
+    const __half* base = x + cube * block * D + g * 8;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll 8
+    for (int t = 0; t < block; ++t) {
+        const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(base + static_cast<long long>(t) * D));
+        const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(h[e]);
+            acc[2 * e] = __fadd_rn(acc[2 * e], f.x);
+            acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], f.y);
+        }
+    }
+    const float cnt = static_cast<float>(block);
+    float4 lo, hi;
+    lo.x = __fdiv_rn(acc[0], cnt); lo.y = __fdiv_rn(acc[1], cnt);
+    lo.z = __fdiv_rn(acc[2], cnt); lo.w = __fdiv_rn(acc[3], cnt);
+    hi.x = __fdiv_rn(acc[4], cnt); hi.y = __fdiv_rn(acc[5], cnt);
+    hi.z = __fdiv_rn(acc[6], cnt); hi.w = __fdiv_rn(acc[7], cnt);
+    float4* dst = reinterpret_cast<float4*>(out + cube * D + g * 8);
+    dst[0] = lo;
+    dst[1] = hi;
+}
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// grid: (ceil(NC / kQueriesPerCta), B*H); block: 32 * kQueriesPerCta; D == 128.
+__global__ void __launch_bounds__(32 * kQueriesPerCta) vsa_score_topk_kernel(
+    const float* __restrict__ qm, const float* __restrict__ km, int NC, int topk,
+    int32_t* __restrict__ idx) {
+    constexpr int D = 128;
+    __shared__ float sk[kKeyChunk][D + 1];     // +1 pad: lanes read distinct banks
+    __shared__ float sq[kQueriesPerCta][D];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y;
+    const int qc = blockIdx.x * kQueriesPerCta + warp;
+    const float* qbase = qm + static_cast<long long>(bh) * NC * D;
+    const float* kbase = km + static_cast<long long>(bh) * NC * D;
+    for (int i = threadIdx.x; i < kQueriesPerCta * D; i += blockDim.x) {
+        const int w = i / D, d = i % D;
+        const int c = blockIdx.x * kQueriesPerCta + w;
+        sq[w][d] = c < NC ? qbase[static_cast<long long>(c) * D + d] : 0.0f;
+    }
+    const int nchunks = (NC + kKeyChunk - 1) / kKeyChunk;
+    uint32_t key[kMaxChunks];
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) key[c] = 0u;   // 0 sorts below every real score
+
+#pragma unroll 1
+    for (int ch = 0; ch < nchunks; ++ch) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < kKeyChunk * D; i += blockDim.x) {
+            const int r = i / D, d = i % D;
+            const int kc = ch * kKeyChunk + r;
+            sk[r][d] = kc < NC ? kbase[static_cast<long long>(kc) * D + d] : 0.0f;
+        }
+        __syncthreads();
+        float acc = 0.0f;
+#pragma unroll 16
+        for (int d = 0; d < D; ++d) acc = __fadd_rn(acc, __fmul_rn(sq[warp][d], sk[lane][d]));
+        const uint32_t kk = (ch * kKeyChunk + lane < NC) ? order_key(acc) : 0u;
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c)
+            if (c == ch) key[c] = kk;
+    }
+    if (qc >= NC) return;
+
+    // Threshold: the largest T such that at least topk keys are >= T.
+    uint32_t T = 0;
+#pragma unroll 1
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = T | (1u << bit);
+        int cnt = 0;
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) cnt += (c < nchunks && key[c] >= cand) ? 1 : 0;
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        if (cnt >= topk) T = cand;
+    }
+    int greater = 0;
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) greater += (c < nchunks && key[c] > T) ? 1 : 0;
+    greater = __reduce_add_sync(0xffffffffu, greater);
+    int need = topk - greater;            // equal-to-threshold scores still to take
+
+    const uint32_t lt = (1u << lane) - 1u;
+    int32_t* out = idx + (static_cast<long long>(bh) * NC + qc) * topk;
+    int base = 0;
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+        if (c < nchunks) {
+            const bool valid = c * kKeyChunk + lane < NC;
+            const bool eq = valid && key[c] == T;
+            const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+            const int take = min(need, __popc(eqm));
+            const bool sel = valid && (key[c] > T || (eq && __popc(eqm & lt) < take));
+            need -= take;
+            const uint32_t selm = __ballot_sync(0xffffffffu, sel);
+            if (sel) out[base + __popc(selm & lt)] = c * kKeyChunk + lane;
+            base += __popc(selm);
+        }
+    }
+}
+
+}  // namespace
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" size_t vsa_select_workspace_size(int B, int H, int S, int D, int block) {
+    if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return 0;
+    const size_t nc = static_cast<size_t>(S / block);
+    return 2 * static_cast<size_t>(B) * H * nc * D * sizeof(float);
+}
+
+extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D,
+                                 int block, int topk, int32_t* idx, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    if (!q || !k || !idx) return GBATTN_ERR_NULL;
+    if (B <= 0 || H <= 0 || S <= 0 || topk <= 0) return GBATTN_ERR_SHAPE;
+    if (D != 128 || block != 64) return GBATTN_ERR_UNSUPPORTED;
+    if (S % block != 0) return GBATTN_ERR_SHAPE;
+    const int NC = S / block;
+    if (NC > kMaxChunks * kKeyChunk || topk > NC) return GBATTN_ERR_SHAPE;
+    if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
+    const size_t need = vsa_select_workspace_size(B, H, S, D, block);
+    if (!workspace || workspace_bytes < need) return GBATTN_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(idx) & 3u))
+        return GBATTN_ERR_ALIGN;
+    const size_t in_bytes = static_cast<size_t>(B) * H * S * D * 2;
+    const size_t idx_bytes = static_cast<size_t>(B) * H * NC * topk * 4;
+    if (overlaps(idx, idx_bytes, q, in_bytes) || overlaps(idx, idx_bytes, k, in_bytes) ||
+        overlaps(workspace, need, q, in_bytes) || overlaps(workspace, need, k, in_bytes) ||
+        overlaps(workspace, need, idx, idx_bytes))
+        return GBATTN_ERR_ALIAS;
+    DeviceState dev;
+    int rc = current_device(&dev);
+    if (rc != GBATTN_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* qm = static_cast<float*>(workspace);
+    float* km = qm + static_cast<size_t>(B) * H * NC * D;
+    const long long n_cubes = static_cast<long long>(B) * H * NC;
+    const long long pool_threads = n_cubes * (D / 8);
+    dim3 pgrid(static_cast<unsigned>((pool_threads + kPoolThreads - 1) / kPoolThreads), 2);
+    vsa_pool_kernel<<<pgrid, kPoolThreads, 0, s>>>(static_cast<const __half*>(q),
+                                                   static_cast<const __half*>(k), n_cubes, D,
+                                                   block, qm, km);
+    dim3 sgrid((NC + kQueriesPerCta - 1) / kQueriesPerCta, B * H);
+    vsa_score_topk_kernel<<<sgrid, 32 * kQueriesPerCta, 0, s>>>(qm, km, NC, topk, idx);
+    count_launches(2);
+    return launch_status();
+}

@@ -1,0 +1,547 @@
+"""Benchmark of the fused FP16 attention hot path on GB300.
+
+One step is one pass of the whole hot path over one batch of synthetic input,
+all three variants at full size:
+  * dense video attention      B1 H24 S32768 D128                (attn_dense_fwd)
+  * VSA                         B1 H24 S32768 D128, 512 cubes, top-64
+                                (vsa_select_blocks + vsa_sparse_fwd)
+  * paged E4M3 long prefill     Hq6 Hkv1 D256, Q=8192 after KV=131072
+                                (e4m3_paged_to_fp16 + attn_causal_prefill_fwd)
+The metric is useful attention TFLOP/s (4 * D * visible (query, key) pairs per
+head; VSA counts only the selected cubes) with the bridge's HBM GB/s beside it.
+Inputs are seeded synthetic data resident in HBM before the timed region; each
+step touches about 1.7 GB, more than the 129 MB L2, so no explicit L2 flush is
+done between steps.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+        [--workload all|dense_video|vsa_video|paged_e4m3|dense_small|causal_small]
+For N > 1 (torchrun, one process per GPU) every rank runs the same step on its
+own GPU (independent replicas, no data-path communication); the time is the
+maximum over ranks and the value counts the work of all ranks.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from attention_fp16_flashattention_gb300 import inputs  # noqa: E402
+
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ------------------------------------------------------------------ work model
+def dense_flops(B, H, Sq, Skv, D):
+    return 4.0 * B * H * Sq * Skv * D
+
+
+def causal_pairs(Q, KV):
+    prefix = KV - Q
+    return Q * prefix + Q * (Q + 1) // 2
+
+
+def causal_flops(B, Hq, Q, KV, D):
+    return 4.0 * D * B * Hq * causal_pairs(Q, KV)
+
+
+def vsa_flops(B, H, S, D, topk, block=64):
+    return 4.0 * B * H * S * topk * block * D
+
+
+def bridge_bytes(KV, Hkv, D, page_size):
+    n_pages = -(-KV // page_size)
+    return 2 * KV * Hkv * D + 4 * n_pages + 2 * 2 * KV * Hkv * D
+
+
+# ------------------------------------------------------------------ workloads on the GPU
+class Workload:
+    """Device-resident inputs and outputs of one sub-workload plus its calls."""
+
+    def __init__(self, name, gb, torch, dev, host_inputs):
+        self.name, self.gb, self.torch, self.dev = name, gb, torch, dev
+        w = inputs.WORKLOADS[name]
+        self.w = w
+        self.host = host_inputs
+        T = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        if w["kind"] == "dense":
+            self.q, self.k, self.v = (T(x) for x in host_inputs)
+            self.o = torch.empty_like(self.q)
+            self.flops = dense_flops(w["B"], w["H"], w["S"], w["S"], w["D"])
+        elif w["kind"] == "causal":
+            self.q, self.k, self.v = (T(x) for x in host_inputs)
+            self.o = torch.empty_like(self.q)
+            ws = gb.attn_causal_prefill_workspace_size(w["B"], w["Hq"], w["Q"], w["KV"], w["D"])
+            self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+            self.flops = causal_flops(w["B"], w["Hq"], w["Q"], w["KV"], w["D"])
+        elif w["kind"] == "vsa":
+            self.q, self.k, self.v = (T(x) for x in host_inputs)
+            S = self.q.shape[2]
+            nc = S // 64
+            self.idx = torch.empty((w["B"], w["H"], nc, w["topk"]), dtype=torch.int32, device=dev)
+            ws = gb.vsa_select_workspace_size(w["B"], w["H"], S, w["D"], 64)
+            self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+            self.o = torch.empty_like(self.q)
+            self.flops = vsa_flops(w["B"], w["H"], S, w["D"], w["topk"])
+        elif w["kind"] == "paged":
+            qh, kp, vp, table = host_inputs
+            self.q, self.kp, self.vp, self.table = T(qh), T(kp), T(vp), T(table)
+            self.kf = torch.empty((w["Hkv"], w["KV"], w["D"]), dtype=torch.float16, device=dev)
+            self.vf = torch.empty_like(self.kf)
+            self.o = torch.empty_like(self.q)
+            ws = gb.attn_causal_prefill_workspace_size(w["B"], w["Hq"], w["Q"], w["KV"], w["D"])
+            self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+            self.flops = causal_flops(w["B"], w["Hq"], w["Q"], w["KV"], w["D"])
+            self.bridge_bytes = bridge_bytes(w["KV"], w["Hkv"], w["D"], w["page_size"])
+
+    def calls(self):
+        """(label, fn) pairs in launch order; each fn queues GPU work on the current stream."""
+        gb, w = self.gb, self.w
+        if w["kind"] == "dense":
+            return [("attn_dense_fwd", lambda: gb.attn_dense_fwd(self.q, self.k, self.v, o=self.o))]
+        if w["kind"] == "causal":
+            return [("attn_causal_prefill_fwd",
+                     lambda: gb.attn_causal_prefill_fwd(self.q, self.k, self.v, o=self.o,
+                                                        workspace=self.ws))]
+        if w["kind"] == "vsa":
+            return [("vsa_select_blocks",
+                     lambda: gb.vsa_select_blocks(self.q, self.k, w["topk"], idx=self.idx,
+                                                  workspace=self.ws)),
+                    ("vsa_sparse_fwd",
+                     lambda: gb.vsa_sparse_fwd(self.q, self.k, self.v, self.idx, o=self.o))]
+        return [("e4m3_paged_to_fp16",
+                 lambda: gb.e4m3_paged_to_fp16(self.kp, self.vp, self.table, w["KV"], w["k_scale"],
+                                               w["v_scale"], k_out=self.kf, v_out=self.vf)),
+                ("attn_causal_prefill_fwd(paged)",
+                 lambda: gb.attn_causal_prefill_fwd(self.q, self.kf[None], self.vf[None], o=self.o,
+                                                    workspace=self.ws))]
+
+    # host <-> device traffic of the end-to-end variant
+    def h2d_pairs(self):
+        if self.w["kind"] == "paged":
+            return [(self.q, 0), (self.kp, 1), (self.vp, 2), (self.table, 3)]
+        return [(self.q, 0), (self.k, 1), (self.v, 2)]
+
+    def d2h(self):
+        out = [self.o]
+        if self.w["kind"] == "vsa":
+            out.append(self.idx)
+        return out
+
+
+def host_inputs(name):
+    w = inputs.WORKLOADS[name]
+    if w["kind"] == "dense":
+        return inputs.dense_inputs(w["B"], w["H"], w["S"], w["D"], w["seed"], video=w.get("video", False))
+    if w["kind"] == "causal":
+        return inputs.causal_inputs(w["B"], w["Hq"], w["Hkv"], w["Q"], w["KV"], w["D"], w["seed"])
+    if w["kind"] == "vsa":
+        return inputs.vsa_inputs(w["B"], w["H"], w["D"], w["seed"], w["grid"], w["cube"])
+    q = inputs.causal_inputs(w["B"], w["Hq"], w["Hkv"], w["Q"], 32, w["D"], w["seed"])[0]
+    kp, vp, table = inputs.paged_e4m3_inputs(w["Hkv"], w["KV"], w["D"], w["seed"], w["page_size"])
+    return q, kp, vp, table
+
+
+# ------------------------------------------------------------------ clocks
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv") \
+            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/gbattn_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in loaded),
+                "samples": len(loaded), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=p["hbm_gbs"], tc=p.get("bf16_tflops"), tc_sust=p.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sust=1700.0, src="fallback")
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_fp16_flashattention_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch from the committed ncu capture, if the sources are unchanged."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    t = json.load(open(PROFILE_TRAFFIC))
+    e = t.get(kernel)
+    if not e or e.get("source_sha") != source_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def physical_gpu_index(local):
+    """nvidia-smi index of this process's GPU (CUDA_VISIBLE_DEVICES maps local ordinals)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local < len(ids) and ids[local].isdigit():
+            return int(ids[local])
+    return local
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        import torch
+        if not torch.cuda.is_available():
+            backend = "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(value, world, device=None):
+    """Maximum of a float over all ranks (host-side bookkeeping only)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle timing (CPU)
+def oracle_sample(names, budget_s=20.0):
+    """Time the CPU oracle on a bounded sample of every sub-workload (rows of the
+    attention outputs; the selection and bridge are not part of the TFLOP/s figure).
+    Returns (useful_flops_done, seconds, description)."""
+    from oracle import attention as OA
+    from oracle import e4m3 as OE
+    from oracle import vsa as OV
+    done = 0.0
+    secs = 0.0
+    desc = []
+    share = budget_s / max(1, len(names))
+    for name in names:
+        w = inputs.WORKLOADS[name]
+        data = host_inputs(name)
+        rows_done = 0
+        t_used = 0.0
+        n = 16
+        while t_used < share:
+            if w["kind"] == "dense":
+                q, k, v = data
+                rows = inputs.sample_rows(w["B"] * w["H"], w["S"], n, seed=9000 + rows_done)
+                t0 = time.perf_counter()
+                OA.dense_attention(q, k, v, inputs.softmax_scale(w["D"]), rows=rows)
+                t_used += time.perf_counter() - t0
+                done += n * 4.0 * w["S"] * w["D"]
+            elif w["kind"] == "vsa":
+                q, k, v = data
+                if rows_done == 0:
+                    t0 = time.perf_counter()
+                    idx = OV.vsa_select(q, k, 64, w["topk"])
+                    t_used += time.perf_counter() - t0
+                rows = inputs.sample_rows(w["B"] * w["H"], q.shape[2], n, seed=9000 + rows_done)
+                t0 = time.perf_counter()
+                OA.vsa_sparse_attention(q, k, v, idx, 64, inputs.softmax_scale(w["D"]), rows=rows)
+                t_used += time.perf_counter() - t0
+                done += n * 4.0 * w["topk"] * 64 * w["D"]
+            elif w["kind"] in ("paged", "causal"):
+                if w["kind"] == "paged":
+                    q, kp, vp, table = data
+                    if rows_done == 0:
+                        t0 = time.perf_counter()
+                        kb, vb = OE.paged_e4m3_to_fp16(kp, vp, table, w["KV"], w["k_scale"],
+                                                       w["v_scale"])
+                        k, v = kb.view(np.float16)[None], vb.view(np.float16)[None]
+                        t_used += time.perf_counter() - t0
+                else:
+                    q, k, v = data
+                rows = inputs.sample_rows(w["B"] * w["Hq"], w["Q"], n, seed=9000 + rows_done)
+                t0 = time.perf_counter()
+                OA.causal_prefill_attention(q, k, v, inputs.softmax_scale(w["D"]), w["Q"], rows=rows)
+                t_used += time.perf_counter() - t0
+                prefix = w["KV"] - w["Q"]
+                done += 4.0 * w["D"] * float(np.sum(prefix + rows[:, 1] + 1))
+            rows_done += n
+            n = min(n * 2, 256)
+        secs += t_used
+        desc.append(f"{name}: {rows_done} sampled rows")
+    return done, secs, "; ".join(desc)
+
+
+# ------------------------------------------------------------------ main
+def run_reference(args, names, world, rank):
+    """The oracle as it stands, on the host cores, same metric and config."""
+    if rank != 0:
+        return 0
+    per_step = []
+    done_total = 0.0
+    for _ in range(args.warmup):
+        oracle_sample(names, budget_s=2.0)
+    desc = ""
+    for _ in range(args.steps):
+        done, secs, desc = oracle_sample(names, budget_s=args.ref_budget)
+        per_step.append((done, secs))
+        done_total += done
+    tflops = sum(d for d, _ in per_step) / sum(s for _, s in per_step) / 1e12
+    ms = 1e3 * sum(s for _, s in per_step) / len(per_step)
+    line = {"metric": "attention useful TFLOP/s", "value": tflops, "unit": "TFLOP/s",
+            "impl": "reference", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "+".join(names), "timing": "host wall clock, oracle on CPU"},
+            "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="all")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    names = ["dense_video", "vsa_video", "paged_e4m3"] if args.workload == "all" else \
+        args.workload.split(",")
+
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        r = run_reference(args, names, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return r
+
+    import torch
+    import attention_fp16_flashattention_gb300 as gb
+    from attention_fp16_flashattention_gb300 import build as gbuild
+    if not gbuild.up_to_date() and rank == 0:
+        gbuild.build()
+    barrier(world)
+    gb.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    hosts = {n: host_inputs(n) for n in names}
+    wls = [Workload(n, gb, torch, dev, hosts[n]) for n in names]
+    calls = [(w, lbl, fn) for w in wls for lbl, fn in w.calls()]
+
+    def step():
+        for _, _, fn in calls:
+            fn()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if gb.device_status() != 0:
+        raise RuntimeError("device status flags set during warm-up")
+
+    # ---- timed region: device time with per-call events on the launching stream
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(physical_gpu_index(local))
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = gb.launch_count()
+    start.record(stream)
+    for s in range(args.steps):
+        for c, (_, _, fn) in enumerate(calls):
+            ev[s][c][0].record(stream)
+            fn()
+            ev[s][c][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    launches = (gb.launch_count() - launches0) // args.steps
+    clock_info = clocks.stop()
+    barrier(world, dev)
+    local_ms = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(local_ms, world, dev)
+    if gb.device_status() != 0:
+        raise RuntimeError("device status flags set during the timed region")
+
+    per_call = {}
+    for c, (w, lbl, _) in enumerate(calls):
+        t = [ev[s][c][0].elapsed_time(ev[s][c][1]) for s in range(args.steps)]
+        per_call[f"{w.name}:{lbl}"] = statistics.median(t)
+
+    flops_step = sum(w.flops for w in wls)
+    value = world * flops_step / (ms * 1e-3) / 1e12
+    pk = peaks()
+
+    # ---- dominant kernel roofline
+    attn_calls = {k: v for k, v in per_call.items() if "select" not in k and "e4m3_paged" not in k}
+    dom = max(attn_calls, key=attn_calls.get)
+    dom_w = next(w for w in wls if dom.startswith(w.name + ":"))
+    achieved = dom_w.flops / (attn_calls[dom] * 1e-3) / 1e12
+    kernel_name = {"dense": "attn_fwd_kernel<128,dense>", "vsa": "attn_fwd_kernel<128,sparse>",
+                   "paged": "attn_fwd_kernel<256,causal>+merge",
+                   "causal": "attn_fwd_kernel<256,causal>+merge"}[dom_w.w["kind"]]
+    peak_tc = pk["tc_sust"] or pk["tc"]
+    roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": achieved, "peak": peak_tc,
+                "unit": "TFLOP/s", "frac": achieved / peak_tc,
+                "peak_source": f"{pk['src']} bf16 sustained (fp16 dense rate = bf16 rate)",
+                "traffic": traffic_for(kernel_name)}
+    extra = {}
+    for w in wls:
+        if w.w["kind"] == "paged":
+            t = per_call[f"{w.name}:e4m3_paged_to_fp16"]
+            gbs = w.bridge_bytes / (t * 1e-3) / 1e9
+            extra["bridge"] = {"achieved": gbs, "unit": "GB/s", "peak": pk["hbm"],
+                               "frac": gbs / pk["hbm"], "bytes_per_launch": w.bridge_bytes,
+                               "traffic": traffic_for("e4m3_bridge_kernel")}
+    per_variant = {}
+    for w in wls:
+        t = sum(v for k, v in per_call.items() if k.startswith(w.name + ":"))
+        per_variant[w.name] = {"ms": t, "tflops": w.flops / (t * 1e-3) / 1e12}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pinned = {}
+        h2d = 0
+        d2h = 0
+        for w in wls:
+            for dtens, i in w.h2d_pairs():
+                hsrc = np.ascontiguousarray(w.host[i])
+                p = torch.from_numpy(hsrc).pin_memory()
+                pinned[(w.name, i)] = (p, dtens)
+                h2d += p.numel() * p.element_size()
+            for o in w.d2h():
+                pinned[(w.name, "out", id(o))] = (torch.empty(o.shape, dtype=o.dtype, pin_memory=True), o)
+                d2h += o.numel() * o.element_size()
+        outs = [(h, d) for k, (h, d) in pinned.items() if k[1] == "out"]
+        ins = [(h, d) for k, (h, d) in pinned.items() if k[1] != "out"]
+
+        def e2e_step():
+            for h, d in ins:
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in outs:
+                h.copy_(d, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, args.steps // 3)
+        barrier(world, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        e2e = {"value": world * flops_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        done, secs, desc = oracle_sample(names, budget_s=args.ref_budget)
+        cpu = {"value": done / secs / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": desc + f" ({secs:.1f} s of CPU time, numpy float64)"}
+
+    if rank == 0:
+        line = {"metric": "attention useful TFLOP/s", "value": value, "unit": "TFLOP/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+                "data": "synthetic",
+                "config": {"workload": "+".join(names),
+                           "shapes": {n: {k: v for k, v in inputs.WORKLOADS[n].items() if k != "seed"}
+                                      for n in names},
+                           "parallelism": "replicas" if world > 1 else "single_gpu",
+                           "l2": "inputs larger than L2 (about 1.7 GB touched per step), no flush"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clock_info, "per_call_ms": per_call, "per_variant": per_variant}
+        line.update(extra)
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,177 @@
+/*
+ * gbattn — fused FP16 attention for one NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * The library computes O = softmax(scale * Q K^T + mask) V with FP16 storage,
+ * FP32 accumulation of Q K^T and P V, an FP32 online-softmax state and FP16
+ * probabilities ("Integrate FP32 v37 prefill and exact E4M3 bridge",
+ * Implementation: FP32 QK/PV accumulation and prefix/tail state, probabilities
+ * and final output stored as FP16), in three variants:
+ *   - dense non-causal heads of width 128 (the video-DiT attention of "Share
+ *     SM70 projection, attention and row reduction paths", Purpose);
+ *   - causal long prefill with shared-KV heads at width 256, the query block
+ *     appended after a key prefix, optionally fed from a paged E4M3 cache
+ *     through an exact E4M3 -> FP16 bridge ("Integrate FP32 v37 prefill and
+ *     exact E4M3 bridge", Implementation);
+ *   - VSA block-sparse attention: 64-token cubes, mean-pooled cube scores pick
+ *     the top-k key cubes of every query cube, then attention runs over only
+ *     those cubes ("Integrate H3 SM70 execution, metrics and VSA diagnostics",
+ *     Purpose: top-k = 64).
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *     library allocates no memory; scratch space is passed in as
+ *     `workspace`, sized by the matching *_workspace_size() query.
+ *   - Tensors are dense, row-major, in the layout each call states, with
+ *     16-byte aligned base addresses.
+ *   - `stream` is a cudaStream_t passed as void*; all GPU work is queued on it
+ *     and the call returns without waiting.  Inputs must stay unchanged and
+ *     outputs unread until that work completes.
+ *   - Every call returns a status (enum gbattn_status).  Arguments are
+ *     validated before anything is queued; on a validation error nothing is
+ *     written.  An output range that overlaps an input range is rejected.
+ *   - Errors found by a kernel while it runs (a pipeline wait that passed its
+ *     time limit, a page-table entry or a cube index out of range) are
+ *     recorded as bits in a per-device status word, read and cleared with
+ *     gbattn_device_status().
+ */
+#ifndef GBATTN_H
+#define GBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum gbattn_status {
+    GBATTN_OK = 0,
+    GBATTN_ERR_NULL = 1,        /* a required pointer is NULL */
+    GBATTN_ERR_SHAPE = 2,       /* a size is out of range or inconsistent */
+    GBATTN_ERR_UNSUPPORTED = 3, /* a valid but unsupported configuration (e.g. head width) */
+    GBATTN_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+    GBATTN_ERR_ALIAS = 5,       /* an output overlaps an input */
+    GBATTN_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than required */
+    GBATTN_ERR_CUDA = 7,        /* a CUDA runtime call failed (no device, launch error) */
+    GBATTN_ERR_SCALE = 8        /* a scale is not a finite positive number */
+};
+
+/* Bits of the per-device status word written by running kernels. */
+enum gbattn_device_flag {
+    GBATTN_DEV_WAIT_TIMEOUT = 1u, /* an in-kernel pipeline wait exceeded its limit; the
+                                     kernel stopped early and its output is invalid */
+    GBATTN_DEV_BAD_PAGE = 2u,     /* a page-table entry was outside [0, num_phys_pages);
+                                     that page's tokens were written as zeros */
+    GBATTN_DEV_BAD_INDEX = 4u     /* a VSA cube list was not strictly ascending or held an
+                                     index outside [0, S/block); the entry was skipped */
+};
+
+/* Library version (major*10000 + minor*100 + patch). */
+int gbattn_version(void);
+
+/* Human-readable text for a gbattn_status value; never NULL. */
+const char* gbattn_status_string(int status);
+
+/* Reads and clears the status word of the current device.  Waits for all work
+ * queued on `stream` first.  *flags_out receives the OR of gbattn_device_flag
+ * bits seen since the previous read.  Returns GBATTN_OK or GBATTN_ERR_CUDA. */
+int gbattn_device_status(void* stream, uint32_t* flags_out);
+
+/* Upper bound, in nanoseconds, of every in-kernel wait of the attention kernels
+ * (default 2e9).  A wait that passes it sets GBATTN_DEV_WAIT_TIMEOUT and the kernel
+ * returns instead of hanging.  Affects launches made after the call. */
+int gbattn_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Number of kernels this library has launched since it was loaded (all devices). */
+uint64_t gbattn_launch_count(void);
+
+/*
+ * Dense non-causal attention, head width D == 128.
+ * Cites: "Share SM70 projection, attention and row reduction paths", Purpose
+ * (D128 attention interfaces); FastVideo compare view, minimax_h3_prefix.cu
+ * (BHSD operands, contiguous 128-wide heads, LSE output).
+ *   q, o : [B][H][Sq][D]  FP16     k, v : [B][H][Skv][D] FP16
+ *   lse  : optional [B][H][Sq] FP32, natural-log sum of exp of the scaled scores
+ *   scale: finite, > 0 (typically 1/sqrt(D))
+ * Sizes: B, H, Sq, Skv >= 1; B*H <= 65535; Sq, Skv < 2^31.
+ */
+int attn_dense_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int Sq, int Skv, int D, float scale, void* stream);
+
+/*
+ * Causal prefill with shared-KV heads, head width D == 256.
+ * Cites: "Integrate FP32 v37 prefill and exact E4M3 bridge", Implementation
+ * (causal D256 Hq6/Hkv1, queries in multiples of 64, Q < KV, KV a multiple of
+ * 32, real-query causal offsets kept when queries are padded, FP32 prefix/tail
+ * state and final merge, bounded workspace).
+ *   q, o : [B][Hq][Q_pad][D] FP16   k, v : [B][Hkv][KV][D] FP16   lse: optional [B][Hq][Q_pad]
+ *   Query head h reads KV head h / (Hq/Hkv).  Query i < Q_real sits at absolute
+ *   position KV - Q_real + i and sees keys j <= that position.  Rows i >= Q_real
+ *   are written as zeros (lse = -inf).
+ *   Q_pad % 64 == 0, 1 <= Q_real <= Q_pad, Q_real <= KV, KV % 32 == 0, Hq % Hkv == 0.
+ *   The key range of every query tile is split into chunks processed by
+ *   separate CTAs; their FP32 partial outputs and log-sum-exps go to
+ *   `workspace` and a merge kernel combines them.  A workspace smaller than
+ *   attn_causal_prefill_workspace_size() makes the call use fewer chunks
+ *   (down to one, which needs no workspace); NULL with 0 bytes is allowed.
+ */
+size_t attn_causal_prefill_workspace_size(int B, int Hq, int Q_pad, int KV, int D);
+int attn_causal_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int Q_pad, int Q_real, int KV, int D,
+                            float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Paged FP8 E4M3 ("fn" flavour) -> FP16 bridge.
+ * Cites: "Integrate FP32 v37 prefill and exact E4M3 bridge", Purpose and
+ * Implementation (exact E4M3 byte conversion, unit and non-unit scales, live
+ * length); FastVideo compare view, minimax_h3_swiglu_quant.cuh scale_float
+ * (exact E4M3 bit construction).
+ *   k_pages, v_pages : [num_phys_pages][page_size][Hkv][D] bytes
+ *   page_table       : int32 [ceil(kv_len / page_size)], logical page -> physical page
+ *   k_out, v_out     : [Hkv][kv_len][D] FP16 (the K/V input of attn_causal_prefill_fwd, B = 1)
+ *   out = FP16 nearest to decode(byte) * scale, ties to even (one rounding).
+ *   Only tokens t < kv_len are read and written.  D % 16 == 0.  Scales finite, > 0.
+ *   An out-of-range page-table entry sets GBATTN_DEV_BAD_PAGE and writes that
+ *   page's tokens as zeros.
+ */
+int e4m3_paged_to_fp16(const uint8_t* k_pages, const uint8_t* v_pages, const int32_t* page_table,
+                       int num_phys_pages, int page_size, int kv_len, int Hkv, int D,
+                       float k_scale, float v_scale, void* k_out, void* v_out, void* stream);
+
+/*
+ * VSA key-cube selection.
+ * Cites: "Integrate H3 SM70 execution, metrics and VSA diagnostics", Purpose
+ * (top-k = 64); FastVideo compare view, minimax_h3_fusions/query_pool.py and
+ * key_quant.py (FP32 tile means: FP32 sum divided by the count, 64-token tiles),
+ * block_lists.py (per-query-block key-block lists).
+ *   q, k : [B][H][S][D] FP16 in cube-major order (cube c = tokens c*block .. c*block+block-1)
+ *   idx  : int32 [B][H][S/block][topk], for every query cube the topk key cubes with the
+ *          largest score, ties to the lower cube index, in ascending cube order.
+ *   Pooled vector = FP32 sum over the cube's tokens in token order / block (FP32, RN).
+ *   Score = FP32 sum over d = 0..D-1, in order, of FP32 products (no fused multiply-add).
+ *   block == 64, D == 128, S % block == 0, 1 <= topk <= S/block <= 1024.
+ */
+size_t vsa_select_workspace_size(int B, int H, int S, int D, int block);
+int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D, int block,
+                      int topk, int32_t* idx, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
+ * VSA block-sparse attention over the selected key cubes.
+ * Cites: "Integrate H3 SM70 execution, metrics and VSA diagnostics", Purpose;
+ * FastVideo compare view, block_lists.py (two 64-token query halves against two
+ * 64-token key halves per 128x128 block, with a 4-bit quadrant mask).
+ *   q, k, v, o : [B][H][S][D] FP16 cube-major; idx: int32 [B][H][S/block][topk]
+ *   strictly ascending per row; lse optional [B][H][S].
+ *   Query token i attends exactly the tokens of cubes idx[b][h][i / block][*].
+ *   block == 64, D == 128, S % block == 0, 1 <= topk <= min(S/block, 512).
+ */
+int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx, void* o,
+                   float* lse, int B, int H, int S, int D, int block, int topk, float scale,
+                   void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H */

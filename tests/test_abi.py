@@ -1,0 +1,143 @@
+"""The C-ABI library builds, loads and rejects bad arguments (CPU only).
+
+Every function declared in include/gbattn.h must be exported by
+libgbattn.so.  Argument validation runs before any CUDA call, so the error
+paths can be exercised on a machine without a GPU; with valid arguments and
+no device the calls return GBATTN_ERR_CUDA instead of crashing.
+"""
+
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbattn.h")
+
+OK, NULL, SHAPE, UNSUPPORTED, ALIGN, ALIAS, WORKSPACE, CUDA, SCALE = range(9)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from attention_fp16_flashattention_gb300 import build
+    build.build()
+    import attention_fp16_flashattention_gb300 as gb
+    return gb.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_0-9]+)\s*\(", text)) - {"if", "sizeof"})
+
+
+def test_header_declares_the_five_entry_points():
+    names = _declared_functions()
+    for n in ("attn_dense_fwd", "attn_causal_prefill_fwd", "e4m3_paged_to_fp16",
+              "vsa_select_blocks", "vsa_sparse_fwd"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert lib.gbattn_version() >= 100
+    for s in range(9):
+        assert lib.gbattn_status_string(s)
+    assert lib.gbattn_status_string(99) == b"unknown status"
+
+
+P = ctypes.c_void_p(0x10000)      # aligned fake device addresses: never dereferenced
+P2 = ctypes.c_void_p(0x20000000)
+P3 = ctypes.c_void_p(0x40000000)
+P4 = ctypes.c_void_p(0x60000000)
+MIS = ctypes.c_void_p(0x10008)    # 8-byte aligned only
+
+
+def test_dense_validation(lib):
+    f = lib.attn_dense_fwd
+    assert f(None, P2, P3, P4, None, 1, 1, 128, 128, 128, 0.1, None) == NULL
+    assert f(P, P2, P3, P4, None, 0, 1, 128, 128, 128, 0.1, None) == SHAPE
+    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 64, 0.1, None) == UNSUPPORTED
+    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 128, 0.0, None) == SCALE
+    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 128, float("nan"), None) == SCALE
+    assert f(MIS, P2, P3, P4, None, 1, 1, 128, 128, 128, 0.1, None) == ALIGN
+    assert f(P, P2, P3, P, None, 1, 1, 128, 128, 128, 0.1, None) == ALIAS
+    assert f(P, P2, P3, ctypes.c_void_p(0x10000 + 4096), None, 1, 1, 128, 128, 128, 0.1,
+             None) == ALIAS
+    assert f(P, P2, P3, P4, None, 256, 256, 128, 128, 128, 0.1, None) == SHAPE
+    # valid arguments, no GPU here -> CUDA error, not a crash
+    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 128, 0.1, None) in (CUDA, OK)
+
+
+def test_causal_validation(lib):
+    f = lib.attn_causal_prefill_fwd
+    args = lambda **kw: dict(dict(B=1, Hq=6, Hkv=1, Qp=1024, Qr=1024, KV=4096, D=256), **kw)
+
+    def call(q=P, o=P4, ws=None, wsb=0, **kw):
+        a = args(**kw)
+        return f(q, P2, P3, o, None, a["B"], a["Hq"], a["Hkv"], a["Qp"], a["Qr"], a["KV"], a["D"],
+                 0.0625, ws, wsb, None)
+    assert call(q=None) == NULL
+    assert call(Hq=5, Hkv=2) == SHAPE             # Hq % Hkv
+    assert call(Qp=1000, Qr=1000) == SHAPE        # Q_pad % 64
+    assert call(Qr=0) == SHAPE
+    assert call(Qr=1025) == SHAPE                 # Q_real > Q_pad
+    assert call(KV=4020) == SHAPE                 # KV % 32
+    assert call(Qp=8192, Qr=8192, KV=4096) == SHAPE   # Q_real > KV
+    assert call(D=128) == UNSUPPORTED
+    assert call(o=P) == ALIAS
+    assert call() in (CUDA, OK)
+
+
+def test_bridge_validation(lib):
+    f = lib.e4m3_paged_to_fp16
+    base = [P, P2, P3, 4, 32, 100, 1, 256, 0.0625, 0.125, P4, ctypes.c_void_p(0x70000000), None]
+
+    def call(i=None, v=None):
+        a = list(base)
+        if i is not None:
+            a[i] = v
+        return f(*a)
+    assert call(0, None) == NULL
+    assert call(5, 0) == SHAPE
+    assert call(7, 24) == UNSUPPORTED
+    assert call(8, -1.0) == SCALE
+    assert call(9, float("inf")) == SCALE
+    assert call(10, MIS) == ALIGN
+    assert call(10, P) == ALIAS
+    assert call(11, P4) == ALIAS
+    assert call() in (CUDA, OK)
+
+
+def test_select_and_sparse_validation(lib):
+    ws = lib.vsa_select_workspace_size(1, 24, 32768, 128, 64)
+    assert ws == 2 * 24 * 512 * 128 * 4
+    f = lib.vsa_select_blocks
+    assert f(P, P2, 1, 24, 32768, 128, 64, 64, P3, P4, ws - 1, None) == WORKSPACE
+    assert f(P, P2, 1, 24, 32768, 128, 32, 64, P3, P4, ws, None) == UNSUPPORTED
+    assert f(P, P2, 1, 24, 32768, 128, 64, 513, P3, P4, ws, None) == SHAPE
+    assert f(P, P2, 1, 24, 32768 + 32, 128, 64, 64, P3, P4, ws, None) == SHAPE
+    assert f(P, P2, 1, 24, 32768, 128, 64, 64, P3, P4, ws, None) in (CUDA, OK)
+    g = lib.vsa_sparse_fwd
+    assert g(P, P2, P3, P4, None, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == NULL
+    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), P, None, 1, 24, 32768, 128, 64, 64, 0.08,
+             None) == ALIAS
+    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), P4, None, 1, 24, 32768, 128, 64, 600, 0.08,
+             None) == SHAPE
+
+
+def test_product_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "attention_fp16_flashattention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith(".py"):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), fn
