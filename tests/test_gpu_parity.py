@@ -150,6 +150,26 @@ def test_dense_video_sampled(gb):
 
 
 # ------------------------------------------------------------------ causal
+def assert_close_fp16_p(got, ref, abs_weighted_v, what, max_frac_over_stated=1e-4):
+    """Stated tolerance plus the rounding bound of FP16 probabilities.
+
+    The pages store P in FP16 ("probabilities ... retain FP16 storage"), so each
+    weight carries a relative rounding error up to 2^-11 and an output element
+    can move by up to 2^-11 * sum_j w_j |v_j| (abs_weighted_v, the oracle
+    evaluated with |V|).  With E4M3 values scaled to |v| <= 56 that term
+    exceeds the 2e-3 absolute part of the stated tolerance in rows whose
+    output cancels.  Every element must meet the stated tolerance widened by
+    that term, and only a tiny fraction may exceed the stated one.
+    """
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - ref)
+    stated = ATOL + RTOL * np.abs(ref)
+    widened = stated + 2.0 ** -11 * abs_weighted_v
+    assert np.all(err <= widened), f"{what}: {(err > widened).sum()} outside the FP16-P bound"
+    frac = float((err > stated).mean())
+    assert frac <= max_frac_over_stated, f"{what}: {frac:.2e} of elements above the stated bound"
+
+
 def _causal_check(gb, B, Hq, Hkv, Qp, q_real, KV, seed, workspace=None, rows=None):
     q, k, v = inputs.causal_inputs(B, Hq, Hkv, Qp, KV, 256, seed)
     lse = torch.empty((B, Hq, Qp), dtype=torch.float32, device=DEV)
@@ -204,7 +224,9 @@ def test_paged_e4m3_prefill_sampled(gb):
     v16 = rv.view(np.float16)[None]
     rows = inputs.sample_rows(w["B"] * w["Hq"], w["Q"], 4096, seed=7005)
     ro, _ = OA.causal_prefill_attention(q, k16, v16, inputs.softmax_scale(w["D"]), w["Q"], rows=rows)
-    assert_close(rows_of(o, rows), ro, "paged_e4m3 prefill")
+    rabs, _ = OA.causal_prefill_attention(q, k16, np.abs(v16), inputs.softmax_scale(w["D"]), w["Q"],
+                                          rows=rows)
+    assert_close_fp16_p(rows_of(o, rows), ro, rabs, "paged_e4m3 prefill")
     assert gb.device_status() == 0
 
 
