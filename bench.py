@@ -379,7 +379,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=20.0)
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override the head count of the dense/VSA workloads (profiling runs)")
     args = ap.parse_args()
+    if args.heads > 0:
+        for n in ("dense_video", "vsa_video"):
+            inputs.WORKLOADS[n] = dict(inputs.WORKLOADS[n], H=args.heads)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     names = ["dense_video", "vsa_video", "paged_e4m3"] if args.workload == "all" else \
