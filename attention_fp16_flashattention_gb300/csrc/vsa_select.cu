@@ -16,6 +16,8 @@
 //     cube index up; the selection is written in ascending cube order.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "host.h"
 #include "ptx.cuh"
 
@@ -193,4 +195,61 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     vsa_score_topk_kernel<<<sgrid, 32 * kQueriesPerCta, 0, s>>>(qm, km, NC, topk, idx);
     count_launches(2);
     return launch_status();
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+//
+// Some callers cannot allocate device memory when they call this library: a
+// plugin inside a host program that fixed its memory budget at start-up and
+// forbids later allocations, code whose device memory is entirely owned by a
+// pool it cannot reach from here, or a latency-critical loop in which a
+// cudaMalloc (which may synchronise the device) is not acceptable.  For them,
+// vsa_select_blocks_noalloc runs the same selection with its scratch (the FP32
+// pooled cube means) in a fixed array of kNoAllocScratchBytes that lives in
+// this library's device image.  Every GPU that loads the library holds the
+// array until the process exits.
+namespace {
+constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
+
+static __device__ __align__(256) unsigned char g_select_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};
+
+// Device address of g_select_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address must come from
+// cudaGetSymbolAddress, once per device, with that device current.
+int scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return GBATTN_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return GBATTN_ERR_CUDA;
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return GBATTN_OK;
+}
+}  // namespace
+
+extern "C" int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S, int D,
+                                         int block, int topk, int32_t* idx, void* stream) {
+    if (!q || !k || !idx) return GBATTN_ERR_NULL;
+    if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return GBATTN_ERR_SHAPE;
+    const size_t need = vsa_select_workspace_size(B, H, S, D, block);
+    if (need > kNoAllocScratchBytes) return GBATTN_ERR_WORKSPACE;   // sizes beyond the fixed scratch
+    void* scratch = nullptr;
+    const int rc = scratch_address(&scratch);
+    if (rc != GBATTN_OK) return rc;
+    // The pool kernel overwrites every scratch byte it later reads, so the
+    // previous call's contents need no clearing.
+    return vsa_select_blocks(q, k, B, H, S, D, block, topk, idx, scratch, kNoAllocScratchBytes,
+                             stream);
 }

@@ -157,6 +157,33 @@ int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D, 
                       void* stream);
 
 /*
+ * vsa_select_blocks for callers that cannot allocate device memory.  The pages
+ * have no counterpart; this entry point exists for callers such as a plugin
+ * whose host program fixed its memory at start-up and forbids later
+ * allocations, code whose device memory is owned by a pool it cannot reach, or
+ * a latency-critical loop where a cudaMalloc (which may synchronise the
+ * device) is not acceptable.  It computes exactly what vsa_select_blocks
+ * computes, with the scratch (the FP32 pooled cube means, 2*B*H*(S/block)*D*4
+ * bytes) taken from a fixed 16 MiB array inside the library, which every GPU
+ * that loads the library keeps until the process exits.
+ *   - Sizes whose scratch exceeds 16 MiB are rejected with GBATTN_ERR_WORKSPACE
+ *     before anything is queued (at D=128, block=64: B*H*S <= 262144 tokens,
+ *     e.g. B=1, H=8, S=32768).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - The library allocates nothing here, and the caller does not allocate
+ *     either: only inputs and outputs are passed.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls whose GPU work overlaps in
+ *     time on one device (for example on two streams) race on it: order them
+ *     on one stream or synchronise between them.
+ */
+#define GBATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S, int D, int block,
+                              int topk, int32_t* idx, void* stream);
+
+/*
  * VSA block-sparse attention over the selected key cubes.
  * Cites: "Integrate H3 SM70 execution, metrics and VSA diagnostics", Purpose;
  * FastVideo compare view, block_lists.py (two 64-token query halves against two
