@@ -10,17 +10,20 @@
 // two-key-half blocks with a 4-bit quadrant mask of block_lists.py in the
 // FastVideo compare view).
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer: Q once, then K and V tiles through an NS-slot ring
 //               in the order the MMA warp consumes them (K0, K1, V0, K2, V1, ...).
 //   warp 1      allocates tensor memory; one lane issues every tcgen05.mma:
 //               S = Q K_j^T (SMEM x SMEM), then O += P_j V_j (P from TMEM).
 //               S_{j+1} is computed while the softmax warps work on tile j.
-//   warps 2..5  softmax: one query row per thread (TMEM lane = row); row max,
-//               exp2, row sum, P -> FP16 into TMEM; lazy O rescaling (only when
-//               the running max grows by more than 2^8); epilogue O / l.
-// Tensor memory (512 columns): S [0,128) FP32, P double buffer [128,192) and
-// [192,256) (FP16 pairs), O [256, 256 + D) FP32.
+//   warps 2..9  softmax: two threads per query row (TMEM lane = row), one per
+//               64-key half of the tile; they exchange the partial row max;
+//               exp2 with packed FP32 pairs, row sum, P -> FP16 into TMEM; lazy
+//               O rescaling (only when the running max grows by more than 2^8),
+//               each thread on its half of O; epilogue O / l.
+// Tensor memory (512 columns): NSB S buffers of 128 FP32 columns (3 for D=128,
+// 2 for D=256); P_j overwrites the first 64 columns of its S buffer as FP16
+// pairs; O [NSB*128, NSB*128 + D) FP32.  The MMA warp keeps QK NSB tiles ahead.
 //
 // Every wait is bounded in time (see WaitCtl): a wait that runs out records
 // GBATTN_DEV_WAIT_TIMEOUT in the device status word, the CTA stops, waits a
@@ -39,7 +42,8 @@ namespace {
 
 constexpr int BM = 128;             // query rows per CTA
 constexpr int BN = 128;             // keys per tile (two halves of 64)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;          // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+constexpr int kSoftmaxThreads = 256;
 constexpr int kMaxSparseTiles = 512;
 constexpr int kMaxTopk = 512;
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s for draining after an abort
@@ -71,12 +75,16 @@ struct AttnArgs {
 template <int D>
 struct Cfg {
     static constexpr int NS = D == 128 ? 4 : 2;          // K/V ring slots
+    static constexpr int NSB = D == 128 ? 3 : 2;         // S buffers in TMEM (QK lookahead)
     static constexpr int CHUNK = 128 * 128;               // 128 rows x 64 FP16 columns
     static constexpr int HALF = 64 * 128;                 // 64 rows x 64 columns
     static constexpr int KCH = D / 64;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int SLOT_BYTES = BN * D * 2;
-    static constexpr uint32_t T_S = 0, T_P0 = 128, T_P1 = 192, T_O = 256;
+    // TMEM columns: S buffer b at b*128 (P of that tile overwrites its first 64
+    // columns as FP16 pairs), O after the S buffers.
+    static constexpr uint32_t T_O = NSB * 128;
+    static_assert(T_O + D <= 512, "tensor memory budget");
     static constexpr uint32_t IDESC_QK = idesc_f16(BM, BN, false, false);
     static constexpr uint32_t IDESC_PV = idesc_f16(BM, D, false, true);
 };
@@ -85,14 +93,26 @@ struct Ctrl {
     uint64_t q_full;
     uint64_t full[4];
     uint64_t empty[4];
-    uint64_t s_full, s_free;
-    uint64_t p_full[2];
-    uint64_t pv_done[2];
+    uint64_t s_full[3];    // QK_j done (buffer j % NSB)
+    uint64_t p_full[3];    // P_j written (buffer j % NSB)
+    uint64_t pv_done[3];   // PV_j done (barrier j % NSB).  QK_j is issued after
+                           // PV_{j-NSB}, so once S_j is visible the previous phase
+                           // of every barrier awaited below has completed.
     uint64_t drain;
+    uint64_t xchg[4];      // per row quarter: the two half-row threads exchange values
     uint32_t tmem_base;
     int abort;
     int n_tiles;
 };
+
+// Values exchanged between the two threads that share a query row.
+struct Exchange {
+    float mx[2][2][128];   // [tile parity][column half][row] partial row max
+    float l[2][128];       // [column half][row] partial row sum (epilogue)
+};
+
+constexpr int kCtrlBytes = 256 + static_cast<int>(sizeof(Exchange));
+static_assert(sizeof(Ctrl) <= 256, "control block");
 
 struct SparseTiles {
     int list_a[kMaxTopk];
@@ -104,7 +124,7 @@ struct SparseTiles {
 
 template <int D, int MODE>
 constexpr int smem_bytes() {
-    return 1024 + Cfg<D>::Q_BYTES + Cfg<D>::NS * Cfg<D>::SLOT_BYTES + 256 +
+    return 1024 + Cfg<D>::Q_BYTES + Cfg<D>::NS * Cfg<D>::SLOT_BYTES + kCtrlBytes +
            (MODE == kSparse ? static_cast<int>(sizeof(SparseTiles)) : 0);
 }
 
@@ -116,12 +136,21 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
-// Item order of the K/V ring: K0, then (K_j, V_{j-1}) for j = 1..n-1, then V_{n-1}.
-__device__ __forceinline__ void ring_item(int it, int n, int& tile, bool& is_v) {
-    if (it == 0) { tile = 0; is_v = false; return; }
-    if (it == 2 * n - 1) { tile = n - 1; is_v = true; return; }
-    if (it & 1) { tile = (it + 1) >> 1; is_v = false; }
-    else { tile = (it >> 1) - 1; is_v = true; }
+// Item order of the K/V ring = the MMA warp's consumption order with a QK
+// lookahead of L tiles: K_0 .. K_{L-1}, then (V_j, K_{j+L}) while j + L < n,
+// then the remaining V_j.
+__device__ __forceinline__ void ring_item(int it, int n, int L, int& tile, bool& is_v) {
+    const int k0 = min(n, L);
+    if (it < k0) { tile = it; is_v = false; return; }
+    const int r = it - k0;
+    const int m = max(n - L, 0);
+    if (r < 2 * m) {
+        if (r & 1) { tile = (r >> 1) + L; is_v = false; }
+        else { tile = r >> 1; is_v = true; }
+        return;
+    }
+    tile = m + (r - 2 * m);
+    is_v = true;
 }
 
 // Merge two strictly ascending cube lists into the tile list of a query-cube
@@ -194,7 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sQ = smem;
     uint8_t* sKV = smem + C::Q_BYTES;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(sKV + C::NS * C::SLOT_BYTES);
-    SparseTiles* st = reinterpret_cast<SparseTiles*>(reinterpret_cast<uint8_t*>(ctrl) + 256);
+    Exchange* ex = reinterpret_cast<Exchange*>(reinterpret_cast<uint8_t*>(ctrl) + 256);
+    SparseTiles* st = reinterpret_cast<SparseTiles*>(reinterpret_cast<uint8_t*>(ctrl) + kCtrlBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.y;
@@ -225,12 +255,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctrl->full[i], 1);
             mbar_init(&ctrl->empty[i], 1);
         }
-        mbar_init(&ctrl->s_full, 1);
-        mbar_init(&ctrl->s_free, 128);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctrl->p_full[i], 128);
-            mbar_init(&ctrl->pv_done[i], 1);
+        for (int i = 0; i < C::NSB; ++i) {
+            mbar_init(&ctrl->s_full[i], 1);
+            mbar_init(&ctrl->p_full[i], kSoftmaxThreads);
         }
+        for (int i = 0; i < C::NSB; ++i) mbar_init(&ctrl->pv_done[i], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&ctrl->xchg[i], 64);
         mbar_init(&ctrl->drain, 1);
         ctrl->abort = 0;
         mbar_init_fence();
@@ -280,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_one(&ctrl->empty[slot], ph ^ 1u, w)) { ok = false; break; }
                 int t;
                 bool is_v;
-                ring_item(it, n_tiles, t, is_v);
+                ring_item(it, n_tiles, C::NSB, t, is_v);
                 int k0, k1;
                 tile_keys(t, k0, k1);
                 const CUtensorMap* m = is_v ? &tmV : &tmK;
@@ -305,54 +335,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && n_tiles > 0) {
             bool ok = wait_one(&ctrl->q_full, 0, w);
             const uint32_t qa = smem_addr(sQ);
-            auto issue_qk = [&](int slot) {
+            auto issue_qk = [&](int slot, int buf) {
                 const uint32_t ka = smem_addr(sKV + slot * C::SLOT_BYTES);
 #pragma unroll
                 for (int k16 = 0; k16 < D / 16; ++k16) {
                     const uint32_t off = (k16 >> 2) * C::CHUNK + (k16 & 3) * 32;
-                    mma_ss(tmem + C::T_S, sdesc_sw128(qa + off, 16, 1024),
+                    mma_ss(tmem + buf * 128, sdesc_sw128(qa + off, 16, 1024),
                            sdesc_sw128(ka + off, 16, 1024), C::IDESC_QK, k16 > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int slot, int b, bool acc) {
+            auto issue_pv = [&](int slot, int buf, bool acc) {
                 const uint32_t va = smem_addr(sKV + slot * C::SLOT_BYTES);
-                const uint32_t pcol = tmem + (b ? C::T_P1 : C::T_P0);
 #pragma unroll
                 for (int k16 = 0; k16 < BN / 16; ++k16)
-                    mma_ts(tmem + C::T_O, pcol + k16 * 8, sdesc_sw128(va + k16 * 2048, C::CHUNK, 1024),
-                           C::IDESC_PV, (acc || k16 > 0) ? 1u : 0u);
+                    mma_ts(tmem + C::T_O, tmem + buf * 128 + k16 * 8,
+                           sdesc_sw128(va + k16 * 2048, C::CHUNK, 1024), C::IDESC_PV,
+                           (acc || k16 > 0) ? 1u : 0u);
             };
             int it = 0;
-            if (ok) ok = wait_one(&ctrl->full[0], 0, w);
-            if (ok) {
+            // S_0 .. S_{L-1} up front, then per tile: PV_j, and QK_{j+L} into the
+            // buffer P_j has just been read from (in order on the tensor pipe).
+            for (int t = 0; ok && t < min(n_tiles, C::NSB); ++t) {
+                const int slot = it % C::NS;
+                ok = wait_one(&ctrl->full[slot], (it / C::NS) & 1, w);
+                if (!ok) break;
                 tc_fence_after();
-                issue_qk(0);
-                mma_commit(&ctrl->s_full);
-                mma_commit(&ctrl->empty[0]);
-                it = 1;
+                issue_qk(slot, t);
+                mma_commit(&ctrl->s_full[t]);
+                mma_commit(&ctrl->empty[slot]);
+                ++it;
             }
             for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles) {
-                    const int slot = it % C::NS;
-                    ok = wait_one(&ctrl->full[slot], (it / C::NS) & 1, w) &&
-                         wait_one(&ctrl->s_free, j & 1, w);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_qk(slot);
-                    mma_commit(&ctrl->s_full);
-                    mma_commit(&ctrl->empty[slot]);
-                    ++it;
-                }
-                const int b = j & 1;
-                const int slot = it % C::NS;
-                ok = wait_one(&ctrl->p_full[b], (j >> 1) & 1, w) &&
+                const int buf = j % C::NSB;
+                int slot = it % C::NS;
+                ok = wait_one(&ctrl->p_full[buf], (j / C::NSB) & 1, w) &&
                      wait_one(&ctrl->full[slot], (it / C::NS) & 1, w);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(slot, b, j > 0);
+                issue_pv(slot, buf, j > 0);
                 mma_commit(&ctrl->empty[slot]);
-                mma_commit(&ctrl->pv_done[b]);
+                mma_commit(&ctrl->pv_done[buf]);
                 ++it;
+                if (j + C::NSB < n_tiles) {
+                    slot = it % C::NS;
+                    ok = wait_one(&ctrl->full[slot], (it / C::NS) & 1, w);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(slot, buf);
+                    mma_commit(&ctrl->s_full[buf]);
+                    mma_commit(&ctrl->empty[slot]);
+                    ++it;
+                }
             }
             if (!ok) {   // wait for issued MMAs before tensor memory is freed
                 mma_commit(&ctrl->drain);
@@ -360,12 +393,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ================= softmax / correction / epilogue (warps 2..5)
+        // ================= softmax / correction / epilogue (warps 2..9)
+        // Two threads share each query row: warps 2..5 own key columns 0..63 of
+        // every tile, warps 6..9 columns 64..127 (TMEM lane quarter = warp % 4).
+        // They exchange their partial row max each tile (and the row sums at the
+        // end) through shared memory, ordered by the per-quarter xchg mbarrier.
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const long long row_g = static_cast<long long>(q_row0) + row;
         const int row_half = row >> 6;
+        uint64_t* xbar = &ctrl->xchg[quarter];
         int lim = a.seq_k;   // keys >= lim are invisible to this row
         if (MODE == kCausal)
             lim = static_cast<int>(min(static_cast<long long>(a.seq_k), a.kv_prefix + row_g + 1));
@@ -374,39 +413,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     static_cast<long long>(a.kv_prefix) + q_row0 + 1))
                              : a.seq_k;
         const float sl2 = a.scale_log2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
         float m_run = -INFINITY, l = 0.0f;
+        uint32_t xphase = 0;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            ok = wait_warp(&ctrl->s_full, j & 1, w);
+            const int buf = j % C::NSB;
+            const uint32_t sbuf = tl + buf * 128;
+            ok = wait_warp(&ctrl->s_full[buf], (j / C::NSB) & 1, w);
             if (!ok) break;
             tc_fence_after();
-            uint32_t s[128];
-            tmem_ld32(tl + C::T_S, s);
-            tmem_ld32(tl + C::T_S + 32, s + 32);
-            tmem_ld32(tl + C::T_S + 64, s + 64);
-            tmem_ld32(tl + C::T_S + 96, s + 96);
+            uint32_t s[64];
+            tmem_ld32(sbuf + half * 64, s);
+            tmem_ld32(sbuf + half * 64 + 32, s + 32);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&ctrl->s_free);
 
             int k0, k1;
             tile_keys(j, k0, k1);
             if (MODE == kSparse) {
                 const uint32_t mk = st->mask[j];
-                if (mk != 0xFu) {
-                    const bool v0 = (mk >> (row_half * 2)) & 1u, v1 = (mk >> (row_half * 2 + 1)) & 1u;
+                if (!((mk >> (row_half * 2 + half)) & 1u)) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (!(c < 64 ? v0 : v1)) s[c] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 64; ++c) s[c] = __float_as_uint(-INFINITY);
                 }
-            } else if (k0 + BN > lim0) {
+            } else {
+                const int kh = half ? k1 : k0;
+                if (kh + 64 > lim0) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (k0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 64; ++c)
+                        if (kh + c >= lim) s[c] = __float_as_uint(-INFINITY);
+                }
             }
-            float mx = -INFINITY;
+            // row max of the 64 values with four independent chains (short latency)
+            float m4[4];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+            for (int k = 0; k < 4; ++k) m4[k] = __uint_as_float(s[k]);
+#pragma unroll
+            for (int c = 4; c < 64; c += 8) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    m4[k] = max3f(m4[k], __uint_as_float(s[c + k]), __uint_as_float(s[c + 4 + k]));
+            }
+            const float pm = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
+            ex->mx[j & 1][half][row] = pm;
+            tc_fence_before();   // our S loads are ordered before the partner's P stores
+            mbar_arrive(xbar);
+            ok = wait_warp(xbar, xphase, w);
+            xphase ^= 1u;
+            if (!ok) break;
+            tc_fence_after();
+            const float mx = fmaxf(pm, ex->mx[j & 1][half ^ 1][row]);
             const float m_new = fmaxf(m_run, mx * sl2);
             const bool need = m_new > m_run + 8.0f;
             float alpha = 1.0f;
@@ -416,48 +472,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool warp_need = __any_sync(0xffffffffu, need);
             const float m_use = m_run == -INFINITY ? 0.0f : m_run;
-            float rs0 = 0.0f, rs1 = 0.0f;
-            uint32_t p2[64];
+            const uint64_t negm = f2_pack(-m_use, -m_use);
+            uint64_t rs[4];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(s[2 * i]), sl2, -m_use));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(s[2 * i + 1]), sl2, -m_use));
-                rs0 += p0;
-                rs1 += p1;
+            for (int k = 0; k < 4; ++k) rs[k] = f2_pack(0.0f, 0.0f);
+            uint32_t p2[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                 sl2x2, negm),
+                          x0, x1);
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                rs[i & 3] = f2_add(rs[i & 3], f2_pack(p0, p1));   // four independent sums
                 p2[i] = pack_half2(p0, p1);
             }
-            l = l * alpha + (rs0 + rs1);
-            const int b = j & 1;
-            if (j >= 2) {   // PV_{j-2} must have finished reading this P buffer
-                ok = wait_warp(&ctrl->pv_done[b], ((j - 2) >> 1) & 1, w);
-                if (!ok) break;
-                tc_fence_after();
-            }
-            const uint32_t pcol = tl + (b ? C::T_P1 : C::T_P0);
-            tmem_st32(pcol, p2);
-            tmem_st32(pcol + 32, p2 + 32);
+            float r0, r1, r2, r3, r4, r5, r6, r7;
+            f2_unpack(rs[0], r0, r1);
+            f2_unpack(rs[1], r2, r3);
+            f2_unpack(rs[2], r4, r5);
+            f2_unpack(rs[3], r6, r7);
+            l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
+            // P_j over the first 64 columns of its S buffer; both threads of the
+            // row have loaded their S halves (they passed the exchange above).
+            tmem_st32(sbuf + half * 32, p2);
             tmem_st_wait();
-            if (warp_need && j > 0) {   // rescale O after PV_{j-1} has landed
-                ok = wait_warp(&ctrl->pv_done[b ^ 1], ((j - 1) >> 1) & 1, w);
+            if (warp_need && j > 0) {   // rescale this thread's half of O after PV_{j-1}
+                ok = wait_warp(&ctrl->pv_done[(j - 1) % C::NSB], ((j - 1) / C::NSB) & 1, w);
                 if (!ok) break;
                 tc_fence_after();
+                const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    const uint32_t col = tl + C::T_O + half * (D / 2) + cc * 32;
                     uint32_t o[32];
-                    tmem_ld32(tl + C::T_O + cc * 32, o);
+                    tmem_ld32(col, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(tl + C::T_O + cc * 32, o);
+                    for (int e = 0; e < 16; ++e) {
+                        float y0, y1;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), a2),
+                                  y0, y1);
+                        o[2 * e] = __float_as_uint(y0);
+                        o[2 * e + 1] = __float_as_uint(y1);
+                    }
+                    tmem_st32(col, o);
                 }
                 tmem_st_wait();
             }
             tc_fence_before();
-            mbar_arrive(&ctrl->p_full[b]);
+            mbar_arrive(&ctrl->p_full[buf]);
         }
         if (ok && n_tiles > 0) {
-            ok = wait_warp(&ctrl->pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, w);
+            ok = wait_warp(&ctrl->pv_done[(n_tiles - 1) % C::NSB], ((n_tiles - 1) / C::NSB) & 1, w);
             tc_fence_after();
+        }
+        if (ok) {   // combine the two partial row sums
+            ex->l[half][row] = l;
+            mbar_arrive(xbar);
+            ok = wait_warp(xbar, xphase, w);
+            if (ok) l += ex->l[half ^ 1][row];
         }
         if (ok) {
             const bool row_ok = row_g < a.seq_q;
@@ -467,10 +541,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool partial = MODE == kCausal && a.n_chunks > 1;
             const long long orow = static_cast<long long>(bh) * a.seq_q + row_g;
 #pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int c0 = half * (D / 2) + cc * 32;   // first output column of this chunk
                 uint32_t o[32];
                 if (n_tiles > 0) {
-                    tmem_ld32(tl + C::T_O + cc * 32, o);
+                    tmem_ld32(tl + C::T_O + c0, o);
                     tmem_ld_wait();
                 } else {
 #pragma unroll
@@ -479,8 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!row_ok) continue;
                 if (partial) {
                     float4* dst = reinterpret_cast<float4*>(
-                        a.part_o + ((static_cast<long long>(chunk) * a.heads_q * a.seq_q + orow) * D +
-                                    cc * 32));
+                        a.part_o + ((static_cast<long long>(chunk) * a.heads_q * a.seq_q + orow) * D + c0));
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l,
@@ -488,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              __uint_as_float(o[4 * e + 2]) * inv_l,
                                              __uint_as_float(o[4 * e + 3]) * inv_l);
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(a.o + orow * D + cc * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(a.o + orow * D + c0);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         uint32_t hw[4];
@@ -500,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (row_ok) {
+            if (row_ok && half == 0) {
                 if (partial)
                     a.part_lse[static_cast<long long>(chunk) * a.heads_q * a.seq_q + orow] = lse2;
                 else if (a.lse)

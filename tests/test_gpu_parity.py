@@ -120,7 +120,8 @@ def test_dense_small_all_rows(gb):
     assert gb.device_status() == 0
 
 
-@pytest.mark.parametrize("Sq,Skv", [(1, 1), (200, 333), (128, 4096), (517, 129), (64, 1000)])
+@pytest.mark.parametrize("Sq,Skv", [(1, 1), (200, 333), (128, 4096), (517, 129), (64, 1000),
+                                     (256, 384), (128, 512), (130, 640), (300, 897)])
 def test_dense_ragged(gb, Sq, Skv):
     q, k, v = inputs.dense_inputs(2, 3, Sq, 128, seed=Sq * 7 + Skv, skv=Skv)
     o = gb.attn_dense_fwd(t(q), t(k), t(v))
