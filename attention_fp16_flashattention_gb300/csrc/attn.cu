@@ -296,18 +296,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (warp == 0) {
-        // ================= TMA producer
-        if (lane == 0 && n_tiles > 0) {
+        // ================= TMA producer (whole warp; one elected lane issues)
+        if (n_tiles > 0) {
             int last_it[4] = {-1, -1, -1, -1};
-            mbar_arrive_expect_tx(&ctrl->q_full, C::Q_BYTES);
+            if (elect_one()) {
+                mbar_arrive_expect_tx(&ctrl->q_full, C::Q_BYTES);
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-                tma_load_3d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, bh);
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_3d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, bh);
+            }
+            __syncwarp();
             bool ok = true;
             for (int it = 0; it < 2 * n_tiles; ++it) {
                 const int slot = it % C::NS;
-                const uint32_t ph = (it / C::NS) & 1;
-                if (!wait_one(&ctrl->empty[slot], ph ^ 1u, w)) { ok = false; break; }
+                if (!wait_warp(&ctrl->empty[slot], ((it / C::NS) & 1) ^ 1u, w)) { ok = false; break; }
                 int t;
                 bool is_v;
                 ring_item(it, n_tiles, C::NSB, t, is_v);
@@ -315,25 +317,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_keys(t, k0, k1);
                 const CUtensorMap* m = is_v ? &tmV : &tmK;
                 uint8_t* dst = sKV + slot * C::SLOT_BYTES;
-                mbar_arrive_expect_tx(&ctrl->full[slot], C::SLOT_BYTES);
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&ctrl->full[slot], C::SLOT_BYTES);
 #pragma unroll
-                for (int c = 0; c < C::KCH; ++c) {
-                    tma_load_3d(dst + c * C::CHUNK, m, &ctrl->full[slot], c * 64, k0, kv_bh);
-                    tma_load_3d(dst + c * C::CHUNK + C::HALF, m, &ctrl->full[slot], c * 64, k1,
-                                kv_bh);
+                    for (int c = 0; c < C::KCH; ++c) {
+                        tma_load_3d(dst + c * C::CHUNK, m, &ctrl->full[slot], c * 64, k0, kv_bh);
+                        tma_load_3d(dst + c * C::CHUNK + C::HALF, m, &ctrl->full[slot], c * 64, k1,
+                                    kv_bh);
+                    }
                 }
+                __syncwarp();
                 last_it[slot] = it;
             }
-            if (!ok) {   // let copies in flight land before the CTA exits
+            if (!ok && lane == 0) {   // let copies in flight land before the CTA exits
                 drain_wait(&ctrl->q_full, 0);
                 for (int s = 0; s < C::NS; ++s)
                     if (last_it[s] >= 0) drain_wait(&ctrl->full[s], (last_it[s] / C::NS) & 1);
             }
         }
     } else if (warp == 1) {
-        // ================= MMA issuer
-        if (lane == 0 && n_tiles > 0) {
-            bool ok = wait_one(&ctrl->q_full, 0, w);
+        // ================= MMA issuer (whole warp waits; one elected lane issues
+        // each group of MMAs and its commits)
+        if (n_tiles > 0) {
+            bool ok = wait_warp(&ctrl->q_full, 0, w);
             const uint32_t qa = smem_addr(sQ);
             auto issue_qk = [&](int slot, int buf) {
                 const uint32_t ka = smem_addr(sKV + slot * C::SLOT_BYTES);
@@ -357,39 +363,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             // buffer P_j has just been read from (in order on the tensor pipe).
             for (int t = 0; ok && t < min(n_tiles, C::NSB); ++t) {
                 const int slot = it % C::NS;
-                ok = wait_one(&ctrl->full[slot], (it / C::NS) & 1, w);
+                ok = wait_warp(&ctrl->full[slot], (it / C::NS) & 1, w);
                 if (!ok) break;
                 tc_fence_after();
-                issue_qk(slot, t);
-                mma_commit(&ctrl->s_full[t]);
-                mma_commit(&ctrl->empty[slot]);
+                if (elect_one()) {
+                    issue_qk(slot, t);
+                    mma_commit(&ctrl->s_full[t]);
+                    mma_commit(&ctrl->empty[slot]);
+                }
+                __syncwarp();
                 ++it;
             }
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int buf = j % C::NSB;
-                int slot = it % C::NS;
-                ok = wait_one(&ctrl->p_full[buf], (j / C::NSB) & 1, w) &&
-                     wait_one(&ctrl->full[slot], (it / C::NS) & 1, w);
+                const int vslot = it % C::NS;
+                ok = wait_warp(&ctrl->p_full[buf], (j / C::NSB) & 1, w) &&
+                     wait_warp(&ctrl->full[vslot], (it / C::NS) & 1, w);
                 if (!ok) break;
-                tc_fence_after();
-                issue_pv(slot, buf, j > 0);
-                mma_commit(&ctrl->empty[slot]);
-                mma_commit(&ctrl->pv_done[buf]);
                 ++it;
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_pv(vslot, buf, j > 0);
+                    mma_commit(&ctrl->empty[vslot]);
+                    mma_commit(&ctrl->pv_done[buf]);
+                }
+                __syncwarp();
                 if (j + C::NSB < n_tiles) {
-                    slot = it % C::NS;
-                    ok = wait_one(&ctrl->full[slot], (it / C::NS) & 1, w);
+                    const int kslot = it % C::NS;
+                    ok = wait_warp(&ctrl->full[kslot], (it / C::NS) & 1, w);
                     if (!ok) break;
-                    tc_fence_after();
-                    issue_qk(slot, buf);
-                    mma_commit(&ctrl->s_full[buf]);
-                    mma_commit(&ctrl->empty[slot]);
                     ++it;
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_qk(kslot, buf);
+                        mma_commit(&ctrl->s_full[buf]);
+                        mma_commit(&ctrl->empty[kslot]);
+                    }
+                    __syncwarp();
                 }
             }
             if (!ok) {   // wait for issued MMAs before tensor memory is freed
-                mma_commit(&ctrl->drain);
-                drain_wait(&ctrl->drain, 0);
+                if (elect_one()) mma_commit(&ctrl->drain);
+                __syncwarp();
+                if (lane == 0) drain_wait(&ctrl->drain, 0);
             }
         }
     } else {

@@ -105,6 +105,20 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// One lane of a converged warp (elect.sync).  Issue tcgen05.mma / TMA from a
+// converged warp through one elected lane per group of instructions: a lone
+// diverged lane issuing them makes every later shared-memory wait of the warp
+// stall behind the tensor pipe.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(p));
+    return p != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
