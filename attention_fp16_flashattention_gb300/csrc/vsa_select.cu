@@ -8,12 +8,14 @@
 //     consecutive channels of one cube and adds the cube's 64 tokens in token
 //     order with FP32 rounding after every addition, then divides by the count
 //     (correctly rounded).  HBM-bound: Q and K are read once with 16-byte loads.
-//  2. vsa_score_topk_kernel: one warp per query cube.  Scores against every key
-//     cube are FP32 sums over d = 0..D-1, in order, of FP32 products (no fused
-//     multiply-add, so both the product and the sum are rounded).  The k-th
-//     largest score is found with a 32-step bitwise search on order-preserving
-//     integer keys; equal scores at the threshold are taken from the lowest
-//     cube index up; the selection is written in ascending cube order.
+//  2. vsa_score_topk_kernel: 32 query cubes per CTA against all key cubes,
+//     register-tiled (2 queries x 4 keys per thread) with operands staged
+//     d-major in shared memory.  Every score is an FP32 sum over d = 0..D-1, in
+//     order, of FP32 products (no fused multiply-add, so both the product and the
+//     sum are rounded).  The k-th largest score of a row is found with a 32-step
+//     bitwise search on order-preserving integer keys; equal scores at the
+//     threshold are taken from the lowest cube index up; the selection is
+//     written in ascending cube order.
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -25,9 +27,7 @@ namespace gbattn {
 namespace {
 
 constexpr int kPoolThreads = 256;
-constexpr int kQueriesPerCta = 8;   // one warp per query cube
-constexpr int kKeyChunk = 32;       // key cubes staged in shared memory per step
-constexpr int kMaxChunks = 32;      // supports up to 1024 cubes per head
+constexpr int kMaxChunks = 32;      // 32-key chunks per row: supports up to 1024 cubes per head
 
 __global__ void __launch_bounds__(kPoolThreads) vsa_pool_kernel(
     const __half* __restrict__ q, const __half* __restrict__ k, long long n_cubes, int D,
@@ -70,79 +70,134 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// grid: (ceil(NC / kQueriesPerCta), B*H); block: 32 * kQueriesPerCta; D == 128.
-__global__ void __launch_bounds__(32 * kQueriesPerCta) vsa_score_topk_kernel(
+constexpr int kSelQ = 16;        // query cubes per CTA (about 75 KB of shared memory: 3 CTAs per SM)
+constexpr int kSelKB = 64;       // key cubes per staged block
+constexpr int kSelThreads = 256;
+constexpr int kSelD = 128;
+
+constexpr size_t sel_smem_bytes(int NC) {
+    return (static_cast<size_t>(kSelD) * kSelQ + static_cast<size_t>(kSelD) * (kSelKB + 4) +
+            static_cast<size_t>(kSelQ) * (NC + 1)) * sizeof(float);
+}
+
+// grid: (ceil(NC / kSelQ), B*H); block: kSelThreads; dynamic smem sel_smem_bytes(NC).
+// Scores for 16 query cubes x all NC key cubes, each an FP32 sum over d in order of
+// FP32 products (no FMA): thread (ty, tx) accumulates query ty against keys
+// 4tx..4tx+3 of each 64-key block with both operands staged d-major.  Then each
+// warp selects the top-k of two query rows; CH = 32-key chunks per row.
+template <int CH>
+__global__ void __launch_bounds__(kSelThreads) vsa_score_topk_kernel(
     const float* __restrict__ qm, const float* __restrict__ km, int NC, int topk,
     int32_t* __restrict__ idx) {
-    constexpr int D = 128;
-    __shared__ float sk[kKeyChunk][D + 1];     // +1 pad: lanes read distinct banks
-    __shared__ float sq[kQueriesPerCta][D];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.y;
-    const int qc = blockIdx.x * kQueriesPerCta + warp;
-    const float* qbase = qm + static_cast<long long>(bh) * NC * D;
-    const float* kbase = km + static_cast<long long>(bh) * NC * D;
-    for (int i = threadIdx.x; i < kQueriesPerCta * D; i += blockDim.x) {
-        const int w = i / D, d = i % D;
-        const int c = blockIdx.x * kQueriesPerCta + w;
-        sq[w][d] = c < NC ? qbase[static_cast<long long>(c) * D + d] : 0.0f;
-    }
-    const int nchunks = (NC + kKeyChunk - 1) / kKeyChunk;
-    uint32_t key[kMaxChunks];
+    extern __shared__ float sm[];
+    float* sq = sm;                                   // [D][kSelQ]
+    float* sk = sq + kSelD * kSelQ;                   // [D][kSelKB + 4]
+    float* ss = sk + kSelD * (kSelKB + 4);            // [kSelQ][NC + 1]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.y, q0 = blockIdx.x * kSelQ;
+    const float* qbase = qm + static_cast<long long>(bh) * NC * kSelD;
+    const float* kbase = km + static_cast<long long>(bh) * NC * kSelD;
+    const int SK = kSelKB + 4, SS = NC + 1;
+    // Stage Q (32 x 128) d-major: every thread issues its four 16-byte loads first.
+    {
+        float4 v[kSelQ * kSelD / 4 / kSelThreads];
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) key[c] = 0u;   // 0 sorts below every real score
-
-#pragma unroll 1
-    for (int ch = 0; ch < nchunks; ++ch) {
-        __syncthreads();
-        for (int i = threadIdx.x; i < kKeyChunk * D; i += blockDim.x) {
-            const int r = i / D, d = i % D;
-            const int kc = ch * kKeyChunk + r;
-            sk[r][d] = kc < NC ? kbase[static_cast<long long>(kc) * D + d] : 0.0f;
+        for (int r = 0; r < kSelQ * kSelD / 4 / kSelThreads; ++r) {
+            const int i = tid + r * kSelThreads, q = i / (kSelD / 4), d4 = i % (kSelD / 4);
+            v[r] = (q0 + q < NC) ? *reinterpret_cast<const float4*>(qbase + static_cast<long long>(q0 + q) * kSelD + 4 * d4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int r = 0; r < kSelQ * kSelD / 4 / kSelThreads; ++r) {
+            const int i = tid + r * kSelThreads, q = i / (kSelD / 4), d4 = i % (kSelD / 4);
+            sq[(4 * d4 + 0) * kSelQ + q] = v[r].x;
+            sq[(4 * d4 + 1) * kSelQ + q] = v[r].y;
+            sq[(4 * d4 + 2) * kSelQ + q] = v[r].z;
+            sq[(4 * d4 + 3) * kSelQ + q] = v[r].w;
+        }
+    }
+    const int ty = tid >> 4, tx = tid & 15;
+    for (int kb = 0; kb < NC; kb += kSelKB) {
+        // Stage 64 key means d-major: eight 16-byte loads in flight per thread.
+        float4 v[kSelKB * kSelD / 4 / kSelThreads];
+#pragma unroll
+        for (int r = 0; r < kSelKB * kSelD / 4 / kSelThreads; ++r) {
+            const int i = tid + r * kSelThreads, k = i / (kSelD / 4), d4 = i % (kSelD / 4);
+            v[r] = (kb + k < NC) ? *reinterpret_cast<const float4*>(kbase + static_cast<long long>(kb + k) * kSelD + 4 * d4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncthreads();
-        float acc = 0.0f;
-#pragma unroll 16
-        for (int d = 0; d < D; ++d) acc = __fadd_rn(acc, __fmul_rn(sq[warp][d], sk[lane][d]));
-        const uint32_t kk = (ch * kKeyChunk + lane < NC) ? order_key(acc) : 0u;
 #pragma unroll
-        for (int c = 0; c < kMaxChunks; ++c)
-            if (c == ch) key[c] = kk;
+        for (int r = 0; r < kSelKB * kSelD / 4 / kSelThreads; ++r) {
+            const int i = tid + r * kSelThreads, k = i / (kSelD / 4), d4 = i % (kSelD / 4);
+            sk[(4 * d4 + 0) * SK + k] = v[r].x;
+            sk[(4 * d4 + 1) * SK + k] = v[r].y;
+            sk[(4 * d4 + 2) * SK + k] = v[r].z;
+            sk[(4 * d4 + 3) * SK + k] = v[r].w;
+        }
+        __syncthreads();
+        float acc[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j] = 0.0f;
+#pragma unroll 8
+        for (int d = 0; d < kSelD; ++d) {
+            const float qv = sq[d * kSelQ + ty];
+            const float4 kv = *reinterpret_cast<const float4*>(sk + d * SK + 4 * tx);
+            acc[0] = __fadd_rn(acc[0], __fmul_rn(qv, kv.x));
+            acc[1] = __fadd_rn(acc[1], __fmul_rn(qv, kv.y));
+            acc[2] = __fadd_rn(acc[2], __fmul_rn(qv, kv.z));
+            acc[3] = __fadd_rn(acc[3], __fmul_rn(qv, kv.w));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (kb + 4 * tx + j < NC) ss[ty * SS + kb + 4 * tx + j] = acc[j];
     }
-    if (qc >= NC) return;
+    __syncthreads();
 
-    // Threshold: the largest T such that at least topk keys are >= T.
-    uint32_t T = 0;
-#pragma unroll 1
-    for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t cand = T | (1u << bit);
-        int cnt = 0;
-#pragma unroll
-        for (int c = 0; c < kMaxChunks; ++c) cnt += (c < nchunks && key[c] >= cand) ? 1 : 0;
-        cnt = __reduce_add_sync(0xffffffffu, cnt);
-        if (cnt >= topk) T = cand;
-    }
-    int greater = 0;
-#pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) greater += (c < nchunks && key[c] > T) ? 1 : 0;
-    greater = __reduce_add_sync(0xffffffffu, greater);
-    int need = topk - greater;            // equal-to-threshold scores still to take
-
+    // Top-k: warp w owns query rows 2w, 2w+1.  Key c*32 + lane -> key[c].
+    const int nchunks = (NC + 31) / 32;
     const uint32_t lt = (1u << lane) - 1u;
-    int32_t* out = idx + (static_cast<long long>(bh) * NC + qc) * topk;
-    int base = 0;
+    for (int r = 0; r < kSelQ / (kSelThreads / 32); ++r) {
+        const int ql = warp * (kSelQ / (kSelThreads / 32)) + r;
+        const int qc = q0 + ql;
+        if (qc >= NC) break;
+        uint32_t key[CH];
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) {
-        if (c < nchunks) {
-            const bool valid = c * kKeyChunk + lane < NC;
-            const bool eq = valid && key[c] == T;
-            const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
-            const int take = min(need, __popc(eqm));
-            const bool sel = valid && (key[c] > T || (eq && __popc(eqm & lt) < take));
-            need -= take;
-            const uint32_t selm = __ballot_sync(0xffffffffu, sel);
-            if (sel) out[base + __popc(selm & lt)] = c * kKeyChunk + lane;
-            base += __popc(selm);
+        for (int c = 0; c < CH; ++c) {
+            const int kc = c * 32 + lane;
+            key[c] = (c < nchunks && kc < NC) ? order_key(ss[ql * SS + kc]) : 0u;   // 0: below any score
+        }
+        // Threshold: the largest T such that at least topk keys are >= T.
+        uint32_t T = 0;
+#pragma unroll 1
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = T | (1u << bit);
+            int cnt = 0;
+#pragma unroll
+            for (int c = 0; c < CH; ++c) cnt += (c < nchunks && key[c] >= cand) ? 1 : 0;
+            cnt = __reduce_add_sync(0xffffffffu, cnt);
+            if (cnt >= topk) T = cand;
+        }
+        int greater = 0;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) greater += (c < nchunks && key[c] > T) ? 1 : 0;
+        greater = __reduce_add_sync(0xffffffffu, greater);
+        int need = topk - greater;            // equal-to-threshold scores still to take
+        int32_t* out = idx + (static_cast<long long>(bh) * NC + qc) * topk;
+        int base = 0;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            if (c < nchunks) {
+                const bool valid = c * 32 + lane < NC;
+                const bool eq = valid && key[c] == T;
+                const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+                const int take = min(need, __popc(eqm));
+                const bool sel = valid && (key[c] > T || (eq && __popc(eqm & lt) < take));
+                need -= take;
+                const uint32_t selm = __ballot_sync(0xffffffffu, sel);
+                if (sel) out[base + __popc(selm & lt)] = c * 32 + lane;
+                base += __popc(selm);
+            }
         }
     }
 }
@@ -166,7 +221,7 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     if (D != 128 || block != 64) return GBATTN_ERR_UNSUPPORTED;
     if (S % block != 0) return GBATTN_ERR_SHAPE;
     const int NC = S / block;
-    if (NC > kMaxChunks * kKeyChunk || topk > NC) return GBATTN_ERR_SHAPE;
+    if (NC > kMaxChunks * 32 || topk > NC) return GBATTN_ERR_SHAPE;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
     const size_t need = vsa_select_workspace_size(B, H, S, D, block);
     if (!workspace || workspace_bytes < need) return GBATTN_ERR_WORKSPACE;
@@ -191,8 +246,21 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     vsa_pool_kernel<<<pgrid, kPoolThreads, 0, s>>>(static_cast<const __half*>(q),
                                                    static_cast<const __half*>(k), n_cubes, D,
                                                    block, qm, km);
-    dim3 sgrid((NC + kQueriesPerCta - 1) / kQueriesPerCta, B * H);
-    vsa_score_topk_kernel<<<sgrid, 32 * kQueriesPerCta, 0, s>>>(qm, km, NC, topk, idx);
+    static std::once_flag attr_once[64];
+    if (dev.device >= 0 && dev.device < 64)
+        std::call_once(attr_once[dev.device], [] {
+            cudaFuncSetAttribute(vsa_score_topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sel_smem_bytes(16 * 32)));
+            cudaFuncSetAttribute(vsa_score_topk_kernel<kMaxChunks>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sel_smem_bytes(kMaxChunks * 32)));
+        });
+    dim3 sgrid((NC + kSelQ - 1) / kSelQ, B * H);
+    if (NC <= 16 * 32)
+        vsa_score_topk_kernel<16><<<sgrid, kSelThreads, sel_smem_bytes(NC), s>>>(qm, km, NC, topk, idx);
+    else
+        vsa_score_topk_kernel<kMaxChunks><<<sgrid, kSelThreads, sel_smem_bytes(NC), s>>>(qm, km, NC, topk,
+                                                                                       idx);
     count_launches(2);
     return launch_status();
 }
