@@ -29,6 +29,7 @@ _SIGNATURES = {
     "gbattn_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "gbattn_set_wait_limit_ns": (_i, [ctypes.c_uint64]),
     "gbattn_launch_count": (ctypes.c_uint64, []),
+    "gbattn_test_inject_fault": (_i, [_i]),
     "attn_dense_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "attn_causal_prefill_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "attn_causal_prefill_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
@@ -111,6 +112,11 @@ def launch_count():
 
 def set_wait_limit_ns(ns):
     _check("gbattn_set_wait_limit_ns", load().gbattn_set_wait_limit_ns(int(ns)))
+
+
+def test_inject_fault(mode):
+    """Test hook: 1 makes attention launches skip their query load (timeout path), 0 restores."""
+    _check("gbattn_test_inject_fault", load().gbattn_test_inject_fault(int(mode)))
 
 
 def device_status(stream=None):

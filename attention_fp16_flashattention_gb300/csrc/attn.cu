@@ -70,6 +70,7 @@ struct AttnArgs {
     const int32_t* idx; // sparse: [heads][n_cubes][topk]
     uint32_t* status;
     uint64_t wait_limit;
+    int fault;          // test hook: 1 = the TMA warp never loads Q (exercises the timeout path)
 };
 
 template <int D>
@@ -299,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= TMA producer (whole warp; one elected lane issues)
         if (n_tiles > 0) {
             int last_it[4] = {-1, -1, -1, -1};
-            if (elect_one()) {
+            const bool load_q = a.fault != 1;
+            if (load_q && elect_one()) {
                 mbar_arrive_expect_tx(&ctrl->q_full, C::Q_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::KCH; ++c)
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 last_it[slot] = it;
             }
             if (!ok && lane == 0) {   // let copies in flight land before the CTA exits
-                drain_wait(&ctrl->q_full, 0);
+                if (load_q) drain_wait(&ctrl->q_full, 0);
                 for (int s = 0; s < C::NS; ++s)
                     if (last_it[s] >= 0) drain_wait(&ctrl->full[s], (last_it[s] / C::NS) & 1);
             }
@@ -686,8 +688,11 @@ int launch_attn(const void* q, const void* k, const void* v, int seq_q, int seq_
     return launch_status();
 }
 
+int g_fault_mode = 0;   // test hook, see gbattn_test_inject_fault
+
 AttnArgs base_args(const DeviceState& dev, float scale) {
     AttnArgs a{};
+    a.fault = g_fault_mode;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.status = dev.status;
     a.wait_limit = wait_limit_ns();
@@ -735,6 +740,12 @@ int sm_count_or_default() {
 }  // namespace gbattn
 
 using namespace gbattn;
+
+extern "C" int gbattn_test_inject_fault(int mode) {
+    if (mode < 0 || mode > 1) return GBATTN_ERR_SHAPE;
+    g_fault_mode = mode;
+    return GBATTN_OK;
+}
 
 extern "C" int attn_dense_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                               int B, int H, int Sq, int Skv, int D, float scale, void* stream) {

@@ -216,21 +216,30 @@ def peaks():
     return dict(hbm=6800.0, tc=1900.0, tc_sust=1700.0, src="fallback")
 
 
-def source_sha():
+KERNEL_SOURCES = {
+    "attn_fwd_kernel<128,dense>": ("attn.cu", "ptx.cuh", "host.h"),
+    "attn_fwd_kernel<128,sparse>": ("attn.cu", "ptx.cuh", "host.h"),
+    "attn_fwd_kernel<256,causal>+merge": ("attn.cu", "ptx.cuh", "host.h"),
+    "e4m3_bridge_kernel": ("bridge.cu", "ptx.cuh", "host.h"),
+}
+
+
+def source_sha(kernel):
+    """Hash of the source files a kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_fp16_flashattention_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
 def traffic_for(kernel):
-    """DRAM bytes per launch from the committed ncu capture, if the sources are unchanged."""
-    if not os.path.exists(PROFILE_TRAFFIC):
+    """DRAM bytes per launch from the committed ncu capture, if the kernel's sources are unchanged."""
+    if not os.path.exists(PROFILE_TRAFFIC) or kernel not in KERNEL_SOURCES:
         return None
     t = json.load(open(PROFILE_TRAFFIC))
     e = t.get(kernel)
-    if not e or e.get("source_sha") != source_sha():
+    if not e or e.get("source_sha") != source_sha(kernel):
         return None
     return e.get("bytes_per_launch")
 

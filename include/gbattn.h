@@ -85,6 +85,15 @@ int gbattn_set_wait_limit_ns(uint64_t limit_ns);
 /* Number of kernels this library has launched since it was loaded (all devices). */
 uint64_t gbattn_launch_count(void);
 
+/* Test hook for the failure path of the bounded waits (the pages ask for
+ * exception-safe operator lifetimes and explicit rollback: "Integrate FP32 v37
+ * prefill and exact E4M3 bridge", Purpose).  mode 1 makes every later
+ * attention launch skip its query-tile load, so its first pipeline wait runs
+ * out after gbattn_set_wait_limit_ns(); the kernel then records
+ * GBATTN_DEV_WAIT_TIMEOUT, frees its tensor memory and returns.  mode 0
+ * (default) restores normal operation.  Returns GBATTN_OK or GBATTN_ERR_SHAPE. */
+int gbattn_test_inject_fault(int mode);
+
 /*
  * Dense non-causal attention, head width D == 128.
  * Cites: "Share SM70 projection, attention and row reduction paths", Purpose
