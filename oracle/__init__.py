@@ -14,6 +14,8 @@ Arithmetic is float64 unless the pages fix another precision:
                   bridge with a single rounding of the scaled value.
 * ``attention`` – softmax(scale * Q K^T + mask) V for the dense, causal
                   (shared-KV heads, prefix offset) and block-sparse variants.
+* ``decode``    – new query tokens attending to a paged E4M3 KV cache through
+                  the bridge's FP16 values (causal among the new tokens).
 * ``vsa``       – cube mean-pooling (FP32, as the pages fix), cube scores and
                   the top-k key-cube selection.
 
@@ -27,4 +29,4 @@ forms, invariants, library routines and brute force; no function here is
 "parity unpinned".
 """
 
-from . import fp16, e4m3, attention, vsa  # noqa: F401
+from . import fp16, e4m3, attention, decode, vsa  # noqa: F401
