@@ -35,6 +35,9 @@ _SIGNATURES = {
     "attn_causal_prefill_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                                      _vp, _sz, _vp]),
     "e4m3_paged_to_fp16": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _vp, _vp, _vp]),
+    "attn_paged_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "attn_paged_decode_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                   _i, _i, _f, _f, _f, _vp, _sz, _vp]),
     "vsa_select_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "vsa_select_blocks": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "vsa_sparse_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
@@ -43,6 +46,7 @@ _SIGNATURES = {
 DEV_WAIT_TIMEOUT = 1
 DEV_BAD_PAGE = 2
 DEV_BAD_INDEX = 4
+DEV_BAD_LENGTH = 8
 
 
 class GbattnError(RuntimeError):
@@ -196,6 +200,47 @@ def e4m3_paged_to_fp16(k_pages, v_pages, page_table, kv_len, k_scale, v_scale, k
                                    _ptr(k_out), _ptr(v_out), _stream(stream))
     _check("e4m3_paged_to_fp16", rc)
     return k_out, v_out
+
+
+def attn_paged_decode_workspace_size(B, Hq, Hkv, nq, max_kv_len, D):
+    return int(load().attn_paged_decode_workspace_size(B, Hq, Hkv, nq, max_kv_len, D))
+
+
+def attn_paged_decode_fwd(q, k_pages, v_pages, page_table, kv_lens, k_scale, v_scale,
+                          max_kv_len=None, o=None, lse=None, scale=None, workspace=None,
+                          stream=None):
+    """Decode over paged E4M3 caches. q [B,Hq,nq,D] FP16; pages [P,page,Hkv,D] uint8;
+    page_table int32 [B,max_pages]; kv_lens int32 [B] (device).  max_kv_len defaults to
+    max_pages * page_size (no device read)."""
+    import torch
+    _need(q, "q", torch.float16, 4)
+    _need(k_pages, "k_pages", torch.uint8, 4)
+    _need(v_pages, "v_pages", torch.uint8, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    B, Hq, nq, D = q.shape
+    P, ps, Hkv, Dk = k_pages.shape
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or Dk != D:
+        raise ValueError("k_pages and v_pages must be [P, page, Hkv, D] matching q")
+    if page_table.shape[0] != B or kv_lens.shape[0] != B:
+        raise ValueError("page_table and kv_lens need one row per sequence")
+    max_pages = page_table.shape[1]
+    max_kv_len = max_pages * ps if max_kv_len is None else int(max_kv_len)
+    o = torch.empty_like(q) if o is None else o
+    _need(o, "o", torch.float16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    if workspace is None:
+        nbytes = attn_paged_decode_workspace_size(B, Hq, Hkv, nq, max_kv_len, D)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    rc = load().attn_paged_decode_fwd(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                      _ptr(kv_lens), _ptr(o), _ptr(lse), B, Hq, Hkv, nq, D, P,
+                                      ps, max_pages, max_kv_len, float(k_scale), float(v_scale),
+                                      _scale(scale, D), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(),
+                                      _stream(stream))
+    _check("attn_paged_decode_fwd", rc)
+    return o
 
 
 def vsa_select_workspace_size(B, H, S, D, block):

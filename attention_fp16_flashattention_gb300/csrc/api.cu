@@ -51,27 +51,46 @@ int current_device(DeviceState* out) {
 uint64_t wait_limit_ns() { return g_wait_limit.load(); }
 void count_launches(int n) { g_launches += static_cast<uint64_t>(n); }
 
+namespace {
+int load_encoder() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return GBATTN_ERR_CUDA;
+        }
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return GBATTN_OK;
+}
+}  // namespace
+
 int encode_tmap_f16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint32_t box0, uint32_t box1) {
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_encode) {
-            void* fn = nullptr;
-            cudaDriverEntryPointQueryResult q;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                 cudaEnableDefault, &q) != cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || !fn) {
-                cudaGetLastError();
-                return GBATTN_ERR_CUDA;
-            }
-            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-        }
-    }
+    if (load_encoder() != GBATTN_OK) return GBATTN_ERR_CUDA;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};   // bytes, dims 1 and 2
     cuuint32_t box[3] = {box0, box1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+int encode_tmap_u8_pages(CUtensorMap* map, const void* base, uint64_t D, uint64_t hkv,
+                         uint64_t rows, uint32_t box_rows) {
+    if (load_encoder() != GBATTN_OK) return GBATTN_ERR_CUDA;
+    cuuint64_t dims[3] = {D, hkv, rows};
+    cuuint64_t strides[2] = {D, D * hkv};   // bytes, dims 1 and 2
+    cuuint32_t box[3] = {128, 1, box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -30,6 +30,12 @@ void count_launches(int n);
 int encode_tmap_f16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint32_t box0, uint32_t box1);
 
+// Encode a 3-D byte tensor map over paged rows [rows][hkv][D] (D bytes per
+// row and head) with a box of 128 bytes x 1 head x box_rows rows and the
+// 128-byte swizzle.  Returns GBATTN_OK or GBATTN_ERR_CUDA.
+int encode_tmap_u8_pages(CUtensorMap* map, const void* base, uint64_t D, uint64_t hkv,
+                         uint64_t rows, uint32_t box_rows);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {

@@ -59,6 +59,7 @@ struct WaitCtl {
 constexpr uint32_t kDevWaitTimeout = 1u;
 constexpr uint32_t kDevBadPage = 2u;
 constexpr uint32_t kDevBadIndex = 4u;
+constexpr uint32_t kDevBadLength = 8u;
 
 // Single-thread wait on (bar, parity).  Returns false if the time limit passed
 // (recording the timeout and raising the CTA abort flag) or another thread of

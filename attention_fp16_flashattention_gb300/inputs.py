@@ -18,6 +18,10 @@ with 64-token cubes and top-k 64):
   paged_e4m3    B1 Hq6 Hkv1 D256, Q=8192 at the tail of KV=131072, K/V as
                 E4M3 bytes uniform over the 254 finite codes in 32-token pages
                 behind a random page-table permutation; scales 1/16 and 1/8
+  paged_decode  B4 Hq6 Hkv1 D256, one new token per sequence over ragged
+                caches of 131072, 122887, 98313 and 65571 tokens (K/V bytes and
+                pages as paged_e4m3, every sequence's pages scattered over one
+                shared physical pool); scales 1/16 and 1/8
 
 Every tensor is drawn from its own numpy PCG64 stream keyed by
 (seed, tensor tag), so shapes can be shrunk for tests without changing the
@@ -166,6 +170,46 @@ def paged_e4m3_inputs(Hkv, KV, D, seed, page_size=32, num_phys_pages=None):
     return kp, vp, table
 
 
+def _e4m3_codes(rng, shape, codes):
+    if codes == "finite":
+        return FINITE_E4M3[rng.integers(0, FINITE_E4M3.size, size=shape)]
+    if codes == "moderate":     # random sign and mantissa, exponent field 3..9
+        sign = rng.integers(0, 2, size=shape, dtype=np.uint8)
+        expo = rng.integers(3, 10, size=shape, dtype=np.uint8)
+        mant = rng.integers(0, 8, size=shape, dtype=np.uint8)
+        return (sign << 7) | (expo << 3) | mant
+    raise ValueError(codes)
+
+
+def paged_decode_inputs(B, Hq, Hkv, nq, kv_lens, D, seed, page_size=32, spare_pages=0,
+                        codes="finite"):
+    """Decode inputs: Q, K/V E4M3 pages, a page table and the sequence lengths.
+
+    q          FP16 [B][Hq][nq][D] ~ N(0,1)
+    k/v pages  uint8 [P][page_size][Hkv][D], P = every sequence's pages + spare_pages
+    page_table int32 [B][max_pages]: sequence b's logical pages on a seeded
+               permutation of the physical pool; entries past its last page are -1
+    kv_lens    int32 [B]
+    codes: "finite" (uniform over the 254 finite E4M3 codes, the paged_e4m3
+    recipe) or "moderate" (|value| in [2^-4, 7.5], so the softmax spreads over
+    many keys).
+    """
+    kv_lens = np.asarray(kv_lens, dtype=np.int32)
+    n_log = [-(-int(n) // page_size) for n in kv_lens]
+    max_pages = max(n_log)
+    P = sum(n_log) + spare_pages
+    q = _normal_fp16(_rng(seed, "q"), (B, Hq, nq, D))
+    kp = _e4m3_codes(_rng(seed, "kpages"), (P, page_size, Hkv, D), codes)
+    vp = _e4m3_codes(_rng(seed, "vpages"), (P, page_size, Hkv, D), codes)
+    perm = _rng(seed, "table").permutation(P).astype(np.int32)
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    at = 0
+    for b in range(B):
+        table[b, :n_log[b]] = perm[at:at + n_log[b]]
+        at += n_log[b]
+    return q, kp, vp, table, kv_lens
+
+
 def sample_rows(n_heads, n_rows, count, seed, row_limit=None):
     """``count`` distinct seeded (head, row) pairs, sorted; rows < row_limit."""
     lim = n_rows if row_limit is None else row_limit
@@ -176,7 +220,7 @@ def sample_rows(n_heads, n_rows, count, seed, row_limit=None):
     return np.stack([pick // lim, pick % lim], axis=1).astype(np.int64)
 
 
-# The five workloads, with their seeds (1000 + workload number).
+# The six workloads, with their seeds (1000 + workload number).
 WORKLOADS = {
     "dense_small": dict(kind="dense", B=1, H=2, S=256, D=128, seed=1001),
     "causal_small": dict(kind="causal", B=1, Hq=6, Hkv=1, Q=1024, KV=4096, D=256, seed=1002),
@@ -185,6 +229,9 @@ WORKLOADS = {
                       seed=1004),
     "paged_e4m3": dict(kind="paged", B=1, Hq=6, Hkv=1, Q=8192, KV=131072, D=256, page_size=32,
                        k_scale=0.0625, v_scale=0.125, seed=1005),
+    "paged_decode": dict(kind="decode", B=4, Hq=6, Hkv=1, nq=1,
+                         kv_lens=(131072, 122887, 98313, 65571), D=256, page_size=32,
+                         k_scale=0.0625, v_scale=0.125, seed=1006),
 }
 
 

@@ -15,6 +15,10 @@ done between steps.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
         [--workload all|dense_video|vsa_video|paged_e4m3|dense_small|causal_small]
+        [--decode on|off|only]
+Beside the step, the paged E4M3 decode (4 ragged sequences of 65571..131072
+cached tokens, Hq6 Hkv1 D256, one new token each; attn_paged_decode_fwd) is
+timed on its own and reported as "decode" with its HBM roofline.
 For N > 1 (torchrun, one process per GPU) every rank runs the same step on its
 own GPU (independent replicas, no data-path communication); the time is the
 maximum over ranks and the value counts the work of all ranks.
@@ -60,6 +64,14 @@ def vsa_flops(B, H, S, D, topk, block=64):
 def bridge_bytes(KV, Hkv, D, page_size):
     n_pages = -(-KV // page_size)
     return 2 * KV * Hkv * D + 4 * n_pages + 2 * 2 * KV * Hkv * D
+
+
+def decode_bytes(kv_lens, B, Hq, Hkv, nq, D, page_size):
+    """Bytes a paged decode must move: every live K and V byte, the page-table
+    entries it reads, Q and the FP16 output (lengths and lse are negligible)."""
+    tokens = int(sum(kv_lens))
+    pages = int(sum(-(-n // page_size) for n in kv_lens))
+    return 2 * tokens * Hkv * D + 4 * pages + 2 * (2 * B * Hq * nq * D)
 
 
 # ------------------------------------------------------------------ workloads on the GPU
@@ -220,7 +232,8 @@ KERNEL_SOURCES = {
     "attn_fwd_kernel<128,dense>": ("attn.cu", "ptx.cuh", "host.h"),
     "attn_fwd_kernel<128,sparse>": ("attn.cu", "ptx.cuh", "host.h"),
     "attn_fwd_kernel<256,causal>+merge": ("attn.cu", "ptx.cuh", "host.h"),
-    "e4m3_bridge_kernel": ("bridge.cu", "ptx.cuh", "host.h"),
+    "e4m3_bridge_kernel": ("bridge.cu", "e4m3.cuh", "ptx.cuh", "host.h"),
+    "paged_decode_kernel+merge": ("decode.cu", "e4m3.cuh", "ptx.cuh", "host.h"),
 }
 
 
@@ -378,6 +391,66 @@ def run_reference(args, names, world, rank):
     return 0
 
 
+def measure_decode(gb, torch, dev, steps, warmup, pk):
+    """Paged E4M3 decode (4 ragged sequences, one new token each), timed on its own.
+
+    Each launch is bracketed by CUDA events on the launching stream; a 256 MB
+    buffer is rewritten between launches (outside the events) so every launch
+    starts with the cache out of L2."""
+    w = inputs.WORKLOADS["paged_decode"]
+    q, kp, vp, table, lens = inputs.paged_decode_inputs(w["B"], w["Hq"], w["Hkv"], w["nq"],
+                                                        w["kv_lens"], w["D"], w["seed"],
+                                                        w["page_size"])
+    T = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    dq, dk, dv, dt, dl = T(q), T(kp), T(vp), T(table), T(lens)
+    o = torch.empty_like(dq)
+    max_kv = int(max(w["kv_lens"]))
+    ws = torch.empty(max(16, gb.attn_paged_decode_workspace_size(w["B"], w["Hq"], w["Hkv"],
+                                                                 w["nq"], max_kv, w["D"])),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        gb.attn_paged_decode_fwd(dq, dk, dv, dt, dl, w["k_scale"], w["v_scale"],
+                                 max_kv_len=max_kv, o=o, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    # A serving loop replays its decode step as a CUDA graph; time the call that way
+    # (both launches, with the merge's programmatic dependency, in one graph).
+    graph = torch.cuda.CUDAGraph()
+    n0 = gb.launch_count()
+    with torch.cuda.graph(graph):
+        call()
+    launches = gb.launch_count() - n0
+    graph.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if gb.device_status() != 0:
+        raise RuntimeError("device status flags set during the decode measurement")
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    nbytes = decode_bytes(w["kv_lens"], w["B"], w["Hq"], w["Hkv"], w["nq"], w["D"],
+                          w["page_size"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "paged_decode_kernel+merge", "bound": "hbm", "achieved": gbs,
+            "unit": "GB/s", "peak": pk["hbm"], "frac": gbs / pk["hbm"],
+            "peak_source": f"{pk['src']} HBM copy bandwidth", "ms_per_launch": ms,
+            "new_tokens_per_s": w["B"] * w["nq"] / (ms * 1e-3), "bytes_per_launch": nbytes,
+            "launches_per_call": launches, "traffic": traffic_for("paged_decode_kernel+merge"),
+            "config": {k: v for k, v in w.items() if k != "seed"},
+            "timing": "CUDA-graph replay of one attn_paged_decode_fwd call, events around each replay",
+            "l2": "256 MB buffer rewritten between launches, outside the timed events"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -388,6 +461,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=20.0)
+    ap.add_argument("--decode", default="on", choices=["on", "off", "only"],
+                    help="paged E4M3 decode measured beside the step (only: print just that)")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count of the dense/VSA workloads (profiling runs)")
     args = ap.parse_args()
@@ -417,6 +492,14 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
+
+    if args.decode == "only":
+        if rank == 0:
+            print(json.dumps(dict(metric="paged decode HBM GB/s", impl="ours", n_gpus=world,
+                                  steps=args.steps, warmup=args.warmup,
+                                  **measure_decode(gb, torch, dev, args.steps, args.warmup,
+                                                   peaks()))))
+        return 0
 
     hosts = {n: host_inputs(n) for n in names}
     wls = [Workload(n, gb, torch, dev, hosts[n]) for n in names]
@@ -564,6 +647,9 @@ def main():
                "ms_per_step": e_ms, "wall_ms_per_step": wall_ms, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
                "overlap": "inputs copied on an H2D stream and results on a D2H stream while other sub-workloads compute"}
+
+    if args.decode == "on" and args.workload == "all":
+        extra["decode"] = measure_decode(gb, torch, dev, args.steps, args.warmup, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

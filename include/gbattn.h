@@ -62,8 +62,10 @@ enum gbattn_device_flag {
                                      kernel stopped early and its output is invalid */
     GBATTN_DEV_BAD_PAGE = 2u,     /* a page-table entry was outside [0, num_phys_pages);
                                      that page's tokens were written as zeros */
-    GBATTN_DEV_BAD_INDEX = 4u     /* a VSA cube list was not strictly ascending or held an
+    GBATTN_DEV_BAD_INDEX = 4u,    /* a VSA cube list was not strictly ascending or held an
                                      index outside [0, S/block); the entry was skipped */
+    GBATTN_DEV_BAD_LENGTH = 8u    /* a decode sequence length was outside [nq, max_kv_len];
+                                     that sequence's rows were written as O = 0, lse = -inf */
 };
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -146,6 +148,45 @@ int attn_causal_prefill_fwd(const void* q, const void* k, const void* v, void* o
 int e4m3_paged_to_fp16(const uint8_t* k_pages, const uint8_t* v_pages, const int32_t* page_table,
                        int num_phys_pages, int page_size, int kv_len, int Hkv, int D,
                        float k_scale, float v_scale, void* k_out, void* v_out, void* stream);
+
+/*
+ * Decode attention over a paged FP8 E4M3 KV cache.
+ * Cites: "Integrate FP32 v37 prefill and exact E4M3 bridge", Implementation (the
+ * exact E4M3 paged -> FP16 bridge and its page table) and Validation (the E4M3
+ * decode wave kernels, the 256000-input decode with shared-KV heads).
+ *   q          : [B][Hq][nq][D] FP16, the nq newest tokens of every sequence
+ *   k_pages,
+ *   v_pages    : [num_phys_pages][page_size][Hkv][D] E4M3 bytes (the bridge's layout)
+ *   page_table : int32 [B][max_pages], row b maps logical page p of sequence b to a
+ *                physical page (entries past ceil(kv_lens[b] / page_size) are not read)
+ *   kv_lens    : int32 [B] on the device, cached tokens per sequence, the new ones included
+ *   o          : [B][Hq][nq][D] FP16; lse optional FP32 [B][Hq][nq] (natural log)
+ *   Query i of sequence b sits at position kv_lens[b] - nq + i and sees the cached
+ *   tokens t <= that position; query head h reads KV head h / (Hq / Hkv).  K and V
+ *   are exactly the bridge's values RNE_fp16(decode(byte) * scale); scores, softmax
+ *   and accumulation are FP32 (probabilities enter the PV product as FP16 hi + lo
+ *   halves), O is rounded to FP16 once.
+ *   D is 128 or 256; page_size a power of two >= 16; Hq % Hkv == 0; B <= 4096;
+ *   nq <= max_kv_len <= max_pages * page_size; num_phys_pages * page_size < 2^31.
+ *   max_kv_len bounds every kv_lens[b]; a length outside [nq, max_kv_len] sets
+ *   GBATTN_DEV_BAD_LENGTH and yields O = 0, lse = -inf for that sequence.  An
+ *   out-of-range page-table entry sets GBATTN_DEV_BAD_PAGE (that page reads
+ *   physical page 0).
+ *   The work (16-token tiles of every sequence, KV head and group of <= 8 query rows)
+ *   is split evenly over the warps of a persistent grid whatever the lengths; each
+ *   warp writes FP32 partial records to `workspace` and a merge kernel combines them.
+ *   The workspace (required) holds one record per warp plus one per (sequence, KV
+ *   head, row group); attn_paged_decode_workspace_size() gives the full-speed size,
+ *   a smaller one runs fewer warps, and below one CTA's worth the call returns
+ *   GBATTN_ERR_WORKSPACE.
+ */
+size_t attn_paged_decode_workspace_size(int B, int Hq, int Hkv, int nq, int max_kv_len, int D);
+int attn_paged_decode_fwd(const void* q, const uint8_t* k_pages, const uint8_t* v_pages,
+                          const int32_t* page_table, const int32_t* kv_lens, void* o, float* lse,
+                          int B, int Hq, int Hkv, int nq, int D, int num_phys_pages,
+                          int page_size, int max_pages, int max_kv_len, float k_scale,
+                          float v_scale, float scale, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /*
  * VSA key-cube selection.

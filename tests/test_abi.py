@@ -117,6 +117,41 @@ def test_bridge_validation(lib):
     assert call() in (CUDA, OK)
 
 
+def test_decode_validation(lib):
+    f = lib.attn_paged_decode_fwd
+    P5, P6 = ctypes.c_void_p(0x70000000), ctypes.c_void_p(0x78000000)
+    # q, k_pages, v_pages, page_table, kv_lens, o, lse, B, Hq, Hkv, nq, D, num_phys,
+    # page_size, max_pages, max_kv_len, k_scale, v_scale, scale, workspace, bytes, stream
+    base = [P, P2, P3, P4, P5, P6, None, 2, 6, 1, 1, 256, 64, 32, 32, 1024, 0.0625, 0.125,
+            0.0625, None, 0, None]
+
+    def call(**kw):
+        a = list(base)
+        for k, v in kw.items():
+            a[int(k[1:])] = v
+        return f(*a)
+    assert call(a0=None) == NULL
+    assert call(a4=None) == NULL
+    assert call(a7=0) == SHAPE
+    assert call(a8=5, a9=2) == SHAPE            # Hq % Hkv
+    assert call(a15=1025) == SHAPE              # max_kv_len > max_pages * page_size
+    assert call(a10=2000) == SHAPE              # nq > max_kv_len
+    assert call(a11=64) == UNSUPPORTED
+    assert call(a13=24, a14=64) == UNSUPPORTED  # page size not a power of two
+    assert call(a13=8, a14=128) == UNSUPPORTED  # page size below 16
+    assert call(a16=0.0) == SCALE
+    assert call(a18=float("nan")) == SCALE
+    assert call(a5=MIS) == ALIGN
+    assert call(a4=ctypes.c_void_p(0x70000002)) == ALIGN
+    assert call(a5=P) == ALIAS
+    assert call(a6=ctypes.c_void_p(0x78000000)) == ALIAS
+    assert call() == WORKSPACE                  # the decode always needs a workspace
+    assert call(a19=ctypes.c_void_p(0x7C000000), a20=1 << 24) in (CUDA, OK)
+    assert call(a7=5000) == UNSUPPORTED         # more sequences than one launch takes
+    assert lib.attn_paged_decode_workspace_size(0, 6, 1, 1, 1024, 256) == 0
+    assert lib.attn_paged_decode_workspace_size(2, 6, 1, 1, 1024, 256) > 0
+
+
 def test_select_and_sparse_validation(lib):
     ws = lib.vsa_select_workspace_size(1, 24, 32768, 128, 64)
     assert ws == 2 * 24 * 512 * 128 * 4
