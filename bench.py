@@ -540,10 +540,12 @@ def main():
     if gb.device_status() != 0:
         raise RuntimeError("device status flags set during the timed region")
 
-    per_call = {}
+    per_call, per_call_cv = {}, {}
     for c, (w, lbl, _) in enumerate(calls):
         t = [ev[s][c][0].elapsed_time(ev[s][c][1]) for s in range(args.steps)]
         per_call[f"{w.name}:{lbl}"] = statistics.median(t)
+        per_call_cv[f"{w.name}:{lbl}"] = (statistics.pstdev(t) / statistics.mean(t)
+                                          if len(t) > 1 else 0.0)
 
     flops_step = sum(w.flops for w in wls)
     value = world * flops_step / (ms * 1e-3) / 1e12
@@ -668,7 +670,8 @@ def main():
                            "parallelism": "replicas" if world > 1 else "single_gpu",
                            "l2": "inputs larger than L2 (about 1.7 GB touched per step), no flush"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-                "clocks": clock_info, "per_call_ms": per_call, "per_variant": per_variant}
+                "clocks": clock_info, "per_call_ms": per_call, "per_call_cv": per_call_cv,
+                "per_variant": per_variant}
         line.update(extra)
         print(json.dumps(line))
     if world > 1:
