@@ -21,7 +21,8 @@ oracle does neither rounding, and the parity tolerance absorbs both.
 Variants ("Integrate FP32 v37 prefill and exact E4M3 bridge", Implementation;
 "Integrate H3 SM70 execution, metrics and VSA diagnostics", Purpose):
 
-* dense      – every key visible (the D128 video-DiT heads).
+* dense      – every key visible (the D128 video-DiT heads); optionally an
+               additive mask term (the "+ mask" of the formula).
 * causal     – query head h reads KV head h // (Hq / Hkv) (shared-KV heads);
                query i of Q_real real queries sits at absolute position
                (KV - Q_real) + i and sees keys j <= that position.  Padded
@@ -43,10 +44,11 @@ def _f64(x):
     return np.asarray(x).astype(np.float64)
 
 
-def attention_rows(q, k, v, scale, visible=None):
+def attention_rows(q, k, v, scale, visible=None, mask=None):
     """Softmax attention for a block of query rows against one key/value set.
 
-    q: [n, D]; k, v: [m, D]; visible: optional bool [n, m].
+    q: [n, D]; k, v: [m, D]; visible: optional bool [n, m]; mask: optional
+    additive term [n, m] (the "+ mask" of the formula; -inf hides a key).
     Returns (o [n, D] float64, lse [n] float64).  A row with no visible key
     gets o = 0 and lse = -inf.
     """
@@ -55,6 +57,8 @@ def attention_rows(q, k, v, scale, visible=None):
     v = _f64(v)
     sc = float(np.float32(scale))
     s = sc * (q @ k.T)
+    if mask is not None:
+        s = s + _f64(mask)
     if visible is not None:
         s = np.where(visible, s, -np.inf)
     m = s.max(axis=1, keepdims=True)
@@ -110,6 +114,28 @@ def dense_attention(q, k, v, scale, rows=None):
     vf = v.reshape(B * H, -1, D)
     groups = _rows_by_head(rows, B * H, Sq)
     results = [attention_rows(qf[h, r], kf[h], vf[h], scale) for h, r in groups]
+    o, lse = _scatter(rows, groups, results, B * H, Sq, D)
+    if rows is None:
+        return o.reshape(B, H, Sq, D), lse.reshape(B, H, Sq)
+    return o, lse
+
+
+def dense_masked_attention(q, k, v, mask, scale, rows=None):
+    """Dense attention with an additive mask: softmax(scale * q.k + mask) v.
+
+    q: [B][H][Sq][D]; k, v: [B][H][Skv][D] (FP16 arrays); mask: FP16 values
+    broadcastable to [B][H][Sq][Skv] (e.g. [Sq][Skv] shared by every head).
+    Entries equal to -inf hide a key; a row whose keys are all hidden gives
+    o = 0, lse = -inf.  rows: as for ``dense_attention``.
+    """
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    mk = np.broadcast_to(np.asarray(mask), (B, H, Sq, Skv)).reshape(B * H, Sq, Skv)
+    qf = q.reshape(B * H, Sq, D)
+    kf = k.reshape(B * H, -1, D)
+    vf = v.reshape(B * H, -1, D)
+    groups = _rows_by_head(rows, B * H, Sq)
+    results = [attention_rows(qf[h, r], kf[h], vf[h], scale, mask=mk[h, r]) for h, r in groups]
     o, lse = _scatter(rows, groups, results, B * H, Sq, D)
     if rows is None:
         return o.reshape(B, H, Sq, D), lse.reshape(B, H, Sq)

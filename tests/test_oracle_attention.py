@@ -206,3 +206,85 @@ def test_sampled_rows_equal_full_evaluation():
         assert np.allclose(os_[n], o[0, h, i], rtol=1e-13, atol=1e-14)
         assert np.isclose(lse[0, h, i], ls[n], rtol=1e-13) or \
             (np.isneginf(ls[n]) and np.isneginf(lse[0, h, i]))
+
+
+# ------------------------------------------------------------------ additive mask
+def _brute_masked(q, k, v, scale, mask):
+    """Pure-Python softmax(scale * q.k + mask) v; -inf entries are skipped."""
+    n, D = q.shape
+    m = k.shape[0]
+    o = np.zeros((n, D))
+    lse = np.zeros(n)
+    sc = float(np.float32(scale))
+    for i in range(n):
+        ws = []
+        for j in range(m):
+            b = float(mask[i, j])
+            if b == -math.inf:
+                continue
+            s = sc * sum(float(q[i, d]) * float(k[j, d]) for d in range(D)) + b
+            ws.append((j, math.exp(s)))
+        if not ws:
+            lse[i] = -math.inf
+            continue
+        tot = sum(w for _, w in ws)
+        for d in range(D):
+            o[i, d] = sum(w * float(v[j, d]) for j, w in ws) / tot
+        lse[i] = math.log(tot)
+    return o, lse
+
+
+def _mask(shape, seed, hide=0.2):
+    rng = np.random.default_rng(seed)
+    m = (rng.standard_normal(shape) * 1.5).astype(np.float16)
+    m[rng.random(shape) < hide] = -np.inf
+    return m
+
+
+def test_masked_brute_force():
+    q, k, v = _rand((1, 2, 5, 8), 60), _rand((1, 2, 9, 8), 61), _rand((1, 2, 9, 8), 62)
+    mask = _mask((5, 9), 63)
+    mask[2] = -np.inf                                   # one fully hidden row
+    o, lse = A.dense_masked_attention(q, k, v, mask, 0.4)
+    for h in range(2):
+        ob, lb = _brute_masked(q[0, h], k[0, h], v[0, h], 0.4, mask)
+        assert np.allclose(o[0, h], ob, rtol=1e-12, atol=1e-13)
+        assert np.array_equal(np.isneginf(lse[0, h]), np.isneginf(lb))
+        fin = np.isfinite(lb)
+        assert np.allclose(lse[0, h][fin], lb[fin], rtol=1e-12, atol=1e-13)
+    assert np.all(o[0, :, 2] == 0)
+
+
+def test_mask_zero_equals_dense_and_inf_equals_visibility():
+    q, k, v = _rand((1, 2, 6, 8), 64), _rand((1, 2, 11, 8), 65), _rand((1, 2, 11, 8), 66)
+    o0, l0 = A.dense_masked_attention(q, k, v, np.zeros((6, 11), np.float16), 0.3)
+    od, ld = A.dense_attention(q, k, v, 0.3)
+    assert np.allclose(o0, od, rtol=1e-14, atol=1e-15) and np.allclose(l0, ld, rtol=1e-14)
+    vis = np.random.default_rng(67).random((6, 11)) < 0.6
+    vis[:, 0] = True
+    om, lm = A.dense_masked_attention(q, k, v, np.where(vis, 0.0, -np.inf).astype(np.float16), 0.3)
+    for h in range(2):
+        ov, lv = A.attention_rows(q[0, h], k[0, h], v[0, h], 0.3, visible=vis)
+        assert np.allclose(om[0, h], ov, rtol=1e-14, atol=1e-15)
+        assert np.allclose(lm[0, h], lv, rtol=1e-14)
+
+
+def test_mask_row_constant_shifts_lse_only():
+    q, k, v = _rand((1, 1, 4, 8), 68), _rand((1, 1, 10, 8), 69), _rand((1, 1, 10, 8), 70)
+    base = _mask((4, 10), 71, hide=0.0)
+    shift = np.array([0.5, -1.25, 2.0, 0.0])[:, None]
+    o1, l1 = A.dense_masked_attention(q, k, v, base, 0.3)
+    o2, l2 = A.dense_masked_attention(q, k, v, (base.astype(np.float64) + shift), 0.3)
+    assert np.allclose(o1, o2, rtol=1e-12, atol=1e-14)
+    assert np.allclose(l2[0, 0] - l1[0, 0], shift[:, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_mask_broadcast_per_head_slices():
+    q, k, v = _rand((2, 3, 4, 8), 72), _rand((2, 3, 7, 8), 73), _rand((2, 3, 7, 8), 74)
+    per_head = _mask((1, 3, 4, 7), 75)
+    o, _ = A.dense_masked_attention(q, k, v, per_head, 0.5)
+    for b in range(2):
+        for h in range(3):
+            oh, _ = A.dense_masked_attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                             v[b:b + 1, h:h + 1], per_head[0, h], 0.5)
+            assert np.allclose(o[b, h], oh[0, 0], rtol=1e-14, atol=1e-15)
