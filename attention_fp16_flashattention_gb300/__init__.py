@@ -31,6 +31,8 @@ _SIGNATURES = {
     "gbattn_launch_count": (ctypes.c_uint64, []),
     "gbattn_test_inject_fault": (_i, [_i]),
     "attn_dense_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "attn_dense_mask_fwd": (_i, [_vp, _vp, _vp, _vp, ctypes.c_longlong, ctypes.c_longlong, _vp, _vp,
+                                 _i, _i, _i, _i, _i, _f, _vp]),
     "attn_causal_prefill_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "attn_causal_prefill_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                                      _vp, _sz, _vp]),
@@ -146,6 +148,36 @@ def attn_dense_fwd(q, k, v, o=None, lse=None, scale=None, stream=None):
     rc = load().attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Skv, D,
                                _scale(scale, D), _stream(stream))
     _check("attn_dense_fwd", rc)
+    return o
+
+
+def attn_dense_mask_fwd(q, k, v, mask, o=None, lse=None, scale=None, stream=None):
+    """Dense attention with an additive FP16 mask broadcastable to [B,H,Sq,Skv]
+    (rows of Skv contiguous; a size-1 batch or head dimension is shared)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.float16, 4)
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    if tuple(k.shape) != (B, H, Skv, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, H, Skv, D] matching q")
+    if not isinstance(mask, torch.Tensor) or not mask.is_cuda or mask.dtype != torch.float16:
+        raise ValueError("mask must be a CUDA float16 tensor")
+    m4 = mask.reshape((1, 1) + tuple(mask.shape)) if mask.dim() == 2 else mask
+    if m4.dim() != 4 or tuple(m4.shape[2:]) != (Sq, Skv) or m4.shape[0] not in (1, B) \
+            or m4.shape[1] not in (1, H):
+        raise ValueError("mask must broadcast to [B, H, Sq, Skv]")
+    if m4.stride(3) != 1 or m4.stride(2) != Skv:
+        raise ValueError("mask rows must be contiguous [Sq][Skv]")
+    sb = m4.stride(0) if m4.shape[0] > 1 else 0
+    sh = m4.stride(1) if m4.shape[1] > 1 else 0
+    o = torch.empty_like(q) if o is None else o
+    _need(o, "o", torch.float16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    rc = load().attn_dense_mask_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(m4), sb, sh, _ptr(o), _ptr(lse),
+                                    B, H, Sq, Skv, D, _scale(scale, D), _stream(stream))
+    _check("attn_dense_mask_fwd", rc)
     return o
 
 

@@ -83,6 +83,20 @@ int encode_tmap_f16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
     return r == CUDA_SUCCESS ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
+int encode_tmap_f16_mask(CUtensorMap* map, const void* base, uint64_t skv, uint64_t sq,
+                         uint64_t heads, uint64_t batch, uint64_t stride_h, uint64_t stride_b) {
+    if (load_encoder() != GBATTN_OK) return GBATTN_ERR_CUDA;
+    cuuint64_t dims[4] = {skv, sq, heads, batch};
+    cuuint64_t strides[3] = {skv * 2, stride_h * 2, stride_b * 2};   // bytes, dims 1..3
+    cuuint32_t box[4] = {64, 32, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
 int encode_tmap_u8_pages(CUtensorMap* map, const void* base, uint64_t D, uint64_t hkv,
                          uint64_t rows, uint32_t box_rows) {
     if (load_encoder() != GBATTN_OK) return GBATTN_ERR_CUDA;

@@ -48,7 +48,8 @@ constexpr int kMaxSparseTiles = 512;
 constexpr int kMaxTopk = 512;
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s for draining after an abort
 
-enum Mode { kDense = 0, kCausal = 1, kSparse = 2 };
+// kMasked: dense with an additive FP16 mask [Sq][Skv] per (batch, head) slice.
+enum Mode { kDense = 0, kCausal = 1, kSparse = 2, kMasked = 3 };
 
 struct AttnArgs {
     int seq_q;          // query rows per head
@@ -63,19 +64,24 @@ struct AttnArgs {
     int n_cubes;        // sparse: S / 64
     int topk;           // sparse
     float scale_log2;   // scale * log2(e)
+    float scale;        // masked: the softmax scale itself
     __half* o;
     float* lse;         // optional natural-log LSE
     float* part_o;      // causal, n_chunks > 1: [C][heads_q][seq_q][D] FP32, normalised
     float* part_lse;    // causal, n_chunks > 1: [C][heads_q][seq_q] log2-sum-exp2
     const int32_t* idx; // sparse: [heads][n_cubes][topk]
+    const __half* mask; // masked: additive mask, row stride seq_k
+    long long mask_sb;  // masked: elements between batch slices (0 = shared)
+    long long mask_sh;  // masked: elements between head slices (0 = shared)
     uint32_t* status;
     uint64_t wait_limit;
     int fault;          // test hook: 1 = the TMA warp never loads Q (exercises the timeout path)
 };
 
-template <int D>
+template <int D, int MODE>
 struct Cfg {
-    static constexpr int NS = D == 128 ? 4 : 2;          // K/V ring slots
+    // K/V ring slots (the masked mode gives one D=128 slot to its mask stages)
+    static constexpr int NS = D == 128 ? (MODE == 3 ? 3 : 4) : 2;
     static constexpr int NSB = D == 128 ? 3 : 2;         // S buffers in TMEM (QK lookahead)
     static constexpr int CHUNK = 128 * 128;               // 128 rows x 64 FP16 columns
     static constexpr int HALF = 64 * 128;                 // 64 rows x 64 columns
@@ -123,10 +129,18 @@ struct SparseTiles {
     uint8_t mask[kMaxSparseTiles];
 };
 
+// Masked mode: every softmax warp stages the mask of its 32 rows x 64 keys of a
+// tile (4 KB, TMA, 128-byte swizzle) in two slots, two tiles ahead; the 16
+// slot barriers follow the stages.
+constexpr int kMaskSlotBytes = 32 * 128;
+constexpr int kMaskStageBytes = 8 * 2 * kMaskSlotBytes + 16 * 8;
+
 template <int D, int MODE>
 constexpr int smem_bytes() {
-    return 1024 + Cfg<D>::Q_BYTES + Cfg<D>::NS * Cfg<D>::SLOT_BYTES + kCtrlBytes +
-           (MODE == kSparse ? static_cast<int>(sizeof(SparseTiles)) : 0);
+    using C = Cfg<D, MODE>;
+    return 1024 + C::Q_BYTES + C::NS * C::SLOT_BYTES + kCtrlBytes +
+           (MODE == kSparse ? static_cast<int>(sizeof(SparseTiles)) : 0) +
+           (MODE == kMasked ? kMaskStageBytes : 0);
 }
 
 // Bounded wait that ignores the abort flag (used only to drain after an abort).
@@ -216,19 +230,27 @@ __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
-    using C = Cfg<D>;
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmM,
+                    const AttnArgs a) {
+    using C = Cfg<D, MODE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sQ = smem;
     uint8_t* sKV = smem + C::Q_BYTES;
-    Ctrl* ctrl = reinterpret_cast<Ctrl*>(sKV + C::NS * C::SLOT_BYTES);
+    // masked mode: mask stages (1024-aligned) and their barriers after the ring
+    uint8_t* sMask = sKV + C::NS * C::SLOT_BYTES;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sMask + 8 * 2 * kMaskSlotBytes);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(sKV + C::NS * C::SLOT_BYTES +
+                                         (MODE == kMasked ? kMaskStageBytes : 0));
     Exchange* ex = reinterpret_cast<Exchange*>(reinterpret_cast<uint8_t*>(ctrl) + 256);
     SparseTiles* st = reinterpret_cast<SparseTiles*>(reinterpret_cast<uint8_t*>(ctrl) + kCtrlBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.y;
+    // Masked mode runs heads fastest (grid (B*H, tiles)) so that the CTAs of all
+    // heads of a query tile run together and share that tile's mask rows in L2.
+    const int bh = MODE == kMasked ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
+    const int qtile = MODE == kMasked ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
 
     // ---- work decode
     int q_row0, kv_bh, n_tiles = 0, tile0 = 0, chunk = 0;
@@ -244,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile0 = static_cast<int>(static_cast<long long>(chunk) * T / a.n_chunks);
         n_tiles = static_cast<int>(static_cast<long long>(chunk + 1) * T / a.n_chunks) - tile0;
     } else {
-        q_row0 = blockIdx.x * BM;
+        q_row0 = qtile * BM;
         kv_bh = bh;
-        if (MODE == kDense) n_tiles = (a.seq_k + BN - 1) / BN;
+        if (MODE == kDense || MODE == kMasked) n_tiles = (a.seq_k + BN - 1) / BN;
     }
 
     // ---- prologue
@@ -262,6 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < C::NSB; ++i) mbar_init(&ctrl->pv_done[i], 1);
         for (int i = 0; i < 4; ++i) mbar_init(&ctrl->xchg[i], 64);
+        if (MODE == kMasked)
+            for (int i = 0; i < 16; ++i) mbar_init(&mbar[i], 1);
         mbar_init(&ctrl->drain, 1);
         ctrl->abort = 0;
         mbar_init_fence();
@@ -271,8 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
+            if (MODE == kMasked) tma_prefetch_desc(&tmM);
         }
-        if (MODE == kSparse) build_sparse_tiles(st, ctrl, a, bh, blockIdx.x);
+        if (MODE == kSparse) build_sparse_tiles(st, ctrl, a, bh, qtile);
         __syncwarp();
     }
     if (warp == 1) {
@@ -430,11 +455,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                              ? static_cast<int>(min(static_cast<long long>(a.seq_k),
                                                     static_cast<long long>(a.kv_prefix) + q_row0 + 1))
                              : a.seq_k;
-        const float sl2 = a.scale_log2;
+        // Exponent factor: scores arrive raw (scale*log2e applies), or in masked
+        // mode as y = scale*s + mask (log2e applies).
+        const float sl2 = MODE == kMasked ? 1.4426950408889634f : a.scale_log2;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         float m_run = -INFINITY, l = 0.0f;
         uint32_t xphase = 0;
         bool ok = true;
+        // Masked mode: this warp's 32 rows x 64 keys of the mask for tile t
+        // arrive by TMA in slot t % 2 (issued two tiles ahead by one lane).
+        const int sw = warp - 2;
+        uint8_t* mslots = sMask + sw * 2 * kMaskSlotBytes;
+        uint64_t* mb = mbar + sw * 2;
+        const int mb_b = bh / a.hq, mb_h = bh - mb_b * a.hq;
+        int m_issued = 0;
+        auto mask_issue = [&](int t) {
+            int f0, f1;
+            tile_keys(t, f0, f1);
+            const int kh = half ? f1 : f0;
+            if (elect_one()) {
+                mbar_arrive_expect_tx(&mb[t & 1], kMaskSlotBytes);
+                tma_load_4d(mslots + (t & 1) * kMaskSlotBytes, &tmM, &mb[t & 1], kh,
+                            q_row0 + quarter * 32, a.mask_sh ? mb_h : 0, a.mask_sb ? mb_b : 0);
+            }
+            __syncwarp();
+            ++m_issued;
+        };
+        if (MODE == kMasked && n_tiles > 0) {
+            mask_issue(0);
+            if (n_tiles > 1) mask_issue(1);
+        }
         for (int j = 0; j < n_tiles; ++j) {
             const int buf = j % C::NSB;
             const uint32_t sbuf = tl + buf * 128;
@@ -448,7 +498,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             int k0, k1;
             tile_keys(j, k0, k1);
-            if (MODE == kSparse) {
+            if (MODE == kMasked) {
+                // y = scale * s + mask, then hidden keys -> -inf.
+                ok = wait_warp(&mb[j & 1], (j >> 1) & 1, w);
+                if (!ok) break;
+                const uint64_t sc2 = f2_pack(a.scale, a.scale);
+                const uint8_t* mrow = mslots + (j & 1) * kMaskSlotBytes + lane * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 mv = *reinterpret_cast<const uint4*>(mrow + ((c ^ (lane & 7)) << 4));
+                    const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 4 * c + e;   // key pair 2i, 2i+1
+                        const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mw[e]));
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                         sc2, f2_pack(mf.x, mf.y)),
+                                  x0, x1);
+                        s[2 * i] = __float_as_uint(x0);
+                        s[2 * i + 1] = __float_as_uint(x1);
+                    }
+                }
+                if (j + 2 < n_tiles) mask_issue(j + 2);   // into the slot just read
+                const int kh = half ? k1 : k0;
+                if (kh + 64 > a.seq_k || row_g >= a.seq_q) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (kh + c >= a.seq_k || row_g >= a.seq_q) s[c] = __float_as_uint(-INFINITY);
+                }
+            } else if (MODE == kSparse) {
                 const uint32_t mk = st->mask[j];
                 if (!((mk >> (row_half * 2 + half)) & 1u)) {
 #pragma unroll
@@ -540,6 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&ctrl->p_full[buf]);
+        }
+        if (MODE == kMasked && !ok && lane == 0) {   // mask copies in flight must land first
+            for (int t = max(0, m_issued - 2); t < m_issued; ++t) drain_wait(&mb[t & 1], (t >> 1) & 1);
         }
         if (ok && n_tiles > 0) {
             ok = wait_warp(&ctrl->pv_done[(n_tiles - 1) % C::NSB], ((n_tiles - 1) / C::NSB) & 1, w);
@@ -675,7 +757,8 @@ int set_smem_attr() {
 
 template <int D, int MODE>
 int launch_attn(const void* q, const void* k, const void* v, int seq_q, int seq_k, int heads_q,
-                int heads_kv, dim3 grid, AttnArgs args, cudaStream_t stream) {
+                int heads_kv, dim3 grid, AttnArgs args, cudaStream_t stream,
+                const CUtensorMap* mask_map = nullptr) {
     CUtensorMap tq, tk, tv;
     if (encode_tmap_f16_3d(&tq, q, D, seq_q, heads_q, 64, BM) != GBATTN_OK ||
         encode_tmap_f16_3d(&tk, k, D, seq_k, heads_kv, 64, 64) != GBATTN_OK ||
@@ -683,7 +766,8 @@ int launch_attn(const void* q, const void* k, const void* v, int seq_q, int seq_
         return GBATTN_ERR_CUDA;
     int rc = set_smem_attr<D, MODE>();
     if (rc != GBATTN_OK) return rc;
-    attn_fwd_kernel<D, MODE><<<grid, kThreads, smem_bytes<D, MODE>(), stream>>>(tq, tk, tv, args);
+    attn_fwd_kernel<D, MODE><<<grid, kThreads, smem_bytes<D, MODE>(), stream>>>(
+        tq, tk, tv, mask_map ? *mask_map : tq, args);
     count_launches(1);
     return launch_status();
 }
@@ -694,6 +778,7 @@ AttnArgs base_args(const DeviceState& dev, float scale) {
     AttnArgs a{};
     a.fault = g_fault_mode;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.scale = scale;
     a.status = dev.status;
     a.wait_limit = wait_limit_ns();
     a.group = 1;
@@ -779,6 +864,61 @@ extern "C" int attn_dense_fwd(const void* q, const void* k, const void* v, void*
     dim3 grid((Sq + BM - 1) / BM, B * H);
     return launch_attn<128, kDense>(q, k, v, Sq, Skv, B * H, B * H, grid, a,
                                     static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_dense_mask_fwd(const void* q, const void* k, const void* v, const void* mask,
+                                   long long mask_stride_b, long long mask_stride_h, void* o,
+                                   float* lse, int B, int H, int Sq, int Skv, int D, float scale,
+                                   void* stream) {
+    if (!q || !k || !v || !mask || !o) return GBATTN_ERR_NULL;
+    if (B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0) return GBATTN_ERR_SHAPE;
+    if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
+    const long long slice = static_cast<long long>(Sq) * Skv;
+    if (mask_stride_b < 0 || mask_stride_h < 0 || Skv % 8 != 0 || mask_stride_b % 8 != 0 ||
+        mask_stride_h % 8 != 0 || (mask_stride_h != 0 && mask_stride_h < slice) ||
+        (mask_stride_b != 0 && mask_stride_b < slice))
+        return GBATTN_ERR_SHAPE;
+    if (D != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(mask) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return GBATTN_ERR_ALIGN;
+    const size_t qb = static_cast<size_t>(B) * H * Sq * D * 2;
+    const size_t kb = static_cast<size_t>(B) * H * Skv * D * 2;
+    const size_t lb = static_cast<size_t>(B) * H * Sq * 4;
+    const size_t mb = (static_cast<size_t>(B - 1) * mask_stride_b +
+                       static_cast<size_t>(H - 1) * mask_stride_h +
+                       static_cast<size_t>(Sq) * Skv) * 2;
+    if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kb) || overlaps(o, qb, v, kb) ||
+        overlaps(o, qb, mask, mb) || overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) ||
+        overlaps(lse, lb, v, kb) || overlaps(lse, lb, mask, mb) || overlaps(lse, lb, o, qb))
+        return GBATTN_ERR_ALIAS;
+    DeviceState dev;
+    int rc = current_device(&dev);
+    if (rc != GBATTN_OK) return rc;
+    AttnArgs a = base_args(dev, scale);
+    a.seq_q = Sq;
+    a.seq_k = Skv;
+    a.heads_q = B * H;
+    a.hq = H;
+    a.hkv = H;
+    a.n_chunks = 1;
+    a.o = static_cast<__half*>(o);
+    a.lse = lse;
+    a.mask = static_cast<const __half*>(mask);
+    a.mask_sb = mask_stride_b;
+    a.mask_sh = mask_stride_h;
+    // Mask map [b][h][Sq][Skv]; a shared dimension has extent 1 (its stride is
+    // then only a placeholder the encoder accepts).
+    const uint64_t hm = mask_stride_h ? H : 1, bm = mask_stride_b ? B : 1;
+    const uint64_t sh = mask_stride_h ? mask_stride_h : slice;
+    const uint64_t sb = mask_stride_b ? mask_stride_b : sh * hm;
+    CUtensorMap tm;
+    if (encode_tmap_f16_mask(&tm, mask, Skv, Sq, hm, bm, sh, sb) != GBATTN_OK)
+        return GBATTN_ERR_CUDA;
+    dim3 grid(B * H, (Sq + BM - 1) / BM);
+    return launch_attn<128, kMasked>(q, k, v, Sq, Skv, B * H, B * H, grid, a,
+                                     static_cast<cudaStream_t>(stream), &tm);
 }
 
 extern "C" size_t attn_causal_prefill_workspace_size(int B, int Hq, int Q_pad, int KV, int D) {

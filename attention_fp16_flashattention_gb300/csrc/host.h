@@ -30,6 +30,13 @@ void count_launches(int n);
 int encode_tmap_f16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint32_t box0, uint32_t box1);
 
+// Encode a 4-D FP16 tensor map over additive-mask slices [batch][heads][sq][skv]
+// (element strides stride_h, stride_b between slices; size-1 dimensions are
+// shared) with a box of 64 keys x 32 rows and the 128-byte swizzle.  Returns
+// GBATTN_OK or GBATTN_ERR_CUDA.
+int encode_tmap_f16_mask(CUtensorMap* map, const void* base, uint64_t skv, uint64_t sq,
+                         uint64_t heads, uint64_t batch, uint64_t stride_h, uint64_t stride_b);
+
 // Encode a 3-D byte tensor map over paged rows [rows][hkv][D] (D bytes per
 // row and head) with a box of 128 bytes x 1 head x box_rows rows and the
 // 128-byte swizzle.  Returns GBATTN_OK or GBATTN_ERR_CUDA.

@@ -18,6 +18,8 @@ with 64-token cubes and top-k 64):
   paged_e4m3    B1 Hq6 Hkv1 D256, Q=8192 at the tail of KV=131072, K/V as
                 E4M3 bytes uniform over the 254 finite codes in 32-token pages
                 behind a random page-table permutation; scales 1/16 and 1/8
+  dense_masked  B1 H24 S8192 D128, Q/K/V ~ N(0,1), one FP16 additive mask
+                [8192][8192] shared by all heads: -2^-9 |i - j| plus 3% hidden keys
   paged_decode  B4 Hq6 Hkv1 D256, one new token per sequence over ragged
                 caches of 131072, 122887, 98313 and 65571 tokens (K/V bytes and
                 pages as paged_e4m3, every sequence's pages scattered over one
@@ -33,7 +35,7 @@ import math
 import numpy as np
 
 TAGS = {"q": 1, "k": 2, "v": 3, "kpages": 4, "vpages": 5, "table": 6,
-        "qmean": 7, "kmean": 8, "qsig": 9, "ksig": 10, "rows": 11}
+        "qmean": 7, "kmean": 8, "qsig": 9, "ksig": 10, "rows": 11, "mask": 12}
 
 
 def _rng(seed, tag):
@@ -210,6 +212,19 @@ def paged_decode_inputs(B, Hq, Hkv, nq, kv_lens, D, seed, page_size=32, spare_pa
     return q, kp, vp, table, kv_lens
 
 
+def additive_mask(Sq, Skv, seed, hidden_keys=0.03, slope=2.0 ** -9):
+    """FP16 additive mask [Sq][Skv]: a relative-position bias -slope*|i - j| (the
+    linear distance bias of ALiBi-style attention) plus a seeded set of hidden
+    key columns (about hidden_keys of them, -inf), as key padding would give."""
+    i = np.arange(Sq, dtype=np.float32)[:, None]
+    j = np.arange(Skv, dtype=np.float32)[None, :]
+    m = (-np.float32(slope) * np.abs(i - j)).astype(np.float16)
+    hide = _rng(seed, "mask").random(Skv) < hidden_keys
+    hide[0] = False
+    m[:, hide] = -np.inf
+    return m
+
+
 def sample_rows(n_heads, n_rows, count, seed, row_limit=None):
     """``count`` distinct seeded (head, row) pairs, sorted; rows < row_limit."""
     lim = n_rows if row_limit is None else row_limit
@@ -220,7 +235,7 @@ def sample_rows(n_heads, n_rows, count, seed, row_limit=None):
     return np.stack([pick // lim, pick % lim], axis=1).astype(np.int64)
 
 
-# The six workloads, with their seeds (1000 + workload number).
+# The seven workloads, with their seeds (1000 + workload number).
 WORKLOADS = {
     "dense_small": dict(kind="dense", B=1, H=2, S=256, D=128, seed=1001),
     "causal_small": dict(kind="causal", B=1, Hq=6, Hkv=1, Q=1024, KV=4096, D=256, seed=1002),
@@ -229,6 +244,7 @@ WORKLOADS = {
                       seed=1004),
     "paged_e4m3": dict(kind="paged", B=1, Hq=6, Hkv=1, Q=8192, KV=131072, D=256, page_size=32,
                        k_scale=0.0625, v_scale=0.125, seed=1005),
+    "dense_masked": dict(kind="masked", B=1, H=24, S=8192, D=128, seed=1007),
     "paged_decode": dict(kind="decode", B=4, Hq=6, Hkv=1, nq=1,
                          kv_lens=(131072, 122887, 98313, 65571), D=256, page_size=32,
                          k_scale=0.0625, v_scale=0.125, seed=1006),

@@ -15,10 +15,12 @@ done between steps.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
         [--workload all|dense_video|vsa_video|paged_e4m3|dense_small|causal_small]
-        [--decode on|off|only]
+        [--decode on|off|only] [--masked on|off|only]
 Beside the step, the paged E4M3 decode (4 ragged sequences of 65571..131072
 cached tokens, Hq6 Hkv1 D256, one new token each; attn_paged_decode_fwd) is
-timed on its own and reported as "decode" with its HBM roofline.
+timed on its own and reported as "decode" with its HBM roofline, and dense attention
+with an additive mask (B1 H24 S8192 D128, one FP16 [8192][8192] mask shared by the
+heads; attn_dense_mask_fwd) as "masked".
 For N > 1 (torchrun, one process per GPU) every rank runs the same step on its
 own GPU (independent replicas, no data-path communication); the time is the
 maximum over ranks and the value counts the work of all ranks.
@@ -234,6 +236,7 @@ KERNEL_SOURCES = {
     "attn_fwd_kernel<256,causal>+merge": ("attn.cu", "ptx.cuh", "host.h"),
     "e4m3_bridge_kernel": ("bridge.cu", "e4m3.cuh", "ptx.cuh", "host.h"),
     "paged_decode_kernel+merge": ("decode.cu", "e4m3.cuh", "ptx.cuh", "host.h"),
+    "attn_fwd_kernel<128,masked>": ("attn.cu", "ptx.cuh", "host.h"),
 }
 
 
@@ -451,6 +454,54 @@ def measure_decode(gb, torch, dev, steps, warmup, pk):
             "l2": "256 MB buffer rewritten between launches, outside the timed events"}
 
 
+def measure_masked(gb, torch, dev, steps, warmup, pk):
+    """Dense attention with an additive mask (B1 H24 S8192 D128, one FP16 mask
+    [8192][8192] shared by the heads), timed on its own; useful FLOP count only
+    the visible (query, key) pairs.  A 256 MB buffer is rewritten between launches."""
+    w = inputs.WORKLOADS["dense_masked"]
+    q, k, v = inputs.dense_inputs(w["B"], w["H"], w["S"], w["D"], w["seed"])
+    mask = inputs.additive_mask(w["S"], w["S"], w["seed"])
+    visible = int(np.isfinite(mask).sum())
+    T = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    dq, dk, dv, dm = T(q), T(k), T(v), T(mask)
+    o = torch.empty_like(dq)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        gb.attn_dense_mask_fwd(dq, dk, dv, dm, o=o)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    n0 = gb.launch_count()
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    launches = (gb.launch_count() - n0) // steps
+    if gb.device_status() != 0:
+        raise RuntimeError("device status flags set during the masked measurement")
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    flops = 4.0 * w["D"] * w["B"] * w["H"] * visible
+    tf = flops / (ms * 1e-3) / 1e12
+    peak = pk["tc"] or pk["tc_sust"]
+    mask_bytes = 2 * w["S"] * w["S"]
+    return {"kernel": "attn_fwd_kernel<128,masked>", "bound": "tensor", "achieved": tf,
+            "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
+            "peak_source": f"{pk['src']} bf16 burst (kernel timed alone; fp16 dense rate = bf16 rate)",
+            "ms_per_launch": ms, "useful_flop": flops, "visible_pairs_per_head": visible,
+            "mask_bytes": mask_bytes,
+            "mask_read_gbs_if_once_per_head": w["H"] * mask_bytes / (ms * 1e-3) / 1e9,
+            "launches_per_call": launches, "traffic": traffic_for("attn_fwd_kernel<128,masked>"),
+            "config": {k2: v2 for k2, v2 in w.items() if k2 != "seed"},
+            "l2": "256 MB buffer rewritten between launches, outside the timed events"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -463,6 +514,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--decode", default="on", choices=["on", "off", "only"],
                     help="paged E4M3 decode measured beside the step (only: print just that)")
+    ap.add_argument("--masked", default="on", choices=["on", "off", "only"],
+                    help="dense attention with an additive mask measured beside the step")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count of the dense/VSA workloads (profiling runs)")
     args = ap.parse_args()
@@ -493,6 +546,13 @@ def main():
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
 
+    if args.masked == "only":
+        if rank == 0:
+            print(json.dumps(dict(metric="masked dense attention useful TFLOP/s", impl="ours",
+                                  n_gpus=world, steps=args.steps, warmup=args.warmup,
+                                  **measure_masked(gb, torch, dev, args.steps, args.warmup,
+                                                   peaks()))))
+        return 0
     if args.decode == "only":
         if rank == 0:
             print(json.dumps(dict(metric="paged decode HBM GB/s", impl="ours", n_gpus=world,
@@ -652,6 +712,8 @@ def main():
 
     if args.decode == "on" and args.workload == "all":
         extra["decode"] = measure_decode(gb, torch, dev, args.steps, args.warmup, pk)
+    if args.masked == "on" and args.workload == "all":
+        extra["masked"] = measure_masked(gb, torch, dev, args.steps, args.warmup, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

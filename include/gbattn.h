@@ -150,6 +150,22 @@ int e4m3_paged_to_fp16(const uint8_t* k_pages, const uint8_t* v_pages, const int
                        float k_scale, float v_scale, void* k_out, void* v_out, void* stream);
 
 /*
+ * Dense attention with an additive mask: O = softmax(scale * Q K^T + mask) V.
+ * Cites: the mask term of the attention formula; FastVideo compare view,
+ * minimax_h3_fusions/block_lists.py (H3's mask builder: square masks over the
+ * score matrix per batch entry and head).
+ *   q, o : [B][H][Sq][D] FP16; k, v : [B][H][Skv][D] FP16; lse optional FP32 [B][H][Sq].
+ *   mask : FP16; the slice of (b, h) starts at mask + b*mask_stride_b + h*mask_stride_h
+ *          (element strides; 0 shares one slice) and is [Sq][Skv] row-major.  -inf hides a
+ *          key; a row whose keys are all hidden gets O = 0, lse = -inf.
+ *   D == 128; Skv and both strides multiples of 8 (16-byte rows); mask 16-byte aligned.
+ *   Mask bytes are read once per query tile per (b, h) slice use: 2*Sq*Skv per head.
+ */
+int attn_dense_mask_fwd(const void* q, const void* k, const void* v, const void* mask,
+                        long long mask_stride_b, long long mask_stride_h, void* o, float* lse,
+                        int B, int H, int Sq, int Skv, int D, float scale, void* stream);
+
+/*
  * Decode attention over a paged FP8 E4M3 KV cache.
  * Cites: "Integrate FP32 v37 prefill and exact E4M3 bridge", Implementation (the
  * exact E4M3 paged -> FP16 bridge and its page table) and Validation (the E4M3

@@ -117,6 +117,28 @@ def test_bridge_validation(lib):
     assert call() in (CUDA, OK)
 
 
+def test_dense_mask_validation(lib):
+    f = lib.attn_dense_mask_fwd
+    # q, k, v, mask, stride_b, stride_h, o, lse, B, H, Sq, Skv, D, scale, stream
+    base = [P, P2, P3, ctypes.c_void_p(0x70000000), 0, 0, P4, None, 1, 2, 256, 256, 128, 0.088, None]
+
+    def call(i=None, val=None):
+        a = list(base)
+        if i is not None:
+            a[i] = val
+        return f(*a)
+    assert call(3, None) == NULL
+    assert call(11, 260) == SHAPE              # mask rows must be 16-byte multiples
+    assert call(5, 12) == SHAPE                # head stride not a multiple of 8
+    assert call(5, 8) == SHAPE                 # head slices overlapping
+    assert call(4, -8) == SHAPE
+    assert call(12, 64) == UNSUPPORTED
+    assert call(13, 0.0) == SCALE
+    assert call(3, MIS) == ALIGN
+    assert call(6, ctypes.c_void_p(0x70000000)) == ALIAS
+    assert call() in (CUDA, OK)
+
+
 def test_decode_validation(lib):
     f = lib.attn_paged_decode_fwd
     P5, P6 = ctypes.c_void_p(0x70000000), ctypes.c_void_p(0x78000000)
