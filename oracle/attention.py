@@ -170,29 +170,49 @@ def causal_prefill_attention(q, k, v, scale, q_real, rows=None):
     return o, lse
 
 
-def vsa_sparse_attention(q, k, v, idx, block, scale, rows=None):
-    """Block-sparse attention over selected key cubes.
+def vsa_sparse_attention(q, k, v, idx, block, scale, rows=None, valid=None, prefix=0):
+    """Block-sparse attention over selected key cubes (the full VSA layout).
 
-    q, k, v: [B][H][S][D] FP16 in cube-major token order (cube c = tokens
-    c*block .. c*block+block-1); idx: int [B][H][S/block][topk], the key cubes
-    each query cube attends.  Query token i attends exactly the tokens of the
-    cubes idx[b, h, i // block, :] (a gather of those keys, then ordinary
-    softmax attention over them).
+    q, k, v: [B][H][S][D] FP16.  Tokens [0, prefix) are prefix tokens (text or
+    audio, not in cubes); tokens [prefix, S) are the video tokens in
+    cube-major order, cube c = slots prefix + c*block .. + block - 1, of which
+    the first valid[c] are real and the rest padding (valid None: full cubes).
+    idx: int [B][H][(S - prefix)/block][topk], the key cubes each video query
+    cube attends.
+
+    * A prefix query (row < prefix) attends densely to every prefix token and
+      every real video token ("prefix-dense queries").
+    * A real video query in cube c attends exactly the real tokens of the
+      cubes idx[b, h, c, :] (a gather of those keys, then ordinary softmax).
+    * A padding query slot gives o = 0, lse = -inf.
     """
     B, H, S, D = q.shape
+    nc = (S - prefix) // block
+    val = np.full(nc, block, dtype=np.int64) if valid is None else np.asarray(valid, np.int64)
     qf = q.reshape(B * H, S, D)
     kf = k.reshape(B * H, S, D)
     vf = v.reshape(B * H, S, D)
-    idxf = np.asarray(idx).reshape(B * H, S // block, -1)
+    idxf = np.asarray(idx).reshape(B * H, nc, -1)
+    real_video = np.concatenate([prefix + c * block + np.arange(val[c]) for c in range(nc)])
+    all_keys = np.concatenate([np.arange(prefix), real_video]).astype(np.int64)
     groups = _rows_by_head(rows, B * H, S)
     results = []
     for bh, r in groups:
         o_h = np.zeros((len(r), D))
-        l_h = np.zeros(len(r))
-        cubes = r // block
+        l_h = np.full(len(r), -np.inf)
+        pre = np.nonzero(r < prefix)[0]
+        if pre.size:
+            o_h[pre], l_h[pre] = attention_rows(qf[bh, r[pre]], kf[bh, all_keys], vf[bh, all_keys],
+                                                scale)
+        vid = np.nonzero(r >= prefix)[0]
+        cubes = (r[vid] - prefix) // block
+        slots = (r[vid] - prefix) % block
         for c in np.unique(cubes):
-            sel = np.nonzero(cubes == c)[0]
-            toks = (idxf[bh, c][:, None] * block + np.arange(block)[None, :]).reshape(-1)
+            sel = vid[(cubes == c) & (slots < val[c])]
+            if sel.size == 0:
+                continue
+            toks = np.concatenate([prefix + kc * block + np.arange(val[kc])
+                                   for kc in idxf[bh, c]]).astype(np.int64)
             o_c, l_c = attention_rows(qf[bh, r[sel]], kf[bh, toks], vf[bh, toks], scale)
             o_h[sel] = o_c
             l_h[sel] = l_c

@@ -25,6 +25,11 @@ Readings where the pages are silent (each listed in the design notes):
   precision and order; this is that order.
 * Ties: the lower key-cube index wins; the selected set is reported in
   ascending key-cube order.
+* Boundary cubes ("boundary handling"; the tile valid counts of the pages'
+  pooling and block-list code): a cube holds ``valid[c]`` real tokens in its
+  first slots and padding after them; pooling sums and divides by the real
+  tokens only.  Prefix tokens (text/audio before the video tokens) are not
+  in cubes and take no part in the selection.
 """
 
 import numpy as np
@@ -33,19 +38,23 @@ import numpy as np
 def pool_means_fp32(x, block, count=None):
     """FP32 cube means.  x: [..., S, D] FP16 (cube-major) -> [..., S/block, D] FP32.
 
-    sum_t is accumulated in token order with an FP32 rounding after every
-    addition, then divided by the valid count (default: ``block``) with an
-    FP32 correctly rounded division.
+    count: None (every cube full), or per-cube valid-token counts [S/block]
+    (boundary cubes of a grid that the cube size does not divide: the valid
+    tokens are the first ``count[c]`` slots of cube c, the rest is padding whose
+    contents are ignored).  sum_t over the valid tokens is accumulated in token
+    order with an FP32 rounding after every addition, then divided by the
+    count with an FP32 correctly rounded division.
     """
     x = np.asarray(x)
     *lead, S, D = x.shape
     nc = S // block
+    cnt = np.full(nc, block, dtype=np.int64) if count is None else np.asarray(count, np.int64)
     xs = x.reshape(*lead, nc, block, D).astype(np.float32)
     acc = np.zeros((*lead, nc, D), dtype=np.float32)
     for t in range(block):
-        acc = np.add(acc, xs[..., t, :], dtype=np.float32)
-    cnt = np.float32(block if count is None else count)
-    return np.divide(acc, cnt, dtype=np.float32)
+        live = (t < cnt)[:, None]
+        acc = np.where(live, np.add(acc, xs[..., t, :], dtype=np.float32), acc)
+    return np.divide(acc, cnt.astype(np.float32)[:, None], dtype=np.float32)
 
 
 def cube_scores_fp32(qm, km):
@@ -76,11 +85,13 @@ def topk_blocks(scores, topk):
     return np.sort(order[..., :topk], axis=-1).astype(np.int32)
 
 
-def vsa_select(q, k, block, topk):
-    """Selection for every query cube.  q, k: [B][H][S][D] FP16 cube-major.
+def vsa_select(q, k, block, topk, valid=None, prefix=0):
+    """Selection for every query cube.  q, k: [B][H][S][D] FP16; tokens
+    [prefix, S) are the cube-major video tokens (S - prefix a multiple of
+    block), valid the per-cube valid-token counts (None: full cubes).
 
-    Returns idx int32 [B][H][S/block][topk].
+    Returns idx int32 [B][H][(S - prefix)/block][topk].
     """
-    qm = pool_means_fp32(q, block)
-    km = pool_means_fp32(k, block)
+    qm = pool_means_fp32(np.asarray(q)[..., prefix:, :], block, valid)
+    km = pool_means_fp32(np.asarray(k)[..., prefix:, :], block, valid)
     return topk_blocks(cube_scores_fp32(qm, km), topk)

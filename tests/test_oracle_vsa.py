@@ -140,3 +140,128 @@ def test_fp32_selection_equals_exact_selection_away_from_ties():
                 assert np.array_equal(idx[h, i], want)
                 checked += 1
     assert checked >= 24
+
+
+# ------------------------------------------------------------------ boundary cubes and prefix
+import math  # noqa: E402
+
+import pytest  # noqa: E402
+
+from oracle import attention as A  # noqa: E402
+
+
+def _valid_counts(nc, seed):
+    rng = np.random.default_rng(seed)
+    v = rng.integers(1, 65, nc)
+    v[0] = 64
+    return v
+
+
+def test_partial_pool_equals_sequential_mean_of_real_tokens():
+    rng = np.random.default_rng(20)
+    nc, D = 5, 8
+    x = rng.standard_normal((2, nc * 64, D)).astype(np.float16)
+    val = _valid_counts(nc, 21)
+    m = pool_means_fp32(x, 64, val)
+    for b in range(2):
+        for c in range(nc):
+            for d in range(D):
+                acc = np.float32(0.0)
+                for t in range(val[c]):
+                    acc = np.float32(acc + np.float32(x[b, c * 64 + t, d]))
+                assert m[b, c, d] == np.float32(acc / np.float32(val[c]))
+
+
+def _layout(prefix, nc, D, seed):
+    rng = np.random.default_rng(seed)
+    S = prefix + nc * 64
+    q, k, v = (rng.standard_normal((1, 2, S, D)).astype(np.float16) for _ in range(3))
+    return q, k, v, _valid_counts(nc, seed + 1)
+
+
+def test_padding_contents_are_ignored():
+    q, k, v, val = _layout(64, 6, 8, 22)
+    idx = vsa_select(q, k, 64, 3, val, prefix=64)
+    o, lse = A.vsa_sparse_attention(q, k, v, idx, 64, 0.4, valid=val, prefix=64)
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    for c in range(6):
+        pad = slice(64 + c * 64 + val[c], 64 + (c + 1) * 64)
+        q2[..., pad, :] = 7.0
+        k2[..., pad, :] = -5.0
+        v2[..., pad, :] = 100.0
+    assert np.array_equal(vsa_select(q2, k2, 64, 3, val, prefix=64), idx)
+    o2, lse2 = A.vsa_sparse_attention(q2, k2, v2, idx, 64, 0.4, valid=val, prefix=64)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+def _brute_rows(q, k, v, scale, keys):
+    out = []
+    sc = float(np.float32(scale))
+    for i, ks in keys:
+        ws = [(j, math.exp(sc * sum(float(q[i, d]) * float(k[j, d]) for d in range(q.shape[1]))))
+              for j in ks]
+        tot = sum(w for _, w in ws)
+        out.append([sum(w * float(v[j, d]) for j, w in ws) / tot for d in range(q.shape[1])])
+    return np.array(out)
+
+
+def _pin_prefix_and_partial(fn):
+    q, k, v, val = _layout(64, 4, 4, 23)
+    idx = np.array([[[0, 2], [1, 3], [0, 3], [2, 3]]] * 2)[None].astype(np.int32)
+    o, lse = fn(q, k, v, idx, 64, 0.5, valid=val, prefix=64)
+    real = [64 + c * 64 + t for c in range(4) for t in range(val[c])]
+    ok = True
+    for h in range(2):
+        rows = [(i, list(range(64)) + real) for i in (0, 17, 63)]
+        for c in range(4):
+            sel = [64 + kc * 64 + t for kc in idx[0, h, c] for t in range(val[kc])]
+            rows.append((64 + c * 64, sel))
+            rows.append((64 + c * 64 + val[c] - 1, sel))
+        want = _brute_rows(q[0, h], k[0, h], v[0, h], 0.5, rows)
+        got = np.array([o[0, h, i] for i, _ in rows])
+        ok &= np.allclose(got, want, rtol=1e-12, atol=1e-13)
+        for c in range(4):                       # padding query slots
+            pads = np.arange(64 + c * 64 + val[c], 64 + (c + 1) * 64)
+            ok &= bool(np.all(o[0, h, pads] == 0)) and bool(np.all(np.isneginf(lse[0, h, pads])))
+    return ok
+
+
+def test_prefix_and_partial_cubes_brute_force():
+    assert _pin_prefix_and_partial(A.vsa_sparse_attention)
+
+
+def test_full_cubes_without_prefix_unchanged():
+    q, k, v, _ = _layout(0, 4, 8, 24)
+    idx = vsa_select(q, k, 64, 2)
+    o1, l1 = A.vsa_sparse_attention(q, k, v, idx, 64, 0.3)
+    o2, l2 = A.vsa_sparse_attention(q, k, v, idx, 64, 0.3, valid=np.full(4, 64), prefix=0)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert np.array_equal(idx, vsa_select(q, k, 64, 2, np.full(4, 64)))
+
+
+def _mutant_sparse(prefix_sees_video=True, mask_padding=True):
+    def fn(q, k, v, idx, block, scale, valid=None, prefix=0):
+        val = np.asarray(valid) if (valid is not None and mask_padding) else None
+        o, lse = A.vsa_sparse_attention(q, k, v, idx, block, scale, valid=val, prefix=prefix)
+        if not prefix_sees_video:
+            for h in range(q.shape[1]):
+                o[0, h, :prefix], lse[0, h, :prefix] = A.attention_rows(
+                    q[0, h, :prefix], k[0, h, :prefix], v[0, h, :prefix], scale)
+        return o, lse
+    return fn
+
+
+@pytest.mark.parametrize("name,fn", [
+    ("padding keys not hidden", _mutant_sparse(mask_padding=False)),
+    ("prefix queries see only the prefix", _mutant_sparse(prefix_sees_video=False)),
+])
+def test_planted_vsa_mistakes_are_caught(name, fn):
+    assert not _pin_prefix_and_partial(fn), name
+
+
+def test_planted_pool_by_block_is_caught():
+    rng = np.random.default_rng(25)
+    x = rng.standard_normal((1, 3 * 64, 4)).astype(np.float16)
+    val = np.array([64, 40, 9])
+    wrong = pool_means_fp32(x, 64, val) * val[None, :, None].astype(np.float32) / np.float32(64)
+    assert not np.allclose(wrong, pool_means_fp32(x, 64, val))
