@@ -41,8 +41,9 @@ _SIGNATURES = {
     "attn_paged_decode_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                    _i, _i, _f, _f, _f, _vp, _sz, _vp]),
     "vsa_select_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
-    "vsa_select_blocks": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
-    "vsa_sparse_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
+    "vsa_select_blocks": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "vsa_sparse_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
+                            _vp]),
 }
 
 DEV_WAIT_TIMEOUT = 1
@@ -279,41 +280,51 @@ def vsa_select_workspace_size(B, H, S, D, block):
     return int(load().vsa_select_workspace_size(B, H, S, D, block))
 
 
-def vsa_select_blocks(q, k, topk, block=64, idx=None, workspace=None, stream=None):
-    """Top-k key cubes per query cube. q, k [B,H,S,D] FP16 -> idx int32 [B,H,S/block,topk]."""
+def vsa_select_blocks(q, k, topk, block=64, prefix=0, cube_valid=None, idx=None, workspace=None,
+                      stream=None):
+    """Top-k key cubes per query cube.  q, k [B,H,S,D] FP16: `prefix` prefix tokens, then
+    cube-major video tokens; cube_valid int32 [cubes] real tokens per cube (None: full).
+    Returns idx int32 [B,H,(S-prefix)/block,topk]."""
     import torch
     _need(q, "q", torch.float16, 4)
     _need(k, "k", torch.float16, 4)
     B, H, S, D = q.shape
     if tuple(k.shape) != tuple(q.shape):
         raise ValueError("q and k must have the same shape")
-    nc = S // block
+    nc = (S - int(prefix)) // block
+    if cube_valid is not None:
+        _need(cube_valid, "cube_valid", torch.int32, 1)
     if idx is None:
         idx = torch.empty((B, H, nc, topk), dtype=torch.int32, device=q.device)
     _need(idx, "idx", torch.int32)
     if workspace is None:
         workspace = torch.empty(max(vsa_select_workspace_size(B, H, S, D, block), 16),
                                 dtype=torch.uint8, device=q.device)
-    rc = load().vsa_select_blocks(_ptr(q), _ptr(k), B, H, S, D, block, int(topk), _ptr(idx),
-                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                  _stream(stream))
+    rc = load().vsa_select_blocks(_ptr(q), _ptr(k), B, H, S, D, block, int(topk), int(prefix),
+                                  _ptr(cube_valid), _ptr(idx), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
     _check("vsa_select_blocks", rc)
     return idx
 
 
-def vsa_sparse_fwd(q, k, v, idx, block=64, o=None, lse=None, scale=None, stream=None):
-    """Block-sparse attention over the cubes in idx. q/k/v [B,H,S,D] FP16 cube-major."""
+def vsa_sparse_fwd(q, k, v, idx, block=64, prefix=0, cube_valid=None, o=None, lse=None,
+                   scale=None, stream=None):
+    """Block-sparse attention over the cubes in idx.  q/k/v [B,H,S,D] FP16: `prefix` dense
+    prefix tokens, then cube-major video tokens; cube_valid int32 [cubes] or None."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.float16, 4)
     _need(idx, "idx", torch.int32, 4)
+    if cube_valid is not None:
+        _need(cube_valid, "cube_valid", torch.int32, 1)
     B, H, S, D = q.shape
     topk = idx.shape[3]
     o = torch.empty_like(q) if o is None else o
     _need(o, "o", torch.float16, 4)
     if lse is not None:
         _need(lse, "lse", torch.float32)
-    rc = load().vsa_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse), B, H, S,
-                               D, block, topk, _scale(scale, D), _stream(stream))
+    rc = load().vsa_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), int(prefix), _ptr(cube_valid),
+                               _ptr(o), _ptr(lse), B, H, S, D, block, topk, _scale(scale, D),
+                               _stream(stream))
     _check("vsa_sparse_fwd", rc)
     return o

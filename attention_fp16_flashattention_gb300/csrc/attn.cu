@@ -49,7 +49,9 @@ constexpr int kMaxTopk = 512;
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s for draining after an abort
 
 // kMasked: dense with an additive FP16 mask [Sq][Skv] per (batch, head) slice.
-enum Mode { kDense = 0, kCausal = 1, kSparse = 2, kMasked = 3 };
+// kSparseFull: kSparse with the full VSA layout (prefix queries, boundary cubes).
+enum Mode { kDense = 0, kCausal = 1, kSparse = 2, kMasked = 3, kSparseFull = 4 };
+__host__ __device__ constexpr bool is_sparse(int mode) { return mode == kSparse || mode == kSparseFull; }
 
 struct AttnArgs {
     int seq_q;          // query rows per head
@@ -70,6 +72,8 @@ struct AttnArgs {
     float* part_o;      // causal, n_chunks > 1: [C][heads_q][seq_q][D] FP32, normalised
     float* part_lse;    // causal, n_chunks > 1: [C][heads_q][seq_q] log2-sum-exp2
     const int32_t* idx; // sparse: [heads][n_cubes][topk]
+    int prefix;         // sparse: prefix tokens before the video cubes (multiple of BM)
+    const int32_t* cube_valid;   // sparse: real tokens per cube, or null (all full)
     const __half* mask; // masked: additive mask, row stride seq_k
     long long mask_sb;  // masked: elements between batch slices (0 = shared)
     long long mask_sh;  // masked: elements between head slices (0 = shared)
@@ -127,6 +131,8 @@ struct SparseTiles {
     int key0[kMaxSparseTiles];
     int key1[kMaxSparseTiles];
     uint8_t mask[kMaxSparseTiles];
+    uint8_t kv0[kMaxSparseTiles];   // real keys in each 64-key half (boundary cubes)
+    uint8_t kv1[kMaxSparseTiles];
 };
 
 // Masked mode: every softmax warp stages the mask of its 32 rows x 64 keys of a
@@ -139,7 +145,7 @@ template <int D, int MODE>
 constexpr int smem_bytes() {
     using C = Cfg<D, MODE>;
     return 1024 + C::Q_BYTES + C::NS * C::SLOT_BYTES + kCtrlBytes +
-           (MODE == kSparse ? static_cast<int>(sizeof(SparseTiles)) : 0) +
+           (is_sparse(MODE) ? static_cast<int>(sizeof(SparseTiles)) : 0) +
            (MODE == kMasked ? kMaskStageBytes : 0);
 }
 
@@ -168,11 +174,56 @@ __device__ __forceinline__ void ring_item(int it, int n, int L, int& tile, bool&
     is_v = true;
 }
 
-// Merge two strictly ascending cube lists into the tile list of a query-cube
-// pair.  Entries that are out of range or not ascending are skipped and flagged.
+// Real tokens of video cube c (boundary cubes are padded); out-of-range counts
+// are flagged and clamped.
+__device__ __forceinline__ int cube_count(const AttnArgs& a, int c) {
+    if (!a.cube_valid) return 64;
+    const int n = a.cube_valid[c];
+    if (n < 1 || n > 64) {
+        atomicOr(a.status, kDevBadIndex);
+        return n < 1 ? 1 : 64;
+    }
+    return n;
+}
+
+// Tile list of a CTA.  Prefix query tiles (qtile < prefix / BM) attend densely:
+// every 128-key prefix tile, then the video cubes two by two.  Video query-cube
+// pairs merge their two strictly ascending cube lists into tiles of two cubes;
+// entries that are out of range or not ascending are skipped and flagged.
+// Video keys sit at prefix + 64 * cube.
+template <bool kFull>
 __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& a, int bh,
-                                   int pair) {
+                                   int qtile) {
     const int lane = threadIdx.x & 31;
+    const int n_pre = kFull ? a.prefix / BM : 0;
+    const int kbase = kFull ? a.prefix : 0;
+    if (kFull && qtile < n_pre) {
+        const int nt = n_pre + (a.n_cubes + 1) / 2;
+        for (int t = lane; t < nt; t += 32) {
+            if (t < n_pre) {
+                st->key0[t] = t * BN;
+                st->key1[t] = t * BN + 64;
+                st->kv0[t] = st->kv1[t] = 64;
+                st->mask[t] = 0xF;
+            } else {
+                const int c0 = 2 * (t - n_pre), c1 = c0 + 1;
+                st->key0[t] = a.prefix + 64 * c0;
+                st->kv0[t] = static_cast<uint8_t>(cube_count(a, c0));
+                if (c1 < a.n_cubes) {
+                    st->key1[t] = a.prefix + 64 * c1;
+                    st->kv1[t] = static_cast<uint8_t>(cube_count(a, c1));
+                    st->mask[t] = 0xF;
+                } else {   // odd cube count: the second half repeats the cube, masked
+                    st->key1[t] = st->key0[t];
+                    st->kv1[t] = st->kv0[t];
+                    st->mask[t] = 0x5;
+                }
+            }
+        }
+        if (lane == 0) ctrl->n_tiles = nt;
+        return;
+    }
+    const int pair = qtile - n_pre;
     const int ca = 2 * pair, cb = 2 * pair + 1;
     const int na = a.topk;
     const int nb = cb < a.n_cubes ? a.topk : 0;
@@ -208,8 +259,8 @@ __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& 
             pend = c;
             pend_f = f;
         } else {
-            st->key0[nt] = pend * 64;
-            st->key1[nt] = c * 64;
+            st->key0[nt] = kbase + pend * 64;
+            st->key1[nt] = kbase + c * 64;
             st->mask[nt] = static_cast<uint8_t>((pend_f & 1) | ((f & 1) << 1) |
                                                 ((pend_f >> 1) << 2) | ((f >> 1) << 3));
             ++nt;
@@ -218,13 +269,23 @@ __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& 
         ++nu;
     }
     if (pend >= 0) {   // odd union: the second half repeats the cube, fully masked
-        st->key0[nt] = pend * 64;
-        st->key1[nt] = pend * 64;
+        st->key0[nt] = kbase + pend * 64;
+        st->key1[nt] = kbase + pend * 64;
         st->mask[nt] = static_cast<uint8_t>((pend_f & 1) | ((pend_f >> 1) << 2));
         ++nt;
     }
     if (bad) atomicOr(a.status, kDevBadIndex);
     ctrl->n_tiles = nt;
+}
+
+// Real keys of every tile half of a video query-cube pair (boundary cubes),
+// filled by the whole warp once the list is built; only with cube counts.
+__device__ void fill_tile_counts(SparseTiles* st, const Ctrl* ctrl, const AttnArgs& a) {
+    const int nt = ctrl->n_tiles;
+    for (int t = threadIdx.x & 31; t < nt; t += 32) {
+        st->kv0[t] = static_cast<uint8_t>(cube_count(a, (st->key0[t] - a.prefix) >> 6));
+        st->kv1[t] = static_cast<uint8_t>(cube_count(a, (st->key1[t] - a.prefix) >> 6));
+    }
 }
 
 template <int D, int MODE>
@@ -267,6 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_tiles = static_cast<int>(static_cast<long long>(chunk + 1) * T / a.n_chunks) - tile0;
     } else {
         q_row0 = qtile * BM;
+        if (MODE == kSparseFull && qtile >= a.prefix / BM)   // video query-cube pair
+            q_row0 = a.prefix + (qtile - a.prefix / BM) * BM;
         kv_bh = bh;
         if (MODE == kDense || MODE == kMasked) n_tiles = (a.seq_k + BN - 1) / BN;
     }
@@ -297,7 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmV);
             if (MODE == kMasked) tma_prefetch_desc(&tmM);
         }
-        if (MODE == kSparse) build_sparse_tiles(st, ctrl, a, bh, qtile);
+        if (is_sparse(MODE)) {
+            build_sparse_tiles<MODE == kSparseFull>(st, ctrl, a, bh, qtile);
+            __syncwarp();
+            if (MODE == kSparseFull && a.cube_valid && qtile >= a.prefix / BM)
+                fill_tile_counts(st, ctrl, a);
+        }
         __syncwarp();
     }
     if (warp == 1) {
@@ -308,11 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
-    if (MODE == kSparse) n_tiles = ctrl->n_tiles;
+    if (is_sparse(MODE)) n_tiles = ctrl->n_tiles;
     const WaitCtl w{a.wait_limit, a.status, &ctrl->abort};
 
     auto tile_keys = [&](int t, int& k0, int& k1) {
-        if (MODE == kSparse) {
+        if (is_sparse(MODE)) {
             k0 = st->key0[t];
             k1 = st->key1[t];
         } else {
@@ -527,11 +595,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 64; ++c)
                         if (kh + c >= a.seq_k || row_g >= a.seq_q) s[c] = __float_as_uint(-INFINITY);
                 }
-            } else if (MODE == kSparse) {
+            } else if (is_sparse(MODE)) {
                 const uint32_t mk = st->mask[j];
                 if (!((mk >> (row_half * 2 + half)) & 1u)) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = __float_as_uint(-INFINITY);
+                } else if (MODE == kSparseFull && a.cube_valid) {   // padding keys of a boundary cube
+                    const int kvl = half ? st->kv1[j] : st->kv0[j];
+                    if (kvl < 64) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (c >= kvl) s[c] = __float_as_uint(-INFINITY);
+                    }
                 }
             } else {
                 const int kh = half ? k1 : k0;
@@ -635,7 +710,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             const bool row_ok = row_g < a.seq_q;
-            const bool zero_row = MODE == kCausal && row_g >= a.q_real;
+            bool zero_row = MODE == kCausal && row_g >= a.q_real;
+            if (MODE == kSparseFull && row_g >= a.prefix && row_g < a.seq_q) {   // padding query slot
+                const int vr = static_cast<int>(row_g - a.prefix);
+                zero_row = (vr & 63) >= cube_count(a, vr >> 6);
+            }
             const float inv_l = (l > 0.0f && !zero_row) ? 1.0f / l : 0.0f;
             const float lse2 = (l > 0.0f && !zero_row) ? m_run + __log2f(l) : -INFINITY;
             const bool partial = MODE == kCausal && a.n_chunks > 1;
@@ -989,14 +1068,17 @@ extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void*
 }
 
 extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
-                              void* o, float* lse, int B, int H, int S, int D, int block, int topk,
-                              float scale, void* stream) {
+                              int prefix, const int32_t* cube_valid, void* o, float* lse, int B,
+                              int H, int S, int D, int block, int topk, float scale, void* stream) {
     if (!q || !k || !v || !idx || !o) return GBATTN_ERR_NULL;
-    if (B <= 0 || H <= 0 || S <= 0 || topk <= 0) return GBATTN_ERR_SHAPE;
+    if (B <= 0 || H <= 0 || S <= 0 || topk <= 0 || prefix < 0 || prefix >= S)
+        return GBATTN_ERR_SHAPE;
     if (D != 128 || block != 64) return GBATTN_ERR_UNSUPPORTED;
-    if (S % block != 0) return GBATTN_ERR_SHAPE;
-    const int nc = S / block;
+    if ((S - prefix) % block != 0 || prefix % BM != 0) return GBATTN_ERR_SHAPE;
+    const int nc = (S - prefix) / block;
     if (topk > nc || topk > kMaxTopk) return GBATTN_ERR_SHAPE;
+    if (prefix / BM + (nc + 1) / 2 > kMaxSparseTiles) return GBATTN_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(cube_valid) & 3u) return GBATTN_ERR_ALIGN;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
     if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
@@ -1022,9 +1104,14 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
     a.n_cubes = nc;
     a.topk = topk;
     a.idx = idx;
+    a.prefix = prefix;
+    a.cube_valid = cube_valid;
     a.o = static_cast<__half*>(o);
     a.lse = lse;
-    dim3 grid((nc + 1) / 2, B * H);
+    dim3 grid(prefix / BM + (nc + 1) / 2, B * H);
+    if (prefix > 0 || cube_valid)
+        return launch_attn<128, kSparseFull>(q, k, v, S, S, B * H, B * H, grid, a,
+                                             static_cast<cudaStream_t>(stream));
     return launch_attn<128, kSparse>(q, k, v, S, S, B * H, B * H, grid, a,
                                      static_cast<cudaStream_t>(stream));
 }

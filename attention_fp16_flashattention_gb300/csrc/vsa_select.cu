@@ -5,9 +5,11 @@
 //
 // Two kernels:
 //  1. vsa_pool_kernel: FP32 cube means of Q and K.  Each thread owns 8
-//     consecutive channels of one cube and adds the cube's 64 tokens in token
-//     order with FP32 rounding after every addition, then divides by the count
-//     (correctly rounded).  HBM-bound: Q and K are read once with 16-byte loads.
+//     consecutive channels of one cube and adds the cube's real tokens (all 64,
+//     or the first valid-count slots of a boundary cube) in token order with
+//     FP32 rounding after every addition, then divides by the count (correctly
+//     rounded).  Video tokens start after `prefix` prefix tokens, which take no
+//     part.  HBM-bound: Q and K are read once with 16-byte loads.
 //  2. vsa_score_topk_kernel: 32 query cubes per CTA against all key cubes,
 //     register-tiled (2 queries x 4 keys per thread) with operands staged
 //     d-major in shared memory.  Every score is an FP32 sum over d = 0..D-1, in
@@ -30,21 +32,33 @@ constexpr int kPoolThreads = 256;
 constexpr int kMaxChunks = 32;      // 32-key chunks per row: supports up to 1024 cubes per head
 
 __global__ void __launch_bounds__(kPoolThreads) vsa_pool_kernel(
-    const __half* __restrict__ q, const __half* __restrict__ k, long long n_cubes, int D,
-    int block, float* __restrict__ qm, float* __restrict__ km) {
+    const __half* __restrict__ q, const __half* __restrict__ k, long long n_bh, int n_cubes,
+    long long seq, int prefix, int D, int block, const int32_t* __restrict__ cube_valid,
+    uint32_t* status, float* __restrict__ qm, float* __restrict__ km) {
     const __half* x = blockIdx.y == 0 ? q : k;
     float* out = blockIdx.y == 0 ? qm : km;
     const int groups = D >> 3;   // 8 channels per thread
     const long long gid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-    if (gid >= n_cubes * groups) return;
-    const long long cube = gid / groups;
+    if (gid >= n_bh * n_cubes * groups) return;
+    const long long cube = gid / groups;            // bh * n_cubes + c
     const int g = static_cast<int>(gid - cube * groups);
-    const __half* base = x + cube * block * D + g * 8;
+    const long long bh = cube / n_cubes;
+    const int c = static_cast<int>(cube - bh * n_cubes);
+    // Real tokens of the cube: its first `count` slots (boundary cubes are padded).
+    int count = block;
+    if (cube_valid) {
+        count = cube_valid[c];
+        if (count < 1 || count > block) {
+            if (g == 0 && bh == 0 && blockIdx.y == 0) atomicOr(status, kDevBadIndex);
+            count = count < 1 ? 1 : block;
+        }
+    }
+    const __half* base = x + (bh * seq + prefix + static_cast<long long>(c) * block) * D + g * 8;
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll 8
-    for (int t = 0; t < block; ++t) {
+    for (int t = 0; t < count; ++t) {
         const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(base + static_cast<long long>(t) * D));
         const __half2* h = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
@@ -54,7 +68,7 @@ __global__ void __launch_bounds__(kPoolThreads) vsa_pool_kernel(
             acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], f.y);
         }
     }
-    const float cnt = static_cast<float>(block);
+    const float cnt = static_cast<float>(count);
     float4 lo, hi;
     lo.x = __fdiv_rn(acc[0], cnt); lo.y = __fdiv_rn(acc[1], cnt);
     lo.z = __fdiv_rn(acc[2], cnt); lo.w = __fdiv_rn(acc[3], cnt);
@@ -214,19 +228,21 @@ extern "C" size_t vsa_select_workspace_size(int B, int H, int S, int D, int bloc
 }
 
 extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D,
-                                 int block, int topk, int32_t* idx, void* workspace,
-                                 size_t workspace_bytes, void* stream) {
+                                 int block, int topk, int prefix, const int32_t* cube_valid,
+                                 int32_t* idx, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
     if (!q || !k || !idx) return GBATTN_ERR_NULL;
-    if (B <= 0 || H <= 0 || S <= 0 || topk <= 0) return GBATTN_ERR_SHAPE;
+    if (B <= 0 || H <= 0 || S <= 0 || topk <= 0 || prefix < 0 || prefix >= S)
+        return GBATTN_ERR_SHAPE;
     if (D != 128 || block != 64) return GBATTN_ERR_UNSUPPORTED;
-    if (S % block != 0) return GBATTN_ERR_SHAPE;
-    const int NC = S / block;
+    if ((S - prefix) % block != 0) return GBATTN_ERR_SHAPE;
+    const int NC = (S - prefix) / block;
     if (NC > kMaxChunks * 32 || topk > NC) return GBATTN_ERR_SHAPE;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
     const size_t need = vsa_select_workspace_size(B, H, S, D, block);
     if (!workspace || workspace_bytes < need) return GBATTN_ERR_WORKSPACE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(workspace) ||
-        (reinterpret_cast<uintptr_t>(idx) & 3u))
+        (reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(cube_valid) & 3u))
         return GBATTN_ERR_ALIGN;
     const size_t in_bytes = static_cast<size_t>(B) * H * S * D * 2;
     const size_t idx_bytes = static_cast<size_t>(B) * H * NC * topk * 4;
@@ -240,12 +256,13 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* qm = static_cast<float*>(workspace);
     float* km = qm + static_cast<size_t>(B) * H * NC * D;
-    const long long n_cubes = static_cast<long long>(B) * H * NC;
-    const long long pool_threads = n_cubes * (D / 8);
+    const long long n_bh = static_cast<long long>(B) * H;
+    const long long pool_threads = n_bh * NC * (D / 8);
     dim3 pgrid(static_cast<unsigned>((pool_threads + kPoolThreads - 1) / kPoolThreads), 2);
     vsa_pool_kernel<<<pgrid, kPoolThreads, 0, s>>>(static_cast<const __half*>(q),
-                                                   static_cast<const __half*>(k), n_cubes, D,
-                                                   block, qm, km);
+                                                   static_cast<const __half*>(k), n_bh, NC, S,
+                                                   prefix, D, block, cube_valid, dev.status, qm,
+                                                   km);
     static std::once_flag attr_once[64];
     if (dev.device >= 0 && dev.device < 64)
         std::call_once(attr_once[dev.device], [] {
@@ -308,7 +325,8 @@ int scratch_address(void** out) {
 }  // namespace
 
 extern "C" int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S, int D,
-                                         int block, int topk, int32_t* idx, void* stream) {
+                                         int block, int topk, int prefix,
+                                         const int32_t* cube_valid, int32_t* idx, void* stream) {
     if (!q || !k || !idx) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return GBATTN_ERR_SHAPE;
     const size_t need = vsa_select_workspace_size(B, H, S, D, block);
@@ -318,6 +336,6 @@ extern "C" int vsa_select_blocks_noalloc(const void* q, const void* k, int B, in
     if (rc != GBATTN_OK) return rc;
     // The pool kernel overwrites every scratch byte it later reads, so the
     // previous call's contents need no clearing.
-    return vsa_select_blocks(q, k, B, H, S, D, block, topk, idx, scratch, kNoAllocScratchBytes,
-                             stream);
+    return vsa_select_blocks(q, k, B, H, S, D, block, topk, prefix, cube_valid, idx, scratch,
+                             kNoAllocScratchBytes, stream);
 }

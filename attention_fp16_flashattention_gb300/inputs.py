@@ -20,6 +20,9 @@ with 64-token cubes and top-k 64):
                 behind a random page-table permutation; scales 1/16 and 1/8
   dense_masked  B1 H24 S8192 D128, Q/K/V ~ N(0,1), one FP16 additive mask
                 [8192][8192] shared by all heads: -2^-9 |i - j| plus 3% hidden keys
+  vsa_full      B1 H24 D128: 1024 prefix tokens (N(0,1)) then an 8x62x62 latent
+                grid in 4x4x4 cubes (2x16x16 = 512 cubes, boundary cubes padded:
+                30752 real of 32768 slots), top-k 64; Q/K as vsa_video
   paged_decode  B4 Hq6 Hkv1 D256, one new token per sequence over ragged
                 caches of 131072, 122887, 98313 and 65571 tokens (K/V bytes and
                 pages as paged_e4m3, every sequence's pages scattered over one
@@ -156,6 +159,61 @@ def vsa_inputs(B, H, D, seed, grid=(8, 64, 64), cube=(4, 4, 4)):
 FINITE_E4M3 = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
 
 
+def padded_cube_layout(grid, cube):
+    """Cube-major layout with boundary padding for a grid the cube may not divide.
+
+    Returns (slot, valid): slot[raster token] = its position in the padded
+    cube-major sequence (cube c owns slots c*V .. c*V + V - 1, V = ct*cy*cx;
+    its real tokens fill the first slots in (t, y, x) raster order inside the
+    cube), valid[c] = real tokens of cube c.
+    """
+    T, Y, X = grid
+    ct, cy, cx = cube
+    nt, ny, nx = -(-T // ct), -(-Y // cy), -(-X // cx)
+    t, y, x = (a.reshape(-1) for a in np.meshgrid(np.arange(T), np.arange(Y), np.arange(X),
+                                                   indexing="ij"))
+    c = ((t // ct) * ny + y // cy) * nx + x // cx
+    inner = ((t % ct) * cy + y % cy) * cx + x % cx
+    order = np.lexsort((inner, c))                 # raster tokens sorted by (cube, inner)
+    valid = np.bincount(c, minlength=nt * ny * nx).astype(np.int32)
+    first = np.concatenate([[0], np.cumsum(valid)[:-1]])
+    rank = np.empty(order.size, dtype=np.int64)
+    rank[order] = np.arange(order.size)
+    slot = c * (ct * cy * cx) + (rank - first[c])
+    return slot, valid
+
+
+def vsa_full_inputs(B, H, D, seed, grid, cube=(4, 4, 4), prefix=0):
+    """The full VSA layout: `prefix` prefix tokens (text/audio, N(0,1)), then the
+    video tokens of `grid` in padded cube-major order (smooth low-frequency signal
+    + N(0,1) for Q and K, N(0,1) for V; padding slots zero).
+
+    Returns q, k, v [B][H][prefix + cubes*64][D] FP16 and valid int32 [cubes].
+    """
+    slot, valid = padded_cube_layout(grid, cube)
+    nc = valid.size
+    V = cube[0] * cube[1] * cube[2]
+    S = prefix + nc * V
+    n = grid[0] * grid[1] * grid[2]
+    out = []
+    for name, sig_tag in (("q", "qsig"), ("k", "ksig")):
+        sig_rng = _rng(seed, sig_tag)
+        rng = _rng(seed, name)
+        x = np.zeros((B, H, S, D), dtype=np.float16)
+        for b in range(B):
+            sig = _smooth_signal(sig_rng, H, D, grid)
+            for h in range(H):
+                x[b, h, :prefix] = rng.standard_normal((prefix, D), dtype=np.float32)
+                z = rng.standard_normal((n, D), dtype=np.float32)
+                x[b, h, prefix + slot] = (sig[h] + z).astype(np.float16)
+        out.append(x)
+    v = np.zeros((B, H, S, D), dtype=np.float16)
+    vr = _normal_fp16(_rng(seed, "v"), (B, H, prefix + n, D))
+    v[:, :, :prefix] = vr[:, :, :prefix]
+    v[:, :, prefix + slot] = vr[:, :, prefix:]
+    return out[0], out[1], v, valid
+
+
 def paged_e4m3_inputs(Hkv, KV, D, seed, page_size=32, num_phys_pages=None):
     """K/V E4M3 pages [P][page_size][Hkv][D] uint8 and an int32 page table.
 
@@ -235,7 +293,7 @@ def sample_rows(n_heads, n_rows, count, seed, row_limit=None):
     return np.stack([pick // lim, pick % lim], axis=1).astype(np.int64)
 
 
-# The seven workloads, with their seeds (1000 + workload number).
+# The eight workloads, with their seeds (1000 + workload number).
 WORKLOADS = {
     "dense_small": dict(kind="dense", B=1, H=2, S=256, D=128, seed=1001),
     "causal_small": dict(kind="causal", B=1, Hq=6, Hkv=1, Q=1024, KV=4096, D=256, seed=1002),
@@ -245,6 +303,8 @@ WORKLOADS = {
     "paged_e4m3": dict(kind="paged", B=1, Hq=6, Hkv=1, Q=8192, KV=131072, D=256, page_size=32,
                        k_scale=0.0625, v_scale=0.125, seed=1005),
     "dense_masked": dict(kind="masked", B=1, H=24, S=8192, D=128, seed=1007),
+    "vsa_full": dict(kind="vsa_full", B=1, H=24, D=128, grid=(8, 62, 62), cube=(4, 4, 4),
+                     prefix=1024, topk=64, seed=1008),
     "paged_decode": dict(kind="decode", B=4, Hq=6, Hkv=1, nq=1,
                          kv_lens=(131072, 122887, 98313, 65571), D=256, page_size=32,
                          k_scale=0.0625, v_scale=0.125, seed=1006),

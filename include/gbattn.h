@@ -210,17 +210,24 @@ int attn_paged_decode_fwd(const void* q, const uint8_t* k_pages, const uint8_t* 
  * (top-k = 64); FastVideo compare view, minimax_h3_fusions/query_pool.py and
  * key_quant.py (FP32 tile means: FP32 sum divided by the count, 64-token tiles),
  * block_lists.py (per-query-block key-block lists).
- *   q, k : [B][H][S][D] FP16 in cube-major order (cube c = tokens c*block .. c*block+block-1)
- *   idx  : int32 [B][H][S/block][topk], for every query cube the topk key cubes with the
- *          largest score, ties to the lower cube index, in ascending cube order.
- *   Pooled vector = FP32 sum over the cube's tokens in token order / block (FP32, RN).
+ *   q, k : [B][H][S][D] FP16.  Tokens [0, prefix) are prefix tokens (text or audio) that take
+ *          no part; tokens [prefix, S) are the video tokens in cube-major order (cube c =
+ *          slots prefix + c*block .. + block-1).
+ *   cube_valid : int32 [(S-prefix)/block] real tokens per cube (1..block; a boundary cube of a
+ *          grid the cube size does not divide holds its real tokens in its first slots and
+ *          padding after them), or NULL when every cube is full.  Out-of-range counts set
+ *          GBATTN_DEV_BAD_INDEX and are clamped to [1, block].
+ *   idx  : int32 [B][H][(S-prefix)/block][topk], for every query cube the topk key cubes with
+ *          the largest score, ties to the lower cube index, in ascending cube order.
+ *   Pooled vector = FP32 sum over the cube's real tokens in token order / their count
+ *   (FP32, RN); padding contents are never read.
  *   Score = FP32 sum over d = 0..D-1, in order, of FP32 products (no fused multiply-add).
- *   block == 64, D == 128, S % block == 0, 1 <= topk <= S/block <= 1024.
+ *   block == 64, D == 128, (S - prefix) % block == 0, 1 <= topk <= (S-prefix)/block <= 1024.
  */
 size_t vsa_select_workspace_size(int B, int H, int S, int D, int block);
 int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D, int block,
-                      int topk, int32_t* idx, void* workspace, size_t workspace_bytes,
-                      void* stream);
+                      int topk, int prefix, const int32_t* cube_valid, int32_t* idx,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * vsa_select_blocks for callers that cannot allocate device memory.  The pages
@@ -247,21 +254,29 @@ int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D, 
  */
 #define GBATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S, int D, int block,
-                              int topk, int32_t* idx, void* stream);
+                              int topk, int prefix, const int32_t* cube_valid, int32_t* idx,
+                              void* stream);
 
 /*
- * VSA block-sparse attention over the selected key cubes.
- * Cites: "Integrate H3 SM70 execution, metrics and VSA diagnostics", Purpose;
- * FastVideo compare view, block_lists.py (two 64-token query halves against two
- * 64-token key halves per 128x128 block, with a 4-bit quadrant mask).
- *   q, k, v, o : [B][H][S][D] FP16 cube-major; idx: int32 [B][H][S/block][topk]
- *   strictly ascending per row; lse optional [B][H][S].
- *   Query token i attends exactly the tokens of cubes idx[b][h][i / block][*].
- *   block == 64, D == 128, S % block == 0, 1 <= topk <= min(S/block, 512).
+ * VSA block-sparse attention over the selected key cubes (the full VSA layout).
+ * Cites: "Integrate H3 SM70 execution, metrics and VSA diagnostics", Purpose (top-k = 64,
+ * prefix-dense queries, per-query video blocks, boundary handling); FastVideo compare view,
+ * block_lists.py (two 64-token query halves against two 64-token key halves per 128x128
+ * block, with a 4-bit quadrant mask, and per-tile valid counts).
+ *   q, k, v, o : [B][H][S][D] FP16; tokens [0, prefix) are prefix tokens, tokens
+ *   [prefix, S) the cube-major video tokens; idx: int32 [B][H][(S-prefix)/block][topk]
+ *   strictly ascending per row; cube_valid as for vsa_select_blocks (NULL: full cubes);
+ *   lse optional [B][H][S].
+ *   A prefix query attends densely to every prefix token and every real video token; a real
+ *   video query in cube c attends exactly the real tokens of cubes idx[b][h][c][*]; a padding
+ *   query slot gets O = 0, lse = -inf.  Padding slots of V must hold finite values (their
+ *   weight is exactly zero).
+ *   block == 64, D == 128, prefix % 128 == 0, (S - prefix) % block == 0,
+ *   1 <= topk <= min((S-prefix)/block, 512), prefix/128 + ceil(cubes/2) <= 512.
  */
-int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx, void* o,
-                   float* lse, int B, int H, int S, int D, int block, int topk, float scale,
-                   void* stream);
+int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx, int prefix,
+                   const int32_t* cube_valid, void* o, float* lse, int B, int H, int S, int D,
+                   int block, int topk, float scale, void* stream);
 
 #ifdef __cplusplus
 }

@@ -59,6 +59,7 @@ P2 = ctypes.c_void_p(0x20000000)
 P3 = ctypes.c_void_p(0x40000000)
 P4 = ctypes.c_void_p(0x60000000)
 MIS = ctypes.c_void_p(0x10008)    # 8-byte aligned only
+MIS2 = ctypes.c_void_p(0x10002)   # not 4-byte aligned
 
 
 def test_dense_validation(lib):
@@ -178,17 +179,25 @@ def test_select_and_sparse_validation(lib):
     ws = lib.vsa_select_workspace_size(1, 24, 32768, 128, 64)
     assert ws == 2 * 24 * 512 * 128 * 4
     f = lib.vsa_select_blocks
-    assert f(P, P2, 1, 24, 32768, 128, 64, 64, P3, P4, ws - 1, None) == WORKSPACE
-    assert f(P, P2, 1, 24, 32768, 128, 32, 64, P3, P4, ws, None) == UNSUPPORTED
-    assert f(P, P2, 1, 24, 32768, 128, 64, 513, P3, P4, ws, None) == SHAPE
-    assert f(P, P2, 1, 24, 32768 + 32, 128, 64, 64, P3, P4, ws, None) == SHAPE
-    assert f(P, P2, 1, 24, 32768, 128, 64, 64, P3, P4, ws, None) in (CUDA, OK)
+    assert f(P, P2, 1, 24, 32768, 128, 64, 64, 0, None, P3, P4, ws - 1, None) == WORKSPACE
+    assert f(P, P2, 1, 24, 32768, 128, 32, 64, 0, None, P3, P4, ws, None) == UNSUPPORTED
+    assert f(P, P2, 1, 24, 32768, 128, 64, 513, 0, None, P3, P4, ws, None) == SHAPE
+    assert f(P, P2, 1, 24, 32768 + 32, 128, 64, 64, 0, None, P3, P4, ws, None) == SHAPE
+    assert f(P, P2, 1, 24, 32768 + 32, 128, 64, 64, 32, None, P3, P4, ws, None) in (CUDA, OK)
+    assert f(P, P2, 1, 24, 32768, 128, 64, 64, -1, None, P3, P4, ws, None) == SHAPE
+    assert f(P, P2, 1, 24, 32768, 128, 64, 64, 0, MIS2, P3, P4, ws, None) == ALIGN
+    assert f(P, P2, 1, 24, 32768, 128, 64, 64, 0, None, P3, P4, ws, None) in (CUDA, OK)
     g = lib.vsa_sparse_fwd
-    assert g(P, P2, P3, P4, None, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == NULL
-    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), P, None, 1, 24, 32768, 128, 64, 64, 0.08,
-             None) == ALIAS
-    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), P4, None, 1, 24, 32768, 128, 64, 600, 0.08,
-             None) == SHAPE
+    # q, k, v, idx, prefix, cube_valid, o, lse, B, H, S, D, block, topk, scale, stream
+    assert g(P, P2, P3, P4, 0, None, None, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == NULL
+    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), 0, None, P, None, 1, 24, 32768, 128, 64, 64,
+             0.08, None) == ALIAS
+    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), 0, None, P4, None, 1, 24, 32768, 128, 64, 600,
+             0.08, None) == SHAPE
+    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), 64, None, P4, None, 1, 24, 32768 + 64, 128,
+             64, 64, 0.08, None) == SHAPE          # prefix must be whole 128-row query tiles
+    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), 128, MIS2, P4, None, 1, 24, 32768 + 128, 128,
+             64, 64, 0.08, None) == ALIGN
 
 
 def test_product_package_does_not_import_oracle():

@@ -28,8 +28,8 @@ WORKSPACE_ERR = 6
 def _noalloc(lib):
     fn = lib.vsa_select_blocks_noalloc
     fn.restype = ctypes.c_int
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 6 + \
-        [ctypes.c_void_p, ctypes.c_void_p]
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 7 + \
+        [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     return fn
 
 
@@ -45,7 +45,7 @@ def test_noalloc_select_matches_workspace_entry_point_twice(gb):
         ref = gb.vsa_select_blocks(tq, tk, topk=topk)
         idx = torch.full((B, H, S // 64, topk), -1, dtype=torch.int32, device="cuda")
         rc = fn(ctypes.c_void_p(tq.data_ptr()), ctypes.c_void_p(tk.data_ptr()), B, H, S, D, 64,
-                topk, ctypes.c_void_p(idx.data_ptr()), stream)
+                topk, 0, None, ctypes.c_void_p(idx.data_ptr()), stream)
         assert rc == 0, gb.status_string(rc)
         torch.cuda.synchronize()
         assert torch.equal(idx, ref)
@@ -60,6 +60,6 @@ def test_noalloc_rejects_sizes_beyond_fixed_scratch(gb):
     before = gb.launch_count()
     # 1 x 24 heads x 32768 tokens needs 12.6 MB of scratch (fits); 48 heads need 25 MB.
     rc = fn(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(q.data_ptr()), 1, 48, 32768, 128, 64,
-            64, ctypes.c_void_p(idx.data_ptr()), stream)
+            64, 0, None, ctypes.c_void_p(idx.data_ptr()), stream)
     assert rc == WORKSPACE_ERR
     assert gb.launch_count() == before
