@@ -15,12 +15,14 @@ done between steps.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
         [--workload all|dense_video|vsa_video|paged_e4m3|dense_small|causal_small]
-        [--decode on|off|only] [--masked on|off|only]
+        [--decode on|off|only] [--masked on|off|only] [--vsa-full on|off|only]
 Beside the step, the paged E4M3 decode (4 ragged sequences of 65571..131072
 cached tokens, Hq6 Hkv1 D256, one new token each; attn_paged_decode_fwd) is
 timed on its own and reported as "decode" with its HBM roofline, and dense attention
 with an additive mask (B1 H24 S8192 D128, one FP16 [8192][8192] mask shared by the
-heads; attn_dense_mask_fwd) as "masked".
+heads; attn_dense_mask_fwd) as "masked", and the full VSA layout (1024 prefix
+tokens + an 8x62x62 grid with padded boundary cubes; vsa_select_blocks +
+vsa_sparse_fwd with prefix and cube counts) as "vsa_full".
 For N > 1 (torchrun, one process per GPU) every rank runs the same step on its
 own GPU (independent replicas, no data-path communication); the time is the
 maximum over ranks and the value counts the work of all ranks.
@@ -502,6 +504,66 @@ def measure_masked(gb, torch, dev, steps, warmup, pk):
             "l2": "256 MB buffer rewritten between launches, outside the timed events"}
 
 
+def measure_vsa_full(gb, torch, dev, steps, warmup, pk):
+    """The full VSA layout (1024 prefix tokens + an 8x62x62 grid in 512 cubes with
+    padded boundary cubes, B1 H24 D128, top-64), selection + sparse attention,
+    timed on its own.  Useful FLOP count the (query, key) pairs the definition
+    visits: prefix rows x every real token, real video rows x the real tokens of
+    their selected cubes.  A 256 MB buffer is rewritten between calls."""
+    w = inputs.WORKLOADS["vsa_full"]
+    q, k, v, valid = inputs.vsa_full_inputs(w["B"], w["H"], w["D"], w["seed"], w["grid"],
+                                            w["cube"], w["prefix"])
+    T = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    dq, dk, dv, dval = T(q), T(k), T(v), T(valid)
+    S = q.shape[2]
+    nc = valid.size
+    idx = torch.empty((w["B"], w["H"], nc, w["topk"]), dtype=torch.int32, device=dev)
+    ws = torch.empty(gb.vsa_select_workspace_size(w["B"], w["H"], S, w["D"], 64), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty_like(dq)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def select():
+        gb.vsa_select_blocks(dq, dk, w["topk"], prefix=w["prefix"], cube_valid=dval, idx=idx,
+                             workspace=ws)
+
+    def sparse():
+        gb.vsa_sparse_fwd(dq, dk, dv, idx, prefix=w["prefix"], cube_valid=dval, o=o)
+
+    for _ in range(warmup):
+        select()
+        sparse()
+    torch.cuda.synchronize()
+    real = int(valid.sum())
+    sel = idx.cpu().numpy()                                 # work count only
+    pairs = w["prefix"] * (w["prefix"] + real) * w["B"] * w["H"]
+    pairs += int((valid[sel].sum(axis=-1) * valid[None, None, :]).sum())
+    flops = 4.0 * w["D"] * pairs
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in ev:
+        flush.fill_(1)
+        e[0].record(stream)
+        select()
+        e[1].record(stream)
+        sparse()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    if gb.device_status() != 0:
+        raise RuntimeError("device status flags set during the full-VSA measurement")
+    t_sel = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    t_sp = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    tf = flops / ((t_sel + t_sp) * 1e-3) / 1e12
+    peak = pk["tc"] or pk["tc_sust"]
+    return {"kernel": "vsa_pool+vsa_score_topk+attn_fwd_kernel<128,sparse_full>", "bound": "tensor",
+            "achieved": tf, "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
+            "peak_source": f"{pk['src']} bf16 burst (timed alone; fp16 dense rate = bf16 rate)",
+            "ms_select": t_sel, "ms_sparse": t_sp, "sparse_tflops": flops / (t_sp * 1e-3) / 1e12,
+            "useful_flop": flops, "real_tokens": real, "slots": S,
+            "config": {k2: v2 for k2, v2 in w.items() if k2 != "seed"},
+            "l2": "256 MB buffer rewritten between calls, outside the timed events"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,6 +578,8 @@ def main():
                     help="paged E4M3 decode measured beside the step (only: print just that)")
     ap.add_argument("--masked", default="on", choices=["on", "off", "only"],
                     help="dense attention with an additive mask measured beside the step")
+    ap.add_argument("--vsa-full", default="on", choices=["on", "off", "only"],
+                    help="the full VSA layout (prefix + boundary cubes) measured beside the step")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count of the dense/VSA workloads (profiling runs)")
     args = ap.parse_args()
@@ -546,6 +610,13 @@ def main():
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
 
+    if args.vsa_full == "only":
+        if rank == 0:
+            print(json.dumps(dict(metric="full VSA useful TFLOP/s", impl="ours", n_gpus=world,
+                                  steps=args.steps, warmup=args.warmup,
+                                  **measure_vsa_full(gb, torch, dev, args.steps, args.warmup,
+                                                     peaks()))))
+        return 0
     if args.masked == "only":
         if rank == 0:
             print(json.dumps(dict(metric="masked dense attention useful TFLOP/s", impl="ours",
@@ -714,6 +785,8 @@ def main():
         extra["decode"] = measure_decode(gb, torch, dev, args.steps, args.warmup, pk)
     if args.masked == "on" and args.workload == "all":
         extra["masked"] = measure_masked(gb, torch, dev, args.steps, args.warmup, pk)
+    if args.vsa_full == "on" and args.workload == "all":
+        extra["vsa_full"] = measure_vsa_full(gb, torch, dev, args.steps, args.warmup, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
