@@ -310,8 +310,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Masked mode runs heads fastest (grid (B*H, tiles)) so that the CTAs of all
     // heads of a query tile run together and share that tile's mask rows in L2.
-    const int bh = MODE == kMasked ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
-    const int qtile = MODE == kMasked ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
+    int bh = MODE == kMasked ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
+    int qtile = MODE == kMasked ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
+    if (MODE == kSparseFull) {
+        // The long prefix tiles of every head launch first, then each head's cube pairs.
+        const int n_pre = a.prefix / BM;
+        const int n_pairs = static_cast<int>(gridDim.x) - n_pre;
+        const long long id = static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x;
+        const long long pre_all = static_cast<long long>(n_pre) * gridDim.y;
+        if (id < pre_all) {
+            bh = static_cast<int>(id / n_pre);
+            qtile = static_cast<int>(id - static_cast<long long>(bh) * n_pre);
+        } else {
+            const long long r = id - pre_all;
+            bh = static_cast<int>(r / n_pairs);
+            qtile = n_pre + static_cast<int>(r - static_cast<long long>(bh) * n_pairs);
+        }
+    }
 
     // ---- work decode
     int q_row0, kv_bh, n_tiles = 0, tile0 = 0, chunk = 0;
