@@ -42,8 +42,9 @@ _SIGNATURES = {
                                    _i, _i, _f, _f, _f, _vp, _sz, _vp]),
     "vsa_select_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "vsa_select_blocks": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
-    "vsa_sparse_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
-                            _vp]),
+    "vsa_sparse_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                            _f, _vp]),
+    "vsa_pair_query_cubes": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
 }
 
 DEV_WAIT_TIMEOUT = 1
@@ -307,23 +308,41 @@ def vsa_select_blocks(q, k, topk, block=64, prefix=0, cube_valid=None, idx=None,
     return idx
 
 
-def vsa_sparse_fwd(q, k, v, idx, block=64, prefix=0, cube_valid=None, o=None, lse=None,
-                   scale=None, stream=None):
+def vsa_pair_query_cubes(idx, pairs=None, stream=None):
+    """Query-cube pairs for vsa_sparse_fwd.  idx int32 [B,H,cubes,topk] ->
+    pairs int32 [B,H,ceil(cubes/2),2] (second entry -1 for a lone cube)."""
+    import torch
+    _need(idx, "idx", torch.int32, 4)
+    B, H, nc, topk = idx.shape
+    if pairs is None:
+        pairs = torch.empty((B, H, (nc + 1) // 2, 2), dtype=torch.int32, device=idx.device)
+    _need(pairs, "pairs", torch.int32)
+    rc = load().vsa_pair_query_cubes(_ptr(idx), B, H, nc, topk, _ptr(pairs), _stream(stream))
+    _check("vsa_pair_query_cubes", rc)
+    return pairs
+
+
+def vsa_sparse_fwd(q, k, v, idx, block=64, prefix=0, cube_valid=None, pairs=None, o=None,
+                   lse=None, scale=None, stream=None):
     """Block-sparse attention over the cubes in idx.  q/k/v [B,H,S,D] FP16: `prefix` dense
-    prefix tokens, then cube-major video tokens; cube_valid int32 [cubes] or None."""
+    prefix tokens, then cube-major video tokens; cube_valid int32 [cubes] or None; pairs from
+    vsa_pair_query_cubes or None (adjacent cubes)."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.float16, 4)
     _need(idx, "idx", torch.int32, 4)
     if cube_valid is not None:
         _need(cube_valid, "cube_valid", torch.int32, 1)
+    if pairs is not None:
+        _need(pairs, "pairs", torch.int32, 4)
     B, H, S, D = q.shape
     topk = idx.shape[3]
     o = torch.empty_like(q) if o is None else o
     _need(o, "o", torch.float16, 4)
     if lse is not None:
         _need(lse, "lse", torch.float32)
-    rc = load().vsa_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), int(prefix), _ptr(cube_valid),
+    rc = load().vsa_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(pairs), int(prefix),
+                               _ptr(cube_valid),
                                _ptr(o), _ptr(lse), B, H, S, D, block, topk, _scale(scale, D),
                                _stream(stream))
     _check("vsa_sparse_fwd", rc)

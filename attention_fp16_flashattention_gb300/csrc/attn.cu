@@ -73,6 +73,8 @@ struct AttnArgs {
     float* part_lse;    // causal, n_chunks > 1: [C][heads_q][seq_q] log2-sum-exp2
     const int32_t* idx; // sparse: [heads][n_cubes][topk]
     int prefix;         // sparse: prefix tokens before the video cubes (multiple of BM)
+    const int32_t* pairs;   // sparse: [heads][ceil(n_cubes/2)][2] query-cube pairs, or null
+                            //         (cubes 2p, 2p+1); a second entry of -1 means none
     const int32_t* cube_valid;   // sparse: real tokens per cube, or null (all full)
     const __half* mask; // masked: additive mask, row stride seq_k
     long long mask_sb;  // masked: elements between batch slices (0 = shared)
@@ -193,7 +195,7 @@ __device__ __forceinline__ int cube_count(const AttnArgs& a, int c) {
 // Video keys sit at prefix + 64 * cube.
 template <bool kFull>
 __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& a, int bh,
-                                   int qtile) {
+                                   int qtile, int ca, int cb) {
     const int lane = threadIdx.x & 31;
     const int n_pre = kFull ? a.prefix / BM : 0;
     const int kbase = kFull ? a.prefix : 0;
@@ -223,12 +225,10 @@ __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& 
         if (lane == 0) ctrl->n_tiles = nt;
         return;
     }
-    const int pair = qtile - n_pre;
-    const int ca = 2 * pair, cb = 2 * pair + 1;
     const int na = a.topk;
-    const int nb = cb < a.n_cubes ? a.topk : 0;
+    const int nb = cb >= 0 ? a.topk : 0;
     const int32_t* la = a.idx + (static_cast<long long>(bh) * a.n_cubes + ca) * a.topk;
-    const int32_t* lb = la + a.topk;
+    const int32_t* lb = a.idx + (static_cast<long long>(bh) * a.n_cubes + (cb >= 0 ? cb : ca)) * a.topk;
     for (int i = lane; i < na; i += 32) st->list_a[i] = la[i];
     for (int i = lane; i < nb; i += 32) st->list_b[i] = lb[i];
     __syncwarp();
@@ -343,10 +343,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_tiles = static_cast<int>(static_cast<long long>(chunk + 1) * T / a.n_chunks) - tile0;
     } else {
         q_row0 = qtile * BM;
-        if (MODE == kSparseFull && qtile >= a.prefix / BM)   // video query-cube pair
-            q_row0 = a.prefix + (qtile - a.prefix / BM) * BM;
         kv_bh = bh;
         if (MODE == kDense || MODE == kMasked) n_tiles = (a.seq_k + BN - 1) / BN;
+    }
+    // First token row of each 64-row half of the query tile.  A VSA video CTA
+    // owns a pair of query cubes (ca, cb), not necessarily adjacent; cb < 0
+    // leaves the second half empty.
+    int ca = -1, cb = -1;
+    int rbase0 = q_row0, rbase1 = q_row0 + 64;
+    if (is_sparse(MODE) && qtile >= (MODE == kSparseFull ? a.prefix / BM : 0)) {
+        const int p = qtile - (MODE == kSparseFull ? a.prefix / BM : 0);
+        ca = 2 * p;
+        cb = 2 * p + 1 < a.n_cubes ? 2 * p + 1 : -1;
+        if (a.pairs) {
+            const int n_pairs = (a.n_cubes + 1) / 2;
+            const int x = a.pairs[(static_cast<long long>(bh) * n_pairs + p) * 2];
+            const int y = a.pairs[(static_cast<long long>(bh) * n_pairs + p) * 2 + 1];
+            if (x >= 0 && x < a.n_cubes && y >= -1 && y < a.n_cubes && x != y) {
+                ca = x;
+                cb = y;
+            } else if (threadIdx.x == 0) {
+                atomicOr(a.status, kDevBadIndex);
+            }
+        }
+        const int kb = MODE == kSparseFull ? a.prefix : 0;
+        rbase0 = kb + 64 * ca;
+        rbase1 = cb >= 0 ? kb + 64 * cb : -1;
+        q_row0 = rbase0;
     }
 
     // ---- prologue
@@ -373,10 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            if (MODE == kMasked) tma_prefetch_desc(&tmM);
+            if (MODE == kMasked || is_sparse(MODE)) tma_prefetch_desc(&tmM);
         }
         if (is_sparse(MODE)) {
-            build_sparse_tiles<MODE == kSparseFull>(st, ctrl, a, bh, qtile);
+            build_sparse_tiles<MODE == kSparseFull>(st, ctrl, a, bh, qtile, ca, cb);
             __syncwarp();
             if (MODE == kSparseFull && a.cube_valid && qtile >= a.prefix / BM)
                 fill_tile_counts(st, ctrl, a);
@@ -411,9 +434,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool load_q = a.fault != 1;
             if (load_q && elect_one()) {
                 mbar_arrive_expect_tx(&ctrl->q_full, C::Q_BYTES);
+                if (is_sparse(MODE)) {   // two 64-row halves (a query-cube pair); tmM has 64-row boxes
+                    const int r1 = rbase1 >= 0 ? rbase1 : rbase0;
 #pragma unroll
-                for (int c = 0; c < C::KCH; ++c)
-                    tma_load_3d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, bh);
+                    for (int c = 0; c < C::KCH; ++c) {
+                        tma_load_3d(sQ + c * C::CHUNK, &tmM, &ctrl->q_full, c * 64, rbase0, bh);
+                        tma_load_3d(sQ + c * C::CHUNK + C::HALF, &tmM, &ctrl->q_full, c * 64, r1, bh);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_3d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, bh);
+                }
             }
             __syncwarp();
             bool ok = true;
@@ -528,7 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const long long row_g = static_cast<long long>(q_row0) + row;
+        // token row of this thread's query row (a missing second cube: past the end)
+        const int rb = row < 64 ? rbase0 : rbase1;
+        const long long row_g = rb < 0 ? static_cast<long long>(a.seq_q) : static_cast<long long>(rb) + (row & 63);
         const int row_half = row >> 6;
         uint64_t* xbar = &ctrl->xchg[quarter];
         int lim = a.seq_k;   // keys >= lim are invisible to this row
@@ -858,10 +892,13 @@ int launch_attn(const void* q, const void* k, const void* v, int seq_q, int seq_
         encode_tmap_f16_3d(&tk, k, D, seq_k, heads_kv, 64, 64) != GBATTN_OK ||
         encode_tmap_f16_3d(&tv, v, D, seq_k, heads_kv, 64, 64) != GBATTN_OK)
         return GBATTN_ERR_CUDA;
+    CUtensorMap tq64;   // sparse modes: query cubes load as two 64-row boxes
+    if (is_sparse(MODE) && encode_tmap_f16_3d(&tq64, q, D, seq_q, heads_q, 64, 64) != GBATTN_OK)
+        return GBATTN_ERR_CUDA;
     int rc = set_smem_attr<D, MODE>();
     if (rc != GBATTN_OK) return rc;
     attn_fwd_kernel<D, MODE><<<grid, kThreads, smem_bytes<D, MODE>(), stream>>>(
-        tq, tk, tv, mask_map ? *mask_map : tq, args);
+        tq, tk, tv, mask_map ? *mask_map : (is_sparse(MODE) ? tq64 : tq), args);
     count_launches(1);
     return launch_status();
 }
@@ -1083,8 +1120,9 @@ extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void*
 }
 
 extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
-                              int prefix, const int32_t* cube_valid, void* o, float* lse, int B,
-                              int H, int S, int D, int block, int topk, float scale, void* stream) {
+                              const int32_t* pairs, int prefix, const int32_t* cube_valid, void* o,
+                              float* lse, int B, int H, int S, int D, int block, int topk,
+                              float scale, void* stream) {
     if (!q || !k || !v || !idx || !o) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || S <= 0 || topk <= 0 || prefix < 0 || prefix >= S)
         return GBATTN_ERR_SHAPE;
@@ -1093,7 +1131,8 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
     const int nc = (S - prefix) / block;
     if (topk > nc || topk > kMaxTopk) return GBATTN_ERR_SHAPE;
     if (prefix / BM + (nc + 1) / 2 > kMaxSparseTiles) return GBATTN_ERR_SHAPE;
-    if (reinterpret_cast<uintptr_t>(cube_valid) & 3u) return GBATTN_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(cube_valid) & 3u) || (reinterpret_cast<uintptr_t>(pairs) & 3u))
+        return GBATTN_ERR_ALIGN;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
     if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
@@ -1121,6 +1160,7 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
     a.idx = idx;
     a.prefix = prefix;
     a.cube_valid = cube_valid;
+    a.pairs = pairs;
     a.o = static_cast<__half*>(o);
     a.lse = lse;
     dim3 grid(prefix / BM + (nc + 1) / 2, B * H);

@@ -282,6 +282,182 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     return launch_status();
 }
 
+// ------------------------------------------------------------------ query-cube pairing
+//
+// The sparse attention kernel processes two query cubes per CTA over the union
+// of their selected key cubes; every key cube only one of the two selected is
+// wasted work for the other.  Pairing cubes whose selections overlap most
+// cuts that waste.  One CTA per head:
+//   1. each cube's selection as a bitset over key cubes;
+//   2. the overlap of every cube with the cubes up to kPairWindow index
+//      positions away (neighbours in the cube grid are close in cube index);
+//   3. kPairRounds rounds of "mutual best": every unpaired cube picks its
+//      unpaired window partner of largest overlap (ties to the lower index);
+//      two cubes that pick each other are paired;
+//   4. the cubes still unpaired are paired in index order.
+// The pairs are written in order of their first cube.  Any pairing gives the
+// same attention result (up to summation order); this one only saves work.
+namespace gbattn {
+namespace {
+constexpr int kPairThreads = 1024;   // one thread per cube
+constexpr int kPairWindow = 32;
+constexpr int kPairRounds = 4;
+constexpr int kPairMaxCubes = 1024;
+constexpr int kPairMaxWords = kPairMaxCubes / 32;
+
+size_t pair_smem_bytes(int nc) {
+    const int words = (nc + 31) / 32;
+    return static_cast<size_t>(nc) * words * 4 + static_cast<size_t>(nc) * kPairWindow +
+           static_cast<size_t>(nc) * 2 * 3 + 64 * 4;
+}
+
+// Exclusive prefix sum of v over the block (one value per thread); returns the
+// total through *total.
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int sh = 1; sh < 32; sh <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, sh);
+        if (lane >= sh) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < kPairThreads / 32 ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, sh);
+            if (lane >= sh) t += y;
+        }
+        warp_tot[lane] = t;   // inclusive over warps
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
+    *total = warp_tot[kPairThreads / 32 - 1];
+    __syncthreads();
+    return before;
+}
+
+__global__ void __launch_bounds__(kPairThreads) vsa_pair_kernel(const int32_t* __restrict__ idx,
+                                                                int nc, int topk,
+                                                                int32_t* __restrict__ pairs) {
+    extern __shared__ uint32_t psm[];
+    __shared__ int warp_tot[32];
+    const int words = (nc + 31) / 32;
+    uint32_t* bits = psm;                                            // [words][nc] (transposed)
+    uint8_t* ov = reinterpret_cast<uint8_t*>(bits + static_cast<size_t>(nc) * words);  // [W][nc]
+    int16_t* partner = reinterpret_cast<int16_t*>(ov + static_cast<size_t>(nc) * kPairWindow);
+    int16_t* best = partner + nc;
+    int16_t* list = best + nc;
+    const long long bh = blockIdx.x;
+    const int32_t* sel = idx + bh * nc * static_cast<long long>(topk);
+    const int a = threadIdx.x;
+    const bool live = a < nc;
+
+    for (int i = a; i < nc * words; i += kPairThreads) bits[i] = 0u;
+    if (live) partner[a] = -1;
+    __syncthreads();
+    for (int e = a; e < nc * topk; e += kPairThreads) {
+        const int c = e / topk;
+        const int kc = sel[e];
+        if (kc >= 0 && kc < nc) atomicOr(&bits[(kc >> 5) * nc + c], 1u << (kc & 31));
+    }
+    __syncthreads();
+    // overlap of a and a + d (d = 1..W) at ov[(d - 1) * nc + a]
+    if (live) {
+        uint32_t mine[kPairMaxWords];
+#pragma unroll
+        for (int w = 0; w < kPairMaxWords; ++w) mine[w] = w < words ? bits[w * nc + a] : 0u;
+        for (int d = 1; d <= kPairWindow; ++d) {
+            const int b = a + d;
+            int n = 0;
+            if (b < nc) {
+#pragma unroll
+                for (int w = 0; w < kPairMaxWords; ++w)
+                    if (w < words) n += __popc(mine[w] & bits[w * nc + b]);
+            }
+            ov[(d - 1) * nc + a] = static_cast<uint8_t>(n > 255 ? 255 : n);
+        }
+    }
+    __syncthreads();
+    for (int r = 0; r < kPairRounds; ++r) {
+        int bb = -1;
+        if (live && partner[a] < 0) {
+            int bw = -1;
+            for (int d = kPairWindow; d >= 1; --d) {      // b = a - d, ascending b
+                const int b = a - d;
+                if (b < 0 || partner[b] >= 0) continue;
+                const int w = ov[(d - 1) * nc + b];
+                if (w > bw) { bw = w; bb = b; }
+            }
+            for (int d = 1; d <= kPairWindow; ++d) {      // b = a + d, ascending b
+                const int b = a + d;
+                if (b >= nc) break;
+                if (partner[b] >= 0) continue;
+                const int w = ov[(d - 1) * nc + a];
+                if (w > bw) { bw = w; bb = b; }
+            }
+        }
+        if (live) best[a] = static_cast<int16_t>(bb);
+        __syncthreads();
+        if (live && partner[a] < 0 && bb >= 0 && best[bb] == a) partner[a] = static_cast<int16_t>(bb);
+        __syncthreads();
+    }
+    // the cubes still unpaired pair up in index order
+    int n_left = 0;
+    const bool left = live && partner[a] < 0;
+    const int lr = block_exclusive_scan(left ? 1 : 0, warp_tot, &n_left);
+    if (left) list[lr] = static_cast<int16_t>(a);
+    __syncthreads();
+    if (left && (lr & 1) == 0 && lr + 1 < n_left) {
+        const int b = list[lr + 1];
+        partner[a] = static_cast<int16_t>(b);
+        partner[b] = static_cast<int16_t>(a);
+    }
+    __syncthreads();
+    // pairs in order of their first cube
+    const int pb = live ? partner[a] : 0;
+    const bool first = live && (pb > a || pb < 0);
+    int n_out = 0;
+    const int p = block_exclusive_scan(first ? 1 : 0, warp_tot, &n_out);
+    if (first) {
+        int32_t* out = pairs + (bh * static_cast<long long>((nc + 1) / 2) + p) * 2;
+        out[0] = a;
+        out[1] = pb > a ? pb : -1;
+    }
+}
+
+}  // namespace
+}  // namespace gbattn
+
+extern "C" int vsa_pair_query_cubes(const int32_t* idx, int B, int H, int n_cubes, int topk,
+                                    int32_t* pairs, void* stream) {
+    if (!idx || !pairs) return GBATTN_ERR_NULL;
+    if (B <= 0 || H <= 0 || n_cubes <= 0 || topk <= 0 || topk > n_cubes) return GBATTN_ERR_SHAPE;
+    if (n_cubes > kPairMaxCubes || static_cast<long long>(B) * H > 0x7FFFFFFFLL)
+        return GBATTN_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(pairs) & 3u))
+        return GBATTN_ERR_ALIGN;
+    const size_t ib = static_cast<size_t>(B) * H * n_cubes * topk * 4;
+    const size_t pb = static_cast<size_t>(B) * H * ((n_cubes + 1) / 2) * 2 * 4;
+    if (overlaps(pairs, pb, idx, ib)) return GBATTN_ERR_ALIAS;
+    DeviceState dev;
+    int rc = current_device(&dev);
+    if (rc != GBATTN_OK) return rc;
+    const size_t smem = pair_smem_bytes(n_cubes);
+    static std::once_flag once[64];
+    if (dev.device >= 0 && dev.device < 64)
+        std::call_once(once[dev.device], [] {
+            cudaFuncSetAttribute(vsa_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(pair_smem_bytes(kPairMaxCubes)));
+        });
+    vsa_pair_kernel<<<static_cast<unsigned>(static_cast<long long>(B) * H), kPairThreads, smem,
+                      static_cast<cudaStream_t>(stream)>>>(idx, n_cubes, topk, pairs);
+    count_launches(1);
+    return launch_status();
+}
+
 // ------------------------------------------------------------------ no-allocation variant
 //
 // Some callers cannot allocate device memory when they call this library: a

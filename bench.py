@@ -4,7 +4,7 @@ One step is one pass of the whole hot path over one batch of synthetic input,
 all three variants at full size:
   * dense video attention      B1 H24 S32768 D128                (attn_dense_fwd)
   * VSA                         B1 H24 S32768 D128, 512 cubes, top-64
-                                (vsa_select_blocks + vsa_sparse_fwd)
+                                (vsa_select_blocks + vsa_pair_query_cubes + vsa_sparse_fwd)
   * paged E4M3 long prefill     Hq6 Hkv1 D256, Q=8192 after KV=131072
                                 (e4m3_paged_to_fp16 + attn_causal_prefill_fwd)
 The metric is useful attention TFLOP/s (4 * D * visible (query, key) pairs per
@@ -103,6 +103,8 @@ class Workload:
             S = self.q.shape[2]
             nc = S // 64
             self.idx = torch.empty((w["B"], w["H"], nc, w["topk"]), dtype=torch.int32, device=dev)
+            self.pairs = torch.empty((w["B"], w["H"], (nc + 1) // 2, 2), dtype=torch.int32,
+                                     device=dev)
             ws = gb.vsa_select_workspace_size(w["B"], w["H"], S, w["D"], 64)
             self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
             self.o = torch.empty_like(self.q)
@@ -131,8 +133,11 @@ class Workload:
             return [("vsa_select_blocks",
                      lambda: gb.vsa_select_blocks(self.q, self.k, w["topk"], idx=self.idx,
                                                   workspace=self.ws)),
+                    ("vsa_pair_query_cubes",
+                     lambda: gb.vsa_pair_query_cubes(self.idx, pairs=self.pairs)),
                     ("vsa_sparse_fwd",
-                     lambda: gb.vsa_sparse_fwd(self.q, self.k, self.v, self.idx, o=self.o))]
+                     lambda: gb.vsa_sparse_fwd(self.q, self.k, self.v, self.idx, pairs=self.pairs,
+                                               o=self.o))]
         return [("e4m3_paged_to_fp16",
                  lambda: gb.e4m3_paged_to_fp16(self.kp, self.vp, self.table, w["KV"], w["k_scale"],
                                                w["v_scale"], k_out=self.kf, v_out=self.vf)),
@@ -528,8 +533,11 @@ def measure_vsa_full(gb, torch, dev, steps, warmup, pk):
         gb.vsa_select_blocks(dq, dk, w["topk"], prefix=w["prefix"], cube_valid=dval, idx=idx,
                              workspace=ws)
 
+    pairs = torch.empty((w["B"], w["H"], (nc + 1) // 2, 2), dtype=torch.int32, device=dev)
+
     def sparse():
-        gb.vsa_sparse_fwd(dq, dk, dv, idx, prefix=w["prefix"], cube_valid=dval, o=o)
+        gb.vsa_pair_query_cubes(idx, pairs=pairs)
+        gb.vsa_sparse_fwd(dq, dk, dv, idx, prefix=w["prefix"], cube_valid=dval, pairs=pairs, o=o)
 
     for _ in range(warmup):
         select()
@@ -537,9 +545,9 @@ def measure_vsa_full(gb, torch, dev, steps, warmup, pk):
     torch.cuda.synchronize()
     real = int(valid.sum())
     sel = idx.cpu().numpy()                                 # work count only
-    pairs = w["prefix"] * (w["prefix"] + real) * w["B"] * w["H"]
-    pairs += int((valid[sel].sum(axis=-1) * valid[None, None, :]).sum())
-    flops = 4.0 * w["D"] * pairs
+    visited = w["prefix"] * (w["prefix"] + real) * w["B"] * w["H"]
+    visited += int((valid[sel].sum(axis=-1) * valid[None, None, :]).sum())
+    flops = 4.0 * w["D"] * visited
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for e in ev:
         flush.fill_(1)
@@ -683,7 +691,8 @@ def main():
     pk = peaks()
 
     # ---- dominant kernel roofline
-    attn_calls = {k: v for k, v in per_call.items() if "select" not in k and "e4m3_paged" not in k}
+    attn_calls = {k: v for k, v in per_call.items()
+                  if "select" not in k and "e4m3_paged" not in k and "pair" not in k}
     dom = max(attn_calls, key=attn_calls.get)
     dom_w = next(w for w in wls if dom.startswith(w.name + ":"))
     achieved = dom_w.flops / (attn_calls[dom] * 1e-3) / 1e12

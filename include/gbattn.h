@@ -265,8 +265,9 @@ int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S,
  * block, with a 4-bit quadrant mask, and per-tile valid counts).
  *   q, k, v, o : [B][H][S][D] FP16; tokens [0, prefix) are prefix tokens, tokens
  *   [prefix, S) the cube-major video tokens; idx: int32 [B][H][(S-prefix)/block][topk]
- *   strictly ascending per row; cube_valid as for vsa_select_blocks (NULL: full cubes);
- *   lse optional [B][H][S].
+ *   strictly ascending per row; pairs: the query cubes each CTA takes two at a time
+ *   (vsa_pair_query_cubes), or NULL for cubes 2p and 2p+1; cube_valid as for
+ *   vsa_select_blocks (NULL: full cubes); lse optional [B][H][S].
  *   A prefix query attends densely to every prefix token and every real video token; a real
  *   video query in cube c attends exactly the real tokens of cubes idx[b][h][c][*]; a padding
  *   query slot gets O = 0, lse = -inf.  Padding slots of V must hold finite values (their
@@ -274,9 +275,26 @@ int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S,
  *   block == 64, D == 128, prefix % 128 == 0, (S - prefix) % block == 0,
  *   1 <= topk <= min((S-prefix)/block, 512), prefix/128 + ceil(cubes/2) <= 512.
  */
-int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx, int prefix,
-                   const int32_t* cube_valid, void* o, float* lse, int B, int H, int S, int D,
-                   int block, int topk, float scale, void* stream);
+int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
+                   const int32_t* pairs, int prefix, const int32_t* cube_valid, void* o,
+                   float* lse, int B, int H, int S, int D, int block, int topk, float scale,
+                   void* stream);
+
+/*
+ * Pairs the video query cubes of every head for vsa_sparse_fwd, which runs two query cubes per
+ * CTA over the union of their selections: cubes whose selections overlap more waste less.
+ * Cites: FastVideo compare view, block_lists.py (two 64-token query halves per 128-row block).
+ * Not a step of the method: the attention result does not depend on the pairing (up to the
+ * summation order); it only changes how much work the union tiles carry.
+ *   idx   : int32 [B][H][n_cubes][topk] from vsa_select_blocks.
+ *   pairs : int32 [B][H][ceil(n_cubes/2)][2], every cube exactly once; the second entry of a
+ *           pair is -1 for the one unpaired cube of an odd count.
+ *   Each head: overlaps of every cube with the cubes up to 32 index positions away, 4 rounds of
+ *   mutual best partners (ties to the lower index), the rest paired in index order; pairs are
+ *   listed by their first cube.  n_cubes <= 1024.
+ */
+int vsa_pair_query_cubes(const int32_t* idx, int B, int H, int n_cubes, int topk, int32_t* pairs,
+                         void* stream);
 
 #ifdef __cplusplus
 }

@@ -188,16 +188,22 @@ def test_select_and_sparse_validation(lib):
     assert f(P, P2, 1, 24, 32768, 128, 64, 64, 0, MIS2, P3, P4, ws, None) == ALIGN
     assert f(P, P2, 1, 24, 32768, 128, 64, 64, 0, None, P3, P4, ws, None) in (CUDA, OK)
     g = lib.vsa_sparse_fwd
-    # q, k, v, idx, prefix, cube_valid, o, lse, B, H, S, D, block, topk, scale, stream
-    assert g(P, P2, P3, P4, 0, None, None, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == NULL
-    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), 0, None, P, None, 1, 24, 32768, 128, 64, 64,
-             0.08, None) == ALIAS
-    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), 0, None, P4, None, 1, 24, 32768, 128, 64, 600,
-             0.08, None) == SHAPE
-    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), 64, None, P4, None, 1, 24, 32768 + 64, 128,
-             64, 64, 0.08, None) == SHAPE          # prefix must be whole 128-row query tiles
-    assert g(P, P2, P3, ctypes.c_void_p(0x70000000), 128, MIS2, P4, None, 1, 24, 32768 + 128, 128,
-             64, 64, 0.08, None) == ALIGN
+    # q, k, v, idx, pairs, prefix, cube_valid, o, lse, B, H, S, D, block, topk, scale, stream
+    I = ctypes.c_void_p(0x70000000)
+    assert g(P, P2, P3, P4, None, 0, None, None, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == NULL
+    assert g(P, P2, P3, I, None, 0, None, P, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == ALIAS
+    assert g(P, P2, P3, I, None, 0, None, P4, None, 1, 24, 32768, 128, 64, 600, 0.08, None) == SHAPE
+    assert g(P, P2, P3, I, None, 64, None, P4, None, 1, 24, 32768 + 64, 128, 64, 64, 0.08,
+             None) == SHAPE                        # prefix must be whole 128-row query tiles
+    assert g(P, P2, P3, I, None, 128, MIS2, P4, None, 1, 24, 32768 + 128, 128, 64, 64, 0.08,
+             None) == ALIGN
+    assert g(P, P2, P3, I, MIS2, 0, None, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == ALIGN
+    h = lib.vsa_pair_query_cubes
+    assert h(None, 1, 24, 512, 64, P4, None) == NULL
+    assert h(I, 1, 24, 2048, 64, P4, None) == SHAPE     # more cubes than the pairing takes
+    assert h(I, 1, 24, 512, 600, P4, None) == SHAPE
+    assert h(I, 1, 24, 512, 64, I, None) == ALIAS
+    assert h(I, 1, 24, 512, 64, P4, None) in (CUDA, OK)
 
 
 def test_product_package_does_not_import_oracle():

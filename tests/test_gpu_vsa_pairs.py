@@ -1,0 +1,105 @@
+"""Query-cube pairing for the sparse attention: a valid pairing, and outputs that
+match the oracle whatever the pairing (|o - ref| <= 2e-3 + 1e-2 |ref|)."""
+
+import numpy as np
+import pytest
+import torch
+
+from attention_fp16_flashattention_gb300 import inputs
+from oracle import attention as OA
+from oracle import vsa as OV
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def t(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def assert_close(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    both_inf = np.isneginf(got) & np.isneginf(ref)
+    with np.errstate(invalid="ignore"):
+        excess = np.where(both_inf, -1.0, np.abs(got - ref) - (ATOL + RTOL * np.abs(ref)))
+    bad = int((excess > 0).sum())
+    assert bad == 0, f"{what}: {bad} of {excess.size} outside tolerance, max excess {excess.max():.3e}"
+
+
+def check_pairing(pairs, nc):
+    for row in pairs.reshape(-1, (nc + 1) // 2, 2):
+        seen = row.reshape(-1)
+        real = seen[seen >= 0]
+        assert np.array_equal(np.sort(real), np.arange(nc))        # every cube exactly once
+        assert (seen < 0).sum() == nc % 2
+        assert np.all(row[:, 0] >= 0)
+        assert np.all(np.diff(row[:, 0]) > 0)                       # listed by first cube
+
+
+@pytest.mark.parametrize("grid,topk", [((8, 32, 32), 16), ((4, 16, 20), 9), ((4, 12, 12), 4)])
+def test_pairing_valid_and_sparse_matches(gb, grid, topk):
+    q, k, v = inputs.vsa_inputs(1, 3, 128, seed=50 + topk, grid=grid)
+    tq, tk, tv = t(q), t(k), t(v)
+    idx = gb.vsa_select_blocks(tq, tk, topk)
+    pairs = gb.vsa_pair_query_cubes(idx)
+    torch.cuda.synchronize()
+    nc = idx.shape[2]
+    check_pairing(pairs.cpu().numpy(), nc)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    o = gb.vsa_sparse_fwd(tq, tk, tv, idx, pairs=pairs, lse=lse)
+    torch.cuda.synchronize()
+    ridx = OV.vsa_select(q, k, 64, topk)
+    ro, rl = OA.vsa_sparse_attention(q, k, v, ridx, 64, inputs.softmax_scale(128))
+    assert gb.device_status() == 0
+    assert_close(o.float().cpu().numpy(), ro, "o")
+    assert_close(lse.cpu().numpy(), rl, "lse")
+
+
+def test_pairing_with_prefix_and_boundary_cubes(gb):
+    q, k, v, valid = inputs.vsa_full_inputs(1, 2, 128, seed=57, grid=(5, 10, 9), prefix=128)
+    tq, tk, tv, tval = t(q), t(k), t(v), t(valid)
+    idx = gb.vsa_select_blocks(tq, tk, 5, prefix=128, cube_valid=tval)
+    pairs = gb.vsa_pair_query_cubes(idx)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    o = gb.vsa_sparse_fwd(tq, tk, tv, idx, prefix=128, cube_valid=tval, pairs=pairs, lse=lse)
+    torch.cuda.synchronize()
+    check_pairing(pairs.cpu().numpy(), valid.size)
+    ridx = OV.vsa_select(q, k, 64, 5, valid, prefix=128)
+    ro, rl = OA.vsa_sparse_attention(q, k, v, ridx, 64, inputs.softmax_scale(128), valid=valid,
+                                     prefix=128)
+    assert gb.device_status() == 0
+    assert_close(o.float().cpu().numpy(), ro, "o")
+    assert_close(lse.cpu().numpy(), rl, "lse")
+
+
+def test_bad_pairs_flagged(gb):
+    q, k, v = inputs.vsa_inputs(1, 1, 128, seed=58, grid=(4, 16, 16))
+    tq, tk, tv = t(q), t(k), t(v)
+    idx = gb.vsa_select_blocks(tq, tk, 4)
+    pairs = gb.vsa_pair_query_cubes(idx)
+    bad = pairs.clone()
+    bad[0, 0, 0, 0] = 10_000
+    gb.vsa_sparse_fwd(tq, tk, tv, idx, pairs=bad)
+    torch.cuda.synchronize()
+    assert gb.device_status() & gb.DEV_BAD_INDEX
+
+
+def test_pairing_full_workload(gb):
+    """The benchmark's launch: B1 H24 S32768 D128, top-64, sampled rows."""
+    w = inputs.WORKLOADS["vsa_video"]
+    q, k, v = inputs.vsa_inputs(w["B"], w["H"], w["D"], w["seed"], w["grid"], w["cube"])
+    tq, tk, tv = t(q), t(k), t(v)
+    idx = gb.vsa_select_blocks(tq, tk, w["topk"])
+    pairs = gb.vsa_pair_query_cubes(idx)
+    o = gb.vsa_sparse_fwd(tq, tk, tv, idx, pairs=pairs)
+    torch.cuda.synchronize()
+    assert gb.device_status() == 0
+    nc = idx.shape[2]
+    check_pairing(pairs.cpu().numpy(), nc)
+    S = q.shape[2]
+    rows = inputs.sample_rows(w["B"] * w["H"], S, 4096, w["seed"])
+    ridx = idx.cpu().numpy()          # the selection itself is checked bit-exact elsewhere
+    ro, _ = OA.vsa_sparse_attention(q, k, v, ridx, 64, inputs.softmax_scale(w["D"]), rows=rows)
+    fo = o.float().cpu().numpy().reshape(-1, S, w["D"])[rows[:, 0], rows[:, 1]]
+    assert_close(fo, ro, "o")
