@@ -37,6 +37,8 @@ _SIGNATURES = {
     "attn_causal_prefill_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                                      _vp, _sz, _vp]),
     "e4m3_paged_to_fp16": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _vp, _vp, _vp]),
+    "attn_causal_prefill_paged_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                           _i, _i, _i, _i, _f, _f, _f, _vp, _sz, _vp]),
     "attn_paged_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "attn_paged_decode_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                    _i, _i, _f, _f, _f, _vp, _sz, _vp]),
@@ -210,6 +212,40 @@ def attn_causal_prefill_fwd(q, k, v, q_real=None, o=None, lse=None, scale=None, 
                                         workspace.numel() * workspace.element_size(),
                                         _stream(stream))
     _check("attn_causal_prefill_fwd", rc)
+    return o
+
+
+def attn_causal_prefill_paged_fwd(q, k_pages, v_pages, page_table, kv_len, k_scale, v_scale,
+                                  q_real=None, o=None, lse=None, scale=None, workspace=None,
+                                  stream=None):
+    """Causal prefill over paged E4M3 K/V (the bridge fused in).  q [B,Hq,Q_pad,D] FP16;
+    pages [P,page,Hkv,D] uint8; page_table int32 [B,max_pages] (or [max_pages] for B=1)."""
+    import torch
+    _need(q, "q", torch.float16, 4)
+    _need(k_pages, "k_pages", torch.uint8, 4)
+    _need(v_pages, "v_pages", torch.uint8, 4)
+    B, Hq, Qp, D = q.shape
+    table = page_table.reshape(1, -1) if page_table.dim() == 1 else page_table
+    _need(table, "page_table", torch.int32, 2)
+    if table.shape[0] != B:
+        raise ValueError("page_table needs one row per batch entry")
+    P, ps, Hkv, Dk = k_pages.shape
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or Dk != D:
+        raise ValueError("k_pages and v_pages must be [P, page, Hkv, D] matching q")
+    q_real = Qp if q_real is None else int(q_real)
+    o = torch.empty_like(q) if o is None else o
+    _need(o, "o", torch.float16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    if workspace is None:
+        nbytes = attn_causal_prefill_workspace_size(B, Hq, Qp, int(kv_len), D)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    rc = load().attn_causal_prefill_paged_fwd(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(table), _ptr(o), _ptr(lse), B, Hq, Hkv, Qp,
+        q_real, int(kv_len), D, P, ps, table.shape[1], float(k_scale), float(v_scale),
+        _scale(scale, D), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check("attn_causal_prefill_paged_fwd", rc)
     return o
 
 

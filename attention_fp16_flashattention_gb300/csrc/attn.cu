@@ -34,6 +34,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "e4m3.cuh"
 #include "host.h"
 #include "ptx.cuh"
 
@@ -42,7 +43,6 @@ namespace {
 
 constexpr int BM = 128;             // query rows per CTA
 constexpr int BN = 128;             // keys per tile (two halves of 64)
-constexpr int kThreads = 320;          // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int kSoftmaxThreads = 256;
 constexpr int kMaxSparseTiles = 512;
 constexpr int kMaxTopk = 512;
@@ -50,8 +50,13 @@ constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s for draining after an abo
 
 // kMasked: dense with an additive FP16 mask [Sq][Skv] per (batch, head) slice.
 // kSparseFull: kSparse with the full VSA layout (prefix queries, boundary cubes).
-enum Mode { kDense = 0, kCausal = 1, kSparse = 2, kMasked = 3, kSparseFull = 4 };
+// kCausalPaged: kCausal reading K/V as E4M3 pages (converted in shared memory).
+enum Mode { kDense = 0, kCausal = 1, kSparse = 2, kMasked = 3, kSparseFull = 4, kCausalPaged = 5 };
 __host__ __device__ constexpr bool is_sparse(int mode) { return mode == kSparse || mode == kSparseFull; }
+__host__ __device__ constexpr bool is_causal(int mode) { return mode == kCausal || mode == kCausalPaged; }
+// threads per CTA: the paged mode adds four converter warps (10..13)
+__host__ __device__ constexpr int threads_for(int mode) { return mode == kCausalPaged ? 448 : 320; }
+constexpr int kConvThreads = 128;
 
 struct AttnArgs {
     int seq_q;          // query rows per head
@@ -73,6 +78,12 @@ struct AttnArgs {
     float* part_lse;    // causal, n_chunks > 1: [C][heads_q][seq_q] log2-sum-exp2
     const int32_t* idx; // sparse: [heads][n_cubes][topk]
     int prefix;         // sparse: prefix tokens before the video cubes (multiple of BM)
+    const int32_t* page_table;   // paged: [B][max_pages] logical -> physical page
+    int num_phys, page_size, max_pages, page_box;   // paged: pool, rows per TMA box
+    int scale_mode;     // paged: 0 folded power of two, 1 FP16-valued, 2 general
+    float ks, vs;       // paged: dequantisation scales
+    __half2 ks2, vs2;
+    float out_mul;      // v_scale when folded (applied to O), else 1
     const int32_t* pairs;   // sparse: [heads][ceil(n_cubes/2)][2] query-cube pairs, or null
                             //         (cubes 2p, 2p+1); a second entry of -1 means none
     const int32_t* cube_valid;   // sparse: real tokens per cube, or null (all full)
@@ -113,6 +124,8 @@ struct Ctrl {
                            // of every barrier awaited below has completed.
     uint64_t drain;
     uint64_t xchg[4];      // per row quarter: the two half-row threads exchange values
+    uint64_t raw_full[2];  // paged: E4M3 bytes of a slot landed (converters may read)
+    uint64_t conv_read[2]; // paged: every converter holds its bytes (the slot may be overwritten)
     uint32_t tmem_base;
     int abort;
     int n_tiles;
@@ -289,7 +302,7 @@ __device__ void fill_tile_counts(SparseTiles* st, const Ctrl* ctrl, const AttnAr
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(MODE), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmM,
                     const AttnArgs a) {
@@ -330,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- work decode
     int q_row0, kv_bh, n_tiles = 0, tile0 = 0, chunk = 0;
-    if (MODE == kCausal) {
+    if (is_causal(MODE)) {
         const int qt = blockIdx.x / a.n_chunks;
         chunk = blockIdx.x - qt * a.n_chunks;
         q_row0 = qt * BM;
@@ -376,9 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(&ctrl->q_full, 1);
         for (int i = 0; i < C::NS; ++i) {
-            mbar_init(&ctrl->full[i], 1);
+            // paged: the four converter warps complete a slot, not the TMA bytes
+            mbar_init(&ctrl->full[i], MODE == kCausalPaged ? kConvThreads / 32 : 1);
             mbar_init(&ctrl->empty[i], 1);
         }
+        if (MODE == kCausalPaged)
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&ctrl->raw_full[i], 1);
+                mbar_init(&ctrl->conv_read[i], kConvThreads / 32);
+            }
         for (int i = 0; i < C::NSB; ++i) {
             mbar_init(&ctrl->s_full[i], 1);
             mbar_init(&ctrl->p_full[i], kSoftmaxThreads);
@@ -449,8 +468,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             bool ok = true;
+            // paged: lane j holds the cache row of box j (page_box tokens) of the
+            // item after the one being issued; boxes cover the item's 128 keys.
+            const int n_box = MODE == kCausalPaged ? BN / a.page_box : 0;
+            auto page_row = [&](int item) -> int {
+                if (MODE != kCausalPaged || lane >= n_box || item >= 2 * n_tiles) return 0;
+                int t, k0, k1;
+                bool iv;
+                ring_item(item, n_tiles, C::NSB, t, iv);
+                tile_keys(t, k0, k1);
+                const int tok = k0 + lane * a.page_box;
+                const int b = kv_bh / a.hkv;
+                int page = tok < a.seq_k ? a.page_table[static_cast<long long>(b) * a.max_pages +
+                                                        tok / a.page_size]
+                                         : 0;
+                if (page < 0 || page >= a.num_phys) {
+                    atomicOr(a.status, kDevBadPage);
+                    page = 0;
+                }
+                return page * a.page_size + tok % a.page_size;
+            };
+            int prow_next = page_row(0);
             for (int it = 0; it < 2 * n_tiles; ++it) {
                 const int slot = it % C::NS;
+                const int prow_cur = prow_next;
+                if (MODE == kCausalPaged) prow_next = page_row(it + 1);
                 if (!wait_warp(&ctrl->empty[slot], ((it / C::NS) & 1) ^ 1u, w)) { ok = false; break; }
                 int t;
                 bool is_v;
@@ -459,6 +501,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_keys(t, k0, k1);
                 const CUtensorMap* m = is_v ? &tmV : &tmK;
                 uint8_t* dst = sKV + slot * C::SLOT_BYTES;
+                if (MODE == kCausalPaged) {
+                    // E4M3 rows of the item (128 keys x D bytes) into the slot's upper half,
+                    // laid out [key half][column half][64 rows][128 bytes], 128-byte swizzle.
+                    uint8_t* stage = dst + C::SLOT_BYTES / 2;
+                    const int hk = kv_bh % a.hkv;
+                    const int rows_per_box = a.page_box;
+                    int rows[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) rows[j] = __shfl_sync(0xffffffffu, prow_cur, j);
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(&ctrl->raw_full[slot], BN * D);
+                        for (int j = 0; j < n_box; ++j) {
+                            const int key = j * rows_per_box;   // 0..127 within the item
+                            const int kh = key >> 6, r = key & 63;
+#pragma unroll
+                            for (int ch = 0; ch < D / 128; ++ch)
+                                tma_load_3d(stage + (kh * (D / 128) + ch) * 8192 + r * 128, m,
+                                            &ctrl->raw_full[slot], 128 * ch, hk, rows[j]);
+                        }
+                    }
+                    __syncwarp();
+                    last_it[slot] = it;
+                    continue;
+                }
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&ctrl->full[slot], C::SLOT_BYTES);
 #pragma unroll
@@ -474,7 +540,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok && lane == 0) {   // let copies in flight land before the CTA exits
                 if (load_q) drain_wait(&ctrl->q_full, 0);
                 for (int s = 0; s < C::NS; ++s)
-                    if (last_it[s] >= 0) drain_wait(&ctrl->full[s], (last_it[s] / C::NS) & 1);
+                    if (last_it[s] >= 0)
+                        drain_wait(MODE == kCausalPaged ? &ctrl->raw_full[s] : &ctrl->full[s],
+                                   (last_it[s] / C::NS) & 1);
             }
         }
     } else if (warp == 1) {
@@ -550,6 +618,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) drain_wait(&ctrl->drain, 0);
             }
         }
+    } else if (MODE == kCausalPaged && warp >= 10) {
+        // ================= E4M3 -> FP16 converters (warps 10..13, paged mode)
+        // Thread ct owns key row ct of every item: it reads the row's D E4M3 bytes
+        // from the slot's upper half into registers, waits for the other
+        // converters (the FP16 tile overwrites that half), then writes the FP16
+        // row into the 128-byte-swizzled K-major layout TMA would have produced.
+        const int ct = threadIdx.x - 320;
+        const int kh = ct >> 6, rr = ct & 63;
+        bool ok = true;
+        for (int it = 0; it < 2 * n_tiles; ++it) {
+            const int slot = it % C::NS;
+            ok = wait_warp(&ctrl->raw_full[slot], (it / C::NS) & 1, w);
+            if (!ok) break;
+            int t;
+            bool is_v;
+            ring_item(it, n_tiles, C::NSB, t, is_v);
+            uint8_t* dst = sKV + slot * C::SLOT_BYTES;
+            const uint8_t* stage = dst + C::SLOT_BYTES / 2;
+            uint4 raw[D / 16];
+#pragma unroll
+            for (int ch = 0; ch < D / 128; ++ch)
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    raw[ch * 8 + u] = *reinterpret_cast<const uint4*>(
+                        stage + (kh * (D / 128) + ch) * 8192 + rr * 128 + ((u ^ (rr & 7)) << 4));
+            // all converters must hold their bytes before any FP16 lands on the bytes
+            // (a time-bounded barrier wait, like every other wait of the kernel)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->conv_read[slot]);
+            ok = wait_warp(&ctrl->conv_read[slot], (it / C::NS) & 1, w);
+            if (!ok) break;
+            const float sc = is_v ? a.vs : a.ks;
+            const __half2 sc2 = is_v ? a.vs2 : a.ks2;
+            int k0, k1;
+            tile_keys(t, k0, k1);
+            const bool live_key = k0 + ct < a.seq_k;   // rows past the cache end become zeros
+#pragma unroll
+            for (int q = 0; q < D / 16; ++q) {   // 16 E4M3 bytes -> 16 halves (2 units)
+                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+                if (live_key) {
+                    if (a.scale_mode == 2) {
+                        convert16<false>(raw[q], sc2, sc, lo, hi);
+                    } else if (a.scale_mode == 1) {
+                        convert16<true>(raw[q], sc2, sc, lo, hi);
+                    } else {   // power-of-two scale: applied to the scores and outputs instead
+                        const uint32_t w4[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+                        uint32_t h[8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            h[2 * i] = e4m3x2_to_f16x2(w4[i] & 0xFFFFu);
+                            h[2 * i + 1] = e4m3x2_to_f16x2(w4[i] >> 16);
+                        }
+                        lo = make_uint4(h[0], h[1], h[2], h[3]);
+                        hi = make_uint4(h[4], h[5], h[6], h[7]);
+                    }
+                }
+                const int d0 = q * 16;            // head-width position of the 16 values
+                const int c = d0 >> 6, u0 = (d0 & 63) >> 3;
+                uint8_t* row = dst + c * C::CHUNK + kh * C::HALF + rr * 128;
+                *reinterpret_cast<uint4*>(row + ((u0 ^ (rr & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ (rr & 7)) << 4)) = hi;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the MMAs
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->full[slot]);
+        }
+        (void)ok;
     } else {
         // ================= softmax / correction / epilogue (warps 2..9)
         // Two threads share each query row: warps 2..5 own key columns 0..63 of
@@ -566,9 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_half = row >> 6;
         uint64_t* xbar = &ctrl->xchg[quarter];
         int lim = a.seq_k;   // keys >= lim are invisible to this row
-        if (MODE == kCausal)
+        if (is_causal(MODE))
             lim = static_cast<int>(min(static_cast<long long>(a.seq_k), a.kv_prefix + row_g + 1));
-        const int lim0 = MODE == kCausal
+        const int lim0 = is_causal(MODE)
                              ? static_cast<int>(min(static_cast<long long>(a.seq_k),
                                                     static_cast<long long>(a.kv_prefix) + q_row0 + 1))
                              : a.seq_k;
@@ -759,14 +894,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             const bool row_ok = row_g < a.seq_q;
-            bool zero_row = MODE == kCausal && row_g >= a.q_real;
+            bool zero_row = is_causal(MODE) && row_g >= a.q_real;
             if (MODE == kSparseFull && row_g >= a.prefix && row_g < a.seq_q) {   // padding query slot
                 const int vr = static_cast<int>(row_g - a.prefix);
                 zero_row = (vr & 63) >= cube_count(a, vr >> 6);
             }
-            const float inv_l = (l > 0.0f && !zero_row) ? 1.0f / l : 0.0f;
+            const float inv_l = (l > 0.0f && !zero_row) ? (MODE == kCausalPaged ? a.out_mul : 1.0f) / l : 0.0f;
             const float lse2 = (l > 0.0f && !zero_row) ? m_run + __log2f(l) : -INFINITY;
-            const bool partial = MODE == kCausal && a.n_chunks > 1;
+            const bool partial = is_causal(MODE) && a.n_chunks > 1;
             const long long orow = static_cast<long long>(bh) * a.seq_q + row_g;
 #pragma unroll 1
             for (int cc = 0; cc < D / 64; ++cc) {
@@ -886,18 +1021,23 @@ int set_smem_attr() {
 template <int D, int MODE>
 int launch_attn(const void* q, const void* k, const void* v, int seq_q, int seq_k, int heads_q,
                 int heads_kv, dim3 grid, AttnArgs args, cudaStream_t stream,
-                const CUtensorMap* mask_map = nullptr) {
+                const CUtensorMap* mask_map = nullptr, const CUtensorMap* kv_maps = nullptr) {
     CUtensorMap tq, tk, tv;
-    if (encode_tmap_f16_3d(&tq, q, D, seq_q, heads_q, 64, BM) != GBATTN_OK ||
-        encode_tmap_f16_3d(&tk, k, D, seq_k, heads_kv, 64, 64) != GBATTN_OK ||
-        encode_tmap_f16_3d(&tv, v, D, seq_k, heads_kv, 64, 64) != GBATTN_OK)
+    if (encode_tmap_f16_3d(&tq, q, D, seq_q, heads_q, 64, BM) != GBATTN_OK)
         return GBATTN_ERR_CUDA;
+    if (kv_maps) {   // paged E4M3 K and V
+        tk = kv_maps[0];
+        tv = kv_maps[1];
+    } else if (encode_tmap_f16_3d(&tk, k, D, seq_k, heads_kv, 64, 64) != GBATTN_OK ||
+               encode_tmap_f16_3d(&tv, v, D, seq_k, heads_kv, 64, 64) != GBATTN_OK) {
+        return GBATTN_ERR_CUDA;
+    }
     CUtensorMap tq64;   // sparse modes: query cubes load as two 64-row boxes
     if (is_sparse(MODE) && encode_tmap_f16_3d(&tq64, q, D, seq_q, heads_q, 64, 64) != GBATTN_OK)
         return GBATTN_ERR_CUDA;
     int rc = set_smem_attr<D, MODE>();
     if (rc != GBATTN_OK) return rc;
-    attn_fwd_kernel<D, MODE><<<grid, kThreads, smem_bytes<D, MODE>(), stream>>>(
+    attn_fwd_kernel<D, MODE><<<grid, threads_for(MODE), smem_bytes<D, MODE>(), stream>>>(
         tq, tk, tv, mask_map ? *mask_map : (is_sparse(MODE) ? tq64 : tq), args);
     count_launches(1);
     return launch_status();
@@ -1118,6 +1258,109 @@ extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void*
     count_launches(1);
     return launch_status();
 }
+
+extern "C" int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pages,
+                                             const uint8_t* v_pages, const int32_t* page_table,
+                                             void* o, float* lse, int B, int Hq, int Hkv,
+                                             int Q_pad, int Q_real, int KV, int D,
+                                             int num_phys_pages, int page_size, int max_pages,
+                                             float k_scale, float v_scale, float scale,
+                                             void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+    if (!q || !k_pages || !v_pages || !page_table || !o) return GBATTN_ERR_NULL;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Q_pad <= 0 || KV <= 0 || num_phys_pages <= 0 ||
+        page_size <= 0 || max_pages <= 0)
+        return GBATTN_ERR_SHAPE;
+    if (Hq % Hkv != 0 || Q_pad % 64 != 0 || Q_real < 1 || Q_real > Q_pad || Q_real > KV ||
+        KV % 32 != 0 || static_cast<long long>(KV) > static_cast<long long>(max_pages) * page_size)
+        return GBATTN_ERR_SHAPE;
+    if (static_cast<long long>(B) * Hq > 65535) return GBATTN_ERR_SHAPE;
+    if (D != 256) return GBATTN_ERR_UNSUPPORTED;
+    if (page_size < 16 || (page_size & (page_size - 1)) != 0 ||
+        static_cast<long long>(num_phys_pages) * page_size > 0x7FFFFFFFLL)
+        return GBATTN_ERR_UNSUPPORTED;
+    if (!finite_positive(scale) || !finite_positive(k_scale) || !finite_positive(v_scale))
+        return GBATTN_ERR_SCALE;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(page_table) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return GBATTN_ERR_ALIGN;
+    const size_t qb = static_cast<size_t>(B) * Hq * Q_pad * D * 2;
+    const size_t pb = static_cast<size_t>(num_phys_pages) * page_size * Hkv * D;
+    const size_t tb = static_cast<size_t>(B) * max_pages * 4;
+    const size_t lb = static_cast<size_t>(B) * Hq * Q_pad * 4;
+    if (overlaps(o, qb, q, qb) || overlaps(o, qb, k_pages, pb) || overlaps(o, qb, v_pages, pb) ||
+        overlaps(o, qb, page_table, tb) || overlaps(lse, lb, q, qb) ||
+        overlaps(lse, lb, k_pages, pb) || overlaps(lse, lb, v_pages, pb) ||
+        overlaps(lse, lb, page_table, tb) || overlaps(lse, lb, o, qb))
+        return GBATTN_ERR_ALIAS;
+    DeviceState dev;
+    int rc = current_device(&dev);
+    if (rc != GBATTN_OK) return rc;
+    int chunks = choose_chunks(B, Hq, Q_pad, KV, dev.num_sms);
+    while (chunks > 1 && (!workspace || workspace_bytes < causal_workspace(chunks, B, Hq, Q_pad, D)))
+        --chunks;
+    const size_t wb = causal_workspace(chunks, B, Hq, Q_pad, D);
+    if (wb > 0 && (overlaps(workspace, wb, q, qb) || overlaps(workspace, wb, k_pages, pb) ||
+                   overlaps(workspace, wb, v_pages, pb) || overlaps(workspace, wb, o, qb) ||
+                   overlaps(workspace, wb, page_table, tb) || overlaps(workspace, wb, lse, lb)))
+        return GBATTN_ERR_ALIAS;
+    const int box = page_size < 64 ? page_size : 64;
+    CUtensorMap kv[2];
+    const uint64_t total_rows = static_cast<uint64_t>(num_phys_pages) * page_size;
+    if (encode_tmap_u8_pages(&kv[0], k_pages, D, Hkv, total_rows, box) != GBATTN_OK ||
+        encode_tmap_u8_pages(&kv[1], v_pages, D, Hkv, total_rows, box) != GBATTN_OK)
+        return GBATTN_ERR_CUDA;
+    // exact scaled values: a power of two in [2^-15, 2^7] folds into the score
+    // scale and the output; an FP16-valued scale uses one FP16 multiply; any
+    // other scale the round-to-odd product (the bridge's rule)
+    auto pow2_in = [](float sv) {
+        int e = 0;
+        const float m = frexpf(sv, &e);
+        return m == 0.5f && e - 1 >= -15 && e - 1 <= 7;
+    };
+    const int mode = pow2_in(k_scale) && pow2_in(v_scale) ? 0
+                     : (is_fp16_value(k_scale) && is_fp16_value(v_scale)) ? 1 : 2;
+    AttnArgs a = base_args(dev, scale * (mode == 0 ? k_scale : 1.0f));
+    a.seq_q = Q_pad;
+    a.seq_k = KV;
+    a.heads_q = B * Hq;
+    a.hq = Hq;
+    a.hkv = Hkv;
+    a.group = Hq / Hkv;
+    a.q_real = Q_real;
+    a.kv_prefix = KV - Q_real;
+    a.n_chunks = chunks;
+    a.o = static_cast<__half*>(o);
+    a.lse = lse;
+    a.page_table = page_table;
+    a.num_phys = num_phys_pages;
+    a.page_size = page_size;
+    a.max_pages = max_pages;
+    a.page_box = box;
+    a.scale_mode = mode;
+    a.ks = k_scale;
+    a.vs = v_scale;
+    a.ks2 = __float2half2_rn(k_scale);
+    a.vs2 = __float2half2_rn(v_scale);
+    a.out_mul = mode == 0 ? v_scale : 1.0f;
+    const long long rows = static_cast<long long>(B) * Hq * Q_pad;
+    if (chunks > 1) {
+        a.part_o = static_cast<float*>(workspace);
+        a.part_lse = a.part_o + static_cast<size_t>(chunks) * rows * D;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    dim3 grid(((Q_pad + BM - 1) / BM) * chunks, B * Hq);
+    rc = launch_attn<256, kCausalPaged>(q, nullptr, nullptr, Q_pad, KV, B * Hq, B * Hkv, grid, a, s,
+                                        nullptr, kv);
+    if (rc != GBATTN_OK || chunks == 1) return rc;
+    const long long threads = rows * 32;
+    attn_merge_kernel<256><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
+        a.part_o, a.part_lse, chunks, rows, Q_pad, Q_real, a.o, lse);
+    count_launches(1);
+    return launch_status();
+}
+
 
 extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
                               const int32_t* pairs, int prefix, const int32_t* cube_valid, void* o,

@@ -16,6 +16,7 @@ done between steps.
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
         [--workload all|dense_video|vsa_video|paged_e4m3|dense_small|causal_small]
         [--decode on|off|only] [--masked on|off|only] [--vsa-full on|off|only]
+        [--paged-fused on|off|only]
 Beside the step, the paged E4M3 decode (4 ragged sequences of 65571..131072
 cached tokens, Hq6 Hkv1 D256, one new token each; attn_paged_decode_fwd) is
 timed on its own and reported as "decode" with its HBM roofline, and dense attention
@@ -572,6 +573,56 @@ def measure_vsa_full(gb, torch, dev, steps, warmup, pk):
             "l2": "256 MB buffer rewritten between calls, outside the timed events"}
 
 
+def measure_paged_fused(gb, torch, dev, steps, warmup, pk):
+    """The paged-E4M3 prefill with the bridge fused into the attention
+    (attn_causal_prefill_paged_fwd) beside the two-pass bridge + FP16 prefill,
+    on the paged_e4m3 workload; both timed on their own with CUDA events."""
+    w = inputs.WORKLOADS["paged_e4m3"]
+    q = inputs.causal_inputs(w["B"], w["Hq"], w["Hkv"], w["Q"], 32, w["D"], w["seed"])[0]
+    kp, vp, table = inputs.paged_e4m3_inputs(w["Hkv"], w["KV"], w["D"], w["seed"], w["page_size"])
+    T = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    dq, dk, dv, dt = T(q), T(kp), T(vp), T(table)
+    o = torch.empty_like(dq)
+    kf = torch.empty((w["Hkv"], w["KV"], w["D"]), dtype=torch.float16, device=dev)
+    vf = torch.empty_like(kf)
+    ws = torch.empty(max(16, gb.attn_causal_prefill_workspace_size(w["B"], w["Hq"], w["Q"], w["KV"],
+                                                                   w["D"])),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fused():
+        gb.attn_causal_prefill_paged_fwd(dq, dk, dv, dt, w["KV"], w["k_scale"], w["v_scale"], o=o,
+                                         workspace=ws)
+
+    def two_pass():
+        gb.e4m3_paged_to_fp16(dk, dv, dt, w["KV"], w["k_scale"], w["v_scale"], k_out=kf, v_out=vf)
+        gb.attn_causal_prefill_fwd(dq, kf[None], vf[None], o=o, workspace=ws)
+
+    res = {}
+    for name, fn in (("fused", fused), ("bridge_then_prefill", two_pass)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    if gb.device_status() != 0:
+        raise RuntimeError("device status flags set during the paged measurement")
+    flops = causal_flops(w["B"], w["Hq"], w["Q"], w["KV"], w["D"])
+    tf = flops / (res["fused"] * 1e-3) / 1e12
+    peak = pk["tc_sust"] or pk["tc"]
+    return {"kernel": "attn_fwd_kernel<256,causal_paged>+merge", "bound": "tensor", "achieved": tf,
+            "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
+            "peak_source": f"{pk['src']} bf16 sustained (fp16 dense rate = bf16 rate)",
+            "ms_fused": res["fused"], "ms_bridge_then_prefill": res["bridge_then_prefill"],
+            "config": {k2: v2 for k2, v2 in w.items() if k2 != "seed"}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -588,6 +639,8 @@ def main():
                     help="dense attention with an additive mask measured beside the step")
     ap.add_argument("--vsa-full", default="on", choices=["on", "off", "only"],
                     help="the full VSA layout (prefix + boundary cubes) measured beside the step")
+    ap.add_argument("--paged-fused", default="on", choices=["on", "off", "only"],
+                    help="the paged prefill with the bridge fused in, beside bridge + prefill")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count of the dense/VSA workloads (profiling runs)")
     args = ap.parse_args()
@@ -618,6 +671,13 @@ def main():
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
 
+    if args.paged_fused == "only":
+        if rank == 0:
+            print(json.dumps(dict(metric="fused paged prefill useful TFLOP/s", impl="ours",
+                                  n_gpus=world, steps=args.steps, warmup=args.warmup,
+                                  **measure_paged_fused(gb, torch, dev, args.steps, args.warmup,
+                                                        peaks()))))
+        return 0
     if args.vsa_full == "only":
         if rank == 0:
             print(json.dumps(dict(metric="full VSA useful TFLOP/s", impl="ours", n_gpus=world,
@@ -794,6 +854,8 @@ def main():
         extra["decode"] = measure_decode(gb, torch, dev, args.steps, args.warmup, pk)
     if args.masked == "on" and args.workload == "all":
         extra["masked"] = measure_masked(gb, torch, dev, args.steps, args.warmup, pk)
+    if args.paged_fused == "on" and args.workload == "all":
+        extra["paged_fused"] = measure_paged_fused(gb, torch, dev, args.steps, args.warmup, pk)
     if args.vsa_full == "on" and args.workload == "all":
         extra["vsa_full"] = measure_vsa_full(gb, torch, dev, args.steps, args.warmup, pk)
 

@@ -132,6 +132,28 @@ int attn_causal_prefill_fwd(const void* q, const void* k, const void* v, void* o
                             float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Causal prefill reading K and V straight from paged E4M3 caches (the bridge fused into the
+ * attention).
+ * Cites: "Integrate FP32 v37 prefill and exact E4M3 bridge", Implementation (exact E4M3 paged
+ * -> FP16 bridge with unit and non-unit scales, FP32 prefill).
+ *   q, o : [B][Hq][Q_pad][D] FP16; k_pages, v_pages : [num_phys_pages][page_size][Hkv][D]
+ *   bytes; page_table : int32 [B][max_pages]; lse optional FP32 [B][Hq][Q_pad].
+ *   Computes exactly what e4m3_paged_to_fp16 followed by attn_causal_prefill_fwd computes: the
+ *   keys and values are RNE_fp16(decode(byte) * scale), formed in shared memory from the
+ *   cached bytes.  Same query positions, padding and split-KV workspace rules as
+ *   attn_causal_prefill_fwd (attn_causal_prefill_workspace_size applies).
+ *   D == 256; page_size a power of two >= 16; KV <= max_pages * page_size, KV % 32 == 0;
+ *   num_phys_pages * page_size < 2^31.  A page-table entry outside [0, num_phys_pages) sets
+ *   GBATTN_DEV_BAD_PAGE (that page reads physical page 0).
+ */
+int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pages, const uint8_t* v_pages,
+                                  const int32_t* page_table, void* o, float* lse, int B, int Hq,
+                                  int Hkv, int Q_pad, int Q_real, int KV, int D,
+                                  int num_phys_pages, int page_size, int max_pages, float k_scale,
+                                  float v_scale, float scale, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
  * Paged FP8 E4M3 ("fn" flavour) -> FP16 bridge.
  * Cites: "Integrate FP32 v37 prefill and exact E4M3 bridge", Purpose and
  * Implementation (exact E4M3 byte conversion, unit and non-unit scales, live
