@@ -143,6 +143,9 @@ static_assert(sizeof(Ctrl) <= 256, "control block");
 struct SparseTiles {
     int list_a[kMaxTopk];
     int list_b[kMaxTopk];
+    uint32_t bits_a[32];            // the two cube sets (at most 1024 cubes)
+    uint32_t bits_b[32];
+    uint8_t mask_hi[kMaxSparseTiles];   // quadrant bits of each tile's second half
     int key0[kMaxSparseTiles];
     int key1[kMaxSparseTiles];
     uint8_t mask[kMaxSparseTiles];
@@ -245,50 +248,75 @@ __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& 
     for (int i = lane; i < na; i += 32) st->list_a[i] = la[i];
     for (int i = lane; i < nb; i += 32) st->list_b[i] = lb[i];
     __syncwarp();
-    if (lane != 0) return;
-    int ia = 0, ib = 0, pa = -1, pb = -1, nu = 0, nt = 0, pend = -1, pend_f = 0;
+    // Set of each list: an entry counts when it lies in range and exceeds every
+    // entry before it (a list that is not strictly ascending is flagged and its
+    // offending entries skipped).
+    if (lane < 32) {
+        st->bits_a[lane] = 0u;
+        st->bits_b[lane] = 0u;
+    }
+    __syncwarp();
     bool bad = false;
-    constexpr int INF = 0x7fffffff;
-    while (true) {
-        int va = INF, vb = INF;
-        while (ia < na) {
-            const int v = st->list_a[ia];
-            if (v > pa && v < a.n_cubes) { va = v; break; }
-            bad = true;
-            ++ia;
+    for (int lst = 0; lst < 2; ++lst) {
+        const int n = lst == 0 ? na : nb;
+        const int* L = lst == 0 ? st->list_a : st->list_b;
+        uint32_t* bits = lst == 0 ? st->bits_a : st->bits_b;
+        int run_max = -1;
+        for (int base = 0; base < n; base += 32) {
+            const int i = base + lane;
+            const int v = i < n ? L[i] : -1;
+            int pre = (v >= 0 && v < a.n_cubes) ? v : -1;   // inclusive prefix max (in range)
+#pragma unroll
+            for (int sh = 1; sh < 32; sh <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, pre, sh);
+                if (lane >= sh) pre = max(pre, y);
+            }
+            int before = __shfl_up_sync(0xffffffffu, pre, 1);
+            if (lane == 0) before = -1;
+            before = max(before, run_max);
+            if (i < n) {
+                if (v > before && v < a.n_cubes) atomicOr(&bits[v >> 5], 1u << (v & 31));
+                else bad = true;
+            }
+            run_max = max(run_max, __shfl_sync(0xffffffffu, pre, 31));
         }
-        while (ib < nb) {
-            const int v = st->list_b[ib];
-            if (v > pb && v < a.n_cubes) { vb = v; break; }
-            bad = true;
-            ++ib;
-        }
-        if (va == INF && vb == INF) break;
-        const int c = min(va, vb);
-        const int f = (va == c ? 1 : 0) | (vb == c ? 2 : 0);
-        if (va == c) { pa = va; ++ia; }
-        if (vb == c) { pb = vb; ++ib; }
-        if (pend < 0) {
-            pend = c;
-            pend_f = f;
+    }
+    __syncwarp();
+    // Union in ascending cube order: word w of the sets belongs to lane w; a warp
+    // prefix sum of the popcounts places every cube; consecutive cubes pair up
+    // into 128-key tiles.
+    const uint32_t ua = st->bits_a[lane], ub = st->bits_b[lane], uu = ua | ub;
+    const int cnt = __popc(uu);
+    int incl = cnt;
+#pragma unroll
+    for (int sh = 1; sh < 32; sh <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, sh);
+        if (lane >= sh) incl += y;
+    }
+    const int nu = __shfl_sync(0xffffffffu, incl, 31);
+    int pos = incl - cnt;
+    for (uint32_t rest = uu; rest; rest &= rest - 1, ++pos) {
+        const int bit = __ffs(rest) - 1;
+        const int c = lane * 32 + bit;
+        const uint32_t f = ((ua >> bit) & 1u) | (((ub >> bit) & 1u) << 1);
+        const int t = pos >> 1;
+        if ((pos & 1) == 0) {
+            st->key0[t] = kbase + c * 64;
+            st->mask[t] = static_cast<uint8_t>((f & 1) | ((f >> 1) << 2));
+            if (pos == nu - 1) {   // odd union: the second half repeats the cube, fully masked
+                st->key1[t] = kbase + c * 64;
+                st->mask_hi[t] = 0;
+            }
         } else {
-            st->key0[nt] = kbase + pend * 64;
-            st->key1[nt] = kbase + c * 64;
-            st->mask[nt] = static_cast<uint8_t>((pend_f & 1) | ((f & 1) << 1) |
-                                                ((pend_f >> 1) << 2) | ((f >> 1) << 3));
-            ++nt;
-            pend = -1;
+            st->key1[t] = kbase + c * 64;
+            st->mask_hi[t] = static_cast<uint8_t>(((f & 1) << 1) | ((f >> 1) << 3));
         }
-        ++nu;
     }
-    if (pend >= 0) {   // odd union: the second half repeats the cube, fully masked
-        st->key0[nt] = kbase + pend * 64;
-        st->key1[nt] = kbase + pend * 64;
-        st->mask[nt] = static_cast<uint8_t>((pend_f & 1) | ((pend_f >> 1) << 2));
-        ++nt;
-    }
-    if (bad) atomicOr(a.status, kDevBadIndex);
-    ctrl->n_tiles = nt;
+    __syncwarp();
+    const int nt = (nu + 1) / 2;
+    for (int t = lane; t < nt; t += 32) st->mask[t] |= st->mask_hi[t];
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, kDevBadIndex);
+    if (lane == 0) ctrl->n_tiles = nt;
 }
 
 // Real keys of every tile half of a video query-cube pair (boundary cubes),

@@ -40,10 +40,21 @@ __global__ void __launch_bounds__(kPoolThreads) vsa_pool_kernel(
     const int groups = D >> 3;   // 8 channels per thread
     const long long gid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     if (gid >= n_bh * n_cubes * groups) return;
-    const long long cube = gid / groups;            // bh * n_cubes + c
-    const int g = static_cast<int>(gid - cube * groups);
-    const long long bh = cube / n_cubes;
-    const int c = static_cast<int>(cube - bh * n_cubes);
+    long long cube, bh;                             // cube = bh * n_cubes + c
+    int g, c;
+    if (gid < (1LL << 31)) {                        // 32-bit index arithmetic when it fits
+        const uint32_t gi = static_cast<uint32_t>(gid), cu = gi / static_cast<uint32_t>(groups);
+        g = static_cast<int>(gi - cu * groups);
+        const uint32_t b32 = cu / static_cast<uint32_t>(n_cubes);
+        c = static_cast<int>(cu - b32 * n_cubes);
+        cube = cu;
+        bh = b32;
+    } else {
+        cube = gid / groups;
+        g = static_cast<int>(gid - cube * groups);
+        bh = cube / n_cubes;
+        c = static_cast<int>(cube - bh * n_cubes);
+    }
     // Real tokens of the cube: its first `count` slots (boundary cubes are padded).
     int count = block;
     if (cube_valid) {
