@@ -828,16 +828,19 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                         if (kh + c >= lim) s[c] = __float_as_uint(-INFINITY);
                 }
             }
-            // row max of the 64 values with four independent chains (short latency)
+            // row max of the 64 values with four independent chains (short latency):
+            // s[0..3] start the chains, s[4..59] in seven steps of eight, s[60..63] last
             float m4[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) m4[k] = __uint_as_float(s[k]);
 #pragma unroll
-            for (int c = 4; c < 64; c += 8) {
+            for (int c = 4; c < 60; c += 8) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     m4[k] = max3f(m4[k], __uint_as_float(s[c + k]), __uint_as_float(s[c + 4 + k]));
             }
+            m4[0] = max3f(m4[0], __uint_as_float(s[60]), __uint_as_float(s[61]));
+            m4[1] = max3f(m4[1], __uint_as_float(s[62]), __uint_as_float(s[63]));
             const float pm = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
             ex->mx[j & 1][half][row] = pm;
             tc_fence_before();   // our S loads are ordered before the partner's P stores
