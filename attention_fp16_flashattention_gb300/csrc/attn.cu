@@ -54,8 +54,18 @@ constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s for draining after an abo
 enum Mode { kDense = 0, kCausal = 1, kSparse = 2, kMasked = 3, kSparseFull = 4, kCausalPaged = 5 };
 __host__ __device__ constexpr bool is_sparse(int mode) { return mode == kSparse || mode == kSparseFull; }
 __host__ __device__ constexpr bool is_causal(int mode) { return mode == kCausal || mode == kCausalPaged; }
-// threads per CTA: the paged mode adds four converter warps (10..13)
-__host__ __device__ constexpr int threads_for(int mode) { return mode == kCausalPaged ? 448 : 320; }
+// The D=128 modes issue their MMAs from two warps: warp 1 the QK groups and
+// warp 10 the PV groups, so that neither stream waits behind the other's
+// barrier waits.  The D=256 causal modes keep one issuing warp: with only two
+// S buffers in tensor memory, waiting for PV_j to finish before QK_{j+2}
+// reuses its buffer would stall the softmax.
+__host__ __device__ constexpr bool dual_issue(int mode) { return !(mode == kCausal || mode == kCausalPaged); }
+constexpr int kPvWarp = 10;
+// threads per CTA: the PV issuer adds a warp (10); the paged mode adds four
+// converter warps (10..13)
+__host__ __device__ constexpr int threads_for(int mode) {
+    return mode == kCausalPaged ? 448 : (dual_issue(mode) ? 352 : 320);
+}
 constexpr int kConvThreads = 128;
 
 struct AttnArgs {
@@ -123,6 +133,7 @@ struct Ctrl {
                            // PV_{j-NSB}, so once S_j is visible the previous phase
                            // of every barrier awaited below has completed.
     uint64_t drain;
+    uint64_t drain_pv;     // the PV issuer's own drain after an abort
     uint64_t xchg[4];      // per row quarter: the two half-row threads exchange values
     uint64_t raw_full[2];  // paged: E4M3 bytes of a slot landed (converters may read)
     uint64_t conv_read[2]; // paged: every converter holds its bytes (the slot may be overwritten)
@@ -435,6 +446,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         if (MODE == kMasked)
             for (int i = 0; i < 16; ++i) mbar_init(&mbar[i], 1);
         mbar_init(&ctrl->drain, 1);
+        mbar_init(&ctrl->drain_pv, 1);
         ctrl->abort = 0;
         mbar_init_fence();
     }
@@ -472,6 +484,31 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             k0 = (tile0 + t) * BN;
             k1 = k0 + 64;
         }
+    };
+
+    // S_t = Q K_t^T into S buffer buf; O += P_j V_j with P_j read from S buffer buf.
+    auto issue_qk = [&](int slot, int buf) {
+        const uint32_t qa = smem_addr(sQ);
+        const uint32_t ka = smem_addr(sKV + slot * C::SLOT_BYTES);
+#pragma unroll
+        for (int k16 = 0; k16 < D / 16; ++k16) {
+            const uint32_t off = (k16 >> 2) * C::CHUNK + (k16 & 3) * 32;
+            mma_ss(tmem + buf * 128, sdesc_sw128(qa + off, 16, 1024),
+                   sdesc_sw128(ka + off, 16, 1024), C::IDESC_QK, k16 > 0 ? 1u : 0u);
+        }
+    };
+    auto issue_pv = [&](int slot, int buf, bool acc) {
+        const uint32_t va = smem_addr(sKV + slot * C::SLOT_BYTES);
+#pragma unroll
+        for (int k16 = 0; k16 < BN / 16; ++k16)
+            mma_ts(tmem + C::T_O, tmem + buf * 128 + k16 * 8,
+                   sdesc_sw128(va + k16 * 2048, C::CHUNK, 1024), C::IDESC_PV,
+                   (acc || k16 > 0) ? 1u : 0u);
+    };
+    // Ring positions (the TMA warp's load order, see ring_item) of K_t and V_j.
+    auto pos_k = [&](int t) { return t < C::NSB ? t : C::NSB + 2 * (t - C::NSB) + 1; };
+    auto pos_v = [&](int j) {
+        return min(n_tiles, C::NSB) + j + min(j, max(0, n_tiles - C::NSB));
     };
 
     if (warp == 0) {
@@ -578,72 +615,117 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         // each group of MMAs and its commits)
         if (n_tiles > 0) {
             bool ok = wait_warp(&ctrl->q_full, 0, w);
-            const uint32_t qa = smem_addr(sQ);
-            auto issue_qk = [&](int slot, int buf) {
-                const uint32_t ka = smem_addr(sKV + slot * C::SLOT_BYTES);
-#pragma unroll
-                for (int k16 = 0; k16 < D / 16; ++k16) {
-                    const uint32_t off = (k16 >> 2) * C::CHUNK + (k16 & 3) * 32;
-                    mma_ss(tmem + buf * 128, sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(ka + off, 16, 1024), C::IDESC_QK, k16 > 0 ? 1u : 0u);
+            if (dual_issue(MODE)) {
+                // QK only (warp 10 issues PV).  QK_t overwrites the S buffer that
+                // PV_{t-NSB} read P_{t-NSB} from, so it waits for that PV to finish.
+                // A parity wait on a slot is unambiguous only if the slot's previous
+                // item is known to have landed: here it is either an earlier K (this
+                // warp waited for it) or a V_i that precedes K_t in the ring, so
+                // i <= t-NSB (K_t follows V_{t-NSB}) and PV_i finished with PV_{t-NSB}.
+                for (int t = 0; ok && t < n_tiles; ++t) {
+                    const int pos = pos_k(t);
+                    const int slot = pos % C::NS;
+                    const int buf = t % C::NSB;
+                    if (t >= C::NSB) ok = wait_warp(&ctrl->pv_done[buf], ((t - C::NSB) / C::NSB) & 1, w);
+                    ok = ok && wait_warp(&ctrl->full[slot], (pos / C::NS) & 1, w);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_qk(slot, buf);
+                        mma_commit(&ctrl->s_full[buf]);
+                        mma_commit(&ctrl->empty[slot]);
+                    }
+                    __syncwarp();
                 }
-            };
-            auto issue_pv = [&](int slot, int buf, bool acc) {
-                const uint32_t va = smem_addr(sKV + slot * C::SLOT_BYTES);
-#pragma unroll
-                for (int k16 = 0; k16 < BN / 16; ++k16)
-                    mma_ts(tmem + C::T_O, tmem + buf * 128 + k16 * 8,
-                           sdesc_sw128(va + k16 * 2048, C::CHUNK, 1024), C::IDESC_PV,
-                           (acc || k16 > 0) ? 1u : 0u);
-            };
-            int it = 0;
-            // S_0 .. S_{L-1} up front, then per tile: PV_j, and QK_{j+L} into the
-            // buffer P_j has just been read from (in order on the tensor pipe).
-            for (int t = 0; ok && t < min(n_tiles, C::NSB); ++t) {
-                const int slot = it % C::NS;
-                ok = wait_warp(&ctrl->full[slot], (it / C::NS) & 1, w);
-                if (!ok) break;
-                tc_fence_after();
-                if (elect_one()) {
-                    issue_qk(slot, t);
-                    mma_commit(&ctrl->s_full[t]);
-                    mma_commit(&ctrl->empty[slot]);
+            } else {
+                int it = 0;
+                // S_0 .. S_{L-1} up front, then per tile: PV_j, and QK_{j+L} into the
+                // buffer P_j has just been read from (in order on the tensor pipe).
+                for (int t = 0; ok && t < min(n_tiles, C::NSB); ++t) {
+                    const int slot = it % C::NS;
+                    ok = wait_warp(&ctrl->full[slot], (it / C::NS) & 1, w);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_qk(slot, t);
+                        mma_commit(&ctrl->s_full[t]);
+                        mma_commit(&ctrl->empty[slot]);
+                    }
+                    __syncwarp();
+                    ++it;
                 }
-                __syncwarp();
-                ++it;
-            }
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int buf = j % C::NSB;
-                const int vslot = it % C::NS;
-                ok = wait_warp(&ctrl->p_full[buf], (j / C::NSB) & 1, w) &&
-                     wait_warp(&ctrl->full[vslot], (it / C::NS) & 1, w);
-                if (!ok) break;
-                ++it;
-                tc_fence_after();
-                if (elect_one()) {
-                    issue_pv(vslot, buf, j > 0);
-                    mma_commit(&ctrl->empty[vslot]);
-                    mma_commit(&ctrl->pv_done[buf]);
-                }
-                __syncwarp();
-                if (j + C::NSB < n_tiles) {
-                    const int kslot = it % C::NS;
-                    ok = wait_warp(&ctrl->full[kslot], (it / C::NS) & 1, w);
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    const int buf = j % C::NSB;
+                    const int vslot = it % C::NS;
+                    ok = wait_warp(&ctrl->p_full[buf], (j / C::NSB) & 1, w) &&
+                         wait_warp(&ctrl->full[vslot], (it / C::NS) & 1, w);
                     if (!ok) break;
                     ++it;
                     tc_fence_after();
                     if (elect_one()) {
-                        issue_qk(kslot, buf);
-                        mma_commit(&ctrl->s_full[buf]);
-                        mma_commit(&ctrl->empty[kslot]);
+                        issue_pv(vslot, buf, j > 0);
+                        mma_commit(&ctrl->empty[vslot]);
+                        mma_commit(&ctrl->pv_done[buf]);
                     }
                     __syncwarp();
+                    if (j + C::NSB < n_tiles) {
+                        const int kslot = it % C::NS;
+                        ok = wait_warp(&ctrl->full[kslot], (it / C::NS) & 1, w);
+                        if (!ok) break;
+                        ++it;
+                        tc_fence_after();
+                        if (elect_one()) {
+                            issue_qk(kslot, buf);
+                            mma_commit(&ctrl->s_full[buf]);
+                            mma_commit(&ctrl->empty[kslot]);
+                        }
+                        __syncwarp();
+                    }
                 }
             }
             if (!ok) {   // wait for issued MMAs before tensor memory is freed
                 if (elect_one()) mma_commit(&ctrl->drain);
                 __syncwarp();
                 if (lane == 0) drain_wait(&ctrl->drain, 0);
+            }
+        }
+    } else if (dual_issue(MODE) && warp == kPvWarp) {
+        // ================= PV issuer (D=128 modes; whole warp waits, one elected
+        // lane issues).  PV_j waits for P_j (the softmax is done with S_j, so
+        // every QK_t with t <= j has finished) and for V_j in the ring.  A parity
+        // wait on a slot is unambiguous only if the slot's previous item is known
+        // to have landed: an earlier V (this warp waited for it) or a K_t with
+        // t <= j is; a K_t with t > j (a 3-slot ring: t = j+1) is first awaited
+        // through its QK.  That QK wait is itself unambiguous: K_t precedes V_j in
+        // the ring, so t <= j+NSB-1 and QK_{t-NSB} finished before S_j was read.
+        if (n_tiles > 0) {
+            bool ok = true;
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int pos = pos_v(j);
+                const int slot = pos % C::NS;
+                const int buf = j % C::NSB;
+                ok = wait_warp(&ctrl->p_full[buf], (j / C::NSB) & 1, w);
+                if (ok && pos >= C::NS) {
+                    int pt;
+                    bool pv;
+                    ring_item(pos - C::NS, n_tiles, C::NSB, pt, pv);
+                    if (!pv && pt > j)
+                        ok = wait_warp(&ctrl->s_full[pt % C::NSB], (pt / C::NSB) & 1, w);
+                }
+                ok = ok && wait_warp(&ctrl->full[slot], (pos / C::NS) & 1, w);
+                if (!ok) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_pv(slot, buf, j > 0);
+                    mma_commit(&ctrl->empty[slot]);
+                    mma_commit(&ctrl->pv_done[buf]);
+                }
+                __syncwarp();
+            }
+            if (!ok) {   // wait for issued MMAs before tensor memory is freed
+                if (elect_one()) mma_commit(&ctrl->drain_pv);
+                __syncwarp();
+                if (lane == 0) drain_wait(&ctrl->drain_pv, 0);
             }
         }
     } else if (MODE == kCausalPaged && warp >= 10) {
