@@ -9,7 +9,7 @@
 // Work split (balanced whatever the lengths): a stream is one (sequence, KV
 // head, group of <= 8 query rows); its work is ceil(kv_len / 16) tiles of 16
 // cached tokens.  The streams' tiles are laid end to end and every warp of a
-// persistent grid (8 warps per SM) takes an equal contiguous range of them.
+// persistent grid (4 warps per SM) takes an equal contiguous range of them.
 //   * Each warp runs its own pipeline: a ring of 16-token stages filled by TMA
 //     (128-byte swizzle, one box per 128-byte half of the head width for K and
 //     V) issued by one elected lane, with the page-table entries of the next 32
@@ -39,7 +39,10 @@ namespace gbattn {
 namespace {
 
 constexpr int kTile = 16;        // tokens per tile (one MMA M block)
-constexpr int kWarps = 8;        // warps per CTA, each with its own pipeline
+// Warps per CTA, each with its own pipeline.  Four deep rings stream as fast as
+// eight shallower ones (the same bytes in flight) and halve the partial records
+// the merge reads; three or two warps cannot keep up with the conversion work.
+constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRows = 8;         // query rows per stream (MMA N)
 constexpr int kMaxSeqs = 4096;   // sequences per launch (prefix table in shared memory)
@@ -56,7 +59,7 @@ enum ScaleMode { kScaleFolded = 0, kScaleHalf = 1, kScaleGeneral = 2 };
 template <int D>
 struct Cfg {
     static constexpr int kHalves = D / 128;
-    static constexpr int kStages = D == 256 ? 3 : 6;
+    static constexpr int kStages = D == 256 ? 4 : 8;          // 32 KB in flight per warp
     static constexpr int kBox = kTile * 128;                     // one TMA box
     static constexpr int kStageBytes = 2 * kHalves * kBox;       // K halves, then V halves
     static constexpr int kSteps = D / 16;                        // QK k-steps, PV d-blocks

@@ -30,6 +30,7 @@ maximum over ranks and the value counts the work of all ranks.
 """
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -173,12 +174,16 @@ def host_inputs(name):
 
 
 # ------------------------------------------------------------------ clocks
-CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
 class ClockSampler:
+    """nvidia-smi samples every 50 ms, started before the warm-up so that it is
+    running when the timed region begins; only samples stamped inside the
+    window given to stop() are summarised."""
+
     def __init__(self, gpu_index):
         self.proc = None
         self.gpu = gpu_index
@@ -190,12 +195,12 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -207,13 +212,18 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
-                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+                when = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append(dict(t=when, sm=float(parts[2]), max=float(parts[3]),
+                                 power=float(parts[4]), hw=parts[6], hwt=parts[7], swt=parts[8],
+                                 swp=parts[9]))
             except ValueError:
                 continue
+        if window is not None:
+            inside = [r for r in rows if window[0] <= r["t"] <= window[1]]
+            rows = inside or rows
         if not rows:
             return None
         loaded = [r for r in rows if r["power"] > 200.0] or rows
@@ -708,6 +718,8 @@ def main():
         for _, _, fn in calls:
             fn()
 
+    clocks = ClockSampler(physical_gpu_index(local))
+    clocks.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -718,11 +730,10 @@ def main():
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in calls] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(physical_gpu_index(local))
     barrier(world, dev)
     torch.cuda.synchronize()
-    clocks.start()
     launches0 = gb.launch_count()
+    t_begin = datetime.datetime.now()
     start.record(stream)
     for s in range(args.steps):
         for c, (_, _, fn) in enumerate(calls):
@@ -731,8 +742,9 @@ def main():
             ev[s][c][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
+    t_end = datetime.datetime.now()
     launches = (gb.launch_count() - launches0) // args.steps
-    clock_info = clocks.stop()
+    clock_info = clocks.stop((t_begin, t_end))
     barrier(world, dev)
     local_ms = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(local_ms, world, dev)

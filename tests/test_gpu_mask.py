@@ -52,7 +52,10 @@ def run(gb, q, k, v, mask, scale):
     (2, 3, 300, 904, "per_head"),
     (2, 2, 130, 136, "per_batch_head"),
     (1, 1, 64, 8, "shared"),
-    (1, 2, 1000, 1000, "shared")])
+    (1, 2, 1000, 1000, "shared"),
+    (1, 2, 200, 384, "shared"),           # 3 key tiles: all S buffers used once
+    (2, 1, 128, 640, "per_batch_head"),   # 5 key tiles: the 3-slot ring wraps
+    (1, 2, 256, 2056, "shared")])         # 17 key tiles with a ragged last one
 def test_masked_parity(gb, B, H, Sq, Skv, mshape):
     q, k, v = inputs.dense_inputs(B, H, Sq, 128, seed=80 + Sq, skv=Skv)
     shape = {"shared": (Sq, Skv), "per_head": (1, H, Sq, Skv),
