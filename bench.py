@@ -216,13 +216,16 @@ class ClockSampler:
                 continue
             try:
                 when = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                when = None   # unknown stamp format: the sample is kept
+            try:
                 rows.append(dict(t=when, sm=float(parts[2]), max=float(parts[3]),
                                  power=float(parts[4]), hw=parts[6], hwt=parts[7], swt=parts[8],
                                  swp=parts[9]))
             except ValueError:
                 continue
         if window is not None:
-            inside = [r for r in rows if window[0] <= r["t"] <= window[1]]
+            inside = [r for r in rows if r["t"] is None or window[0] <= r["t"] <= window[1]]
             rows = inside or rows
         if not rows:
             return None
