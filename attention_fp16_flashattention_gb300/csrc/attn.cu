@@ -810,6 +810,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         const long long row_g = rb < 0 ? static_cast<long long>(a.seq_q) : static_cast<long long>(rb) + (row & 63);
         const int row_half = row >> 6;
         uint64_t* xbar = &ctrl->xchg[quarter];
+        bool pad_row = false;   // a padding query slot of a boundary cube, read before the loop
+        if (MODE == kSparseFull && a.cube_valid && row_g >= a.prefix && row_g < a.seq_q) {
+            const int vr = static_cast<int>(row_g - a.prefix);
+            pad_row = (vr & 63) >= cube_count(a, vr >> 6);
+        }
         int lim = a.seq_k;   // keys >= lim are invisible to this row
         if (is_causal(MODE))
             lim = static_cast<int>(min(static_cast<long long>(a.seq_k), a.kv_prefix + row_g + 1));
@@ -883,24 +888,26 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                     }
                 }
                 if (j + 2 < n_tiles) mask_issue(j + 2);   // into the slot just read
+                // keys past the end and rows past the end hidden through one column limit
                 const int kh = half ? k1 : k0;
-                if (kh + 64 > a.seq_k || row_g >= a.seq_q) {
+                const int lim_c = row_g >= a.seq_q ? 0 : a.seq_k - kh;
+                if (lim_c < 64) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
-                        if (kh + c >= a.seq_k || row_g >= a.seq_q) s[c] = __float_as_uint(-INFINITY);
+                        if (c >= lim_c) s[c] = __float_as_uint(-INFINITY);
                 }
             } else if (is_sparse(MODE)) {
+                // One column limit per tile half: a quadrant hidden from this row's cube
+                // hides all 64 keys, a boundary cube its padding keys.  (Two separate
+                // masking loops here had cost the full-layout kernel 45 registers and
+                // a quarter of its speed.)
                 const uint32_t mk = st->mask[j];
-                if (!((mk >> (row_half * 2 + half)) & 1u)) {
+                int lim_c = ((mk >> (row_half * 2 + half)) & 1u) ? 64 : 0;
+                if (MODE == kSparseFull && a.cube_valid && lim_c) lim_c = half ? st->kv1[j] : st->kv0[j];
+                if (lim_c < 64) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = __float_as_uint(-INFINITY);
-                } else if (MODE == kSparseFull && a.cube_valid) {   // padding keys of a boundary cube
-                    const int kvl = half ? st->kv1[j] : st->kv0[j];
-                    if (kvl < 64) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c >= kvl) s[c] = __float_as_uint(-INFINITY);
-                    }
+                    for (int c = 0; c < 64; ++c)
+                        if (c >= lim_c) s[c] = __float_as_uint(-INFINITY);
                 }
             } else {
                 const int kh = half ? k1 : k0;
@@ -1007,11 +1014,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         }
         if (ok) {
             const bool row_ok = row_g < a.seq_q;
-            bool zero_row = is_causal(MODE) && row_g >= a.q_real;
-            if (MODE == kSparseFull && row_g >= a.prefix && row_g < a.seq_q) {   // padding query slot
-                const int vr = static_cast<int>(row_g - a.prefix);
-                zero_row = (vr & 63) >= cube_count(a, vr >> 6);
-            }
+            const bool zero_row = (is_causal(MODE) && row_g >= a.q_real) || pad_row;
             const float inv_l = (l > 0.0f && !zero_row) ? (MODE == kCausalPaged ? a.out_mul : 1.0f) / l : 0.0f;
             const float lse2 = (l > 0.0f && !zero_row) ? m_run + __log2f(l) : -INFINITY;
             const bool partial = is_causal(MODE) && a.n_chunks > 1;
