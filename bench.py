@@ -37,6 +37,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -184,11 +185,11 @@ class ClockSampler:
     running when the timed region begins; only samples stamped inside the
     window given to stop() are summarised."""
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, path=None):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv") \
-            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/gbattn_clocks_{os.getpid()}.csv"
+        self.path = path or os.path.join(tempfile.gettempdir(),
+                                         f"gbattn_clocks_{os.getpid()}_{gpu_index}.csv")
 
     def start(self):
         try:
@@ -209,36 +210,44 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                when = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
-            except ValueError:
-                when = None   # unknown stamp format: the sample is kept
-            try:
-                rows.append(dict(t=when, sm=float(parts[2]), max=float(parts[3]),
-                                 power=float(parts[4]), hw=parts[6], hwt=parts[7], swt=parts[8],
-                                 swp=parts[9]))
-            except ValueError:
-                continue
-        if window is not None:
-            inside = [r for r in rows if r["t"] is None or window[0] <= r["t"] <= window[1]]
-            rows = inside or rows
-        if not rows:
-            return None
-        loaded = [r for r in rows if r["power"] > 200.0] or rows
-        reasons = set()
-        for r in loaded:
-            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
-                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
-                if r[key].lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
-                "sm_max_mhz": max(r["max"] for r in loaded),
-                "samples": len(loaded), "reasons": sorted(reasons)}
+        with open(self.path) as fh:
+            return summarize_clocks(fh.read().splitlines(), window)
+
+
+def summarize_clocks(lines, window=None):
+    """Median SM clock, maximum clock and active throttle reasons of nvidia-smi CSV
+    lines (CLOCK_QUERY order), over the samples stamped inside `window` (all if
+    none is) and drawing more than 200 W (all if none does)."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            when = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+        except ValueError:
+            when = None   # unknown stamp format: the sample is kept
+        try:
+            rows.append(dict(t=when, sm=float(parts[2]), max=float(parts[3]),
+                             power=float(parts[4]), hw=parts[6], hwt=parts[7], swt=parts[8],
+                             swp=parts[9]))
+        except ValueError:
+            continue
+    if window is not None:
+        inside = [r for r in rows if r["t"] is None or window[0] <= r["t"] <= window[1]]
+        rows = inside or rows
+    if not rows:
+        return None
+    loaded = [r for r in rows if r["power"] > 200.0] or rows
+    reasons = set()
+    for r in loaded:
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+            if r[key].lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+            "sm_max_mhz": max(r["max"] for r in loaded),
+            "samples": len(loaded), "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ helpers
@@ -646,6 +655,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=20.0)
+    ap.add_argument("--clock-log", default=None,
+                    help="file for the raw nvidia-smi samples of the timed region (default: a temp file)")
     ap.add_argument("--decode", default="on", choices=["on", "off", "only"],
                     help="paged E4M3 decode measured beside the step (only: print just that)")
     ap.add_argument("--masked", default="on", choices=["on", "off", "only"],
@@ -721,7 +732,7 @@ def main():
         for _, _, fn in calls:
             fn()
 
-    clocks = ClockSampler(physical_gpu_index(local))
+    clocks = ClockSampler(physical_gpu_index(local), args.clock_log)
     clocks.start()
     for _ in range(args.warmup):
         step()

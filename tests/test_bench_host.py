@@ -57,15 +57,7 @@ def test_max_over_ranks_gloo_two_ranks():
     assert out == {0: 15.0, 1: 15.0}
 
 
-class _FakeSmi:
-    def terminate(self):
-        pass
-
-    def wait(self, timeout=None):
-        return 0
-
-
-def test_clock_samples_are_cut_to_the_timed_window(tmp_path):
+def test_clock_samples_are_cut_to_the_timed_window():
     """Only samples stamped inside the timed window count; idle samples (low power) drop."""
     import datetime
 
@@ -76,20 +68,15 @@ def test_clock_samples_are_cut_to_the_timed_window(tmp_path):
         "2026/12/02 10:00:00.150, 0, 2010, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active",
         "2026/12/02 10:00:00.200, 0, 1100, 2070, 900.0, 0x8, Active, Not Active, Not Active, Not Active",
     ]
-    s = bench.ClockSampler(0)
-    s.path = str(tmp_path / "clocks.csv")
-    s.fh = open(s.path, "w")
-    s.fh.write("\n".join(rows) + "\n")
-    s.fh.flush()
-    s.proc = _FakeSmi()
     t0 = datetime.datetime(2026, 12, 2, 10, 0, 0, 40000)
     t1 = datetime.datetime(2026, 12, 2, 10, 0, 0, 160000)
-    info = s.stop((t0, t1))
-    assert info == {"sm_mhz": 1960.0, "sm_max_mhz": 2070.0, "samples": 3,
-                    "reasons": ["sw_power_cap"]}
-    # the hardware slowdown outside the window is not reported; inside it would be
-    s2 = bench.ClockSampler(0)
-    s2.path, s2.proc = s.path, _FakeSmi()
-    s2.fh = open(s2.path, "a")
-    info2 = s2.stop((t0, datetime.datetime(2026, 12, 2, 10, 0, 1)))
-    assert "hw_slowdown" in info2["reasons"] and info2["samples"] == 4
+    assert bench.summarize_clocks(rows, (t0, t1)) == {
+        "sm_mhz": 1960.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+    # the hardware slowdown outside the window is not reported; inside it is
+    wide = bench.summarize_clocks(rows, (t0, datetime.datetime(2026, 12, 2, 10, 0, 1)))
+    assert "hw_slowdown" in wide["reasons"] and wide["samples"] == 4
+    # a window that holds no sample falls back to every sample; an unknown stamp is kept
+    late = datetime.datetime(2026, 12, 2, 11, 0, 0)
+    assert bench.summarize_clocks(rows, (late, late))["samples"] == 4
+    odd = ["12:00:00, 0, 1500, 2070, 800.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    assert bench.summarize_clocks(odd, (t0, t1))["sm_mhz"] == 1500.0
