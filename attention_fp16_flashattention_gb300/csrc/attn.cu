@@ -383,8 +383,15 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     // ---- work decode
     int q_row0, kv_bh, n_tiles = 0, tile0 = 0, chunk = 0;
     if (is_causal(MODE)) {
-        const int qt = blockIdx.x / a.n_chunks;
-        chunk = blockIdx.x - qt * a.n_chunks;
+        // Launch order: heads fastest, then query tiles, then key chunks, so that the
+        // CTAs in flight walk one key window together (and the query heads that share
+        // a KV head read each K/V tile from L2 at about the same time).
+        const long long id = static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x;
+        const int n_qt = static_cast<int>(gridDim.x) / a.n_chunks;
+        bh = static_cast<int>(id % gridDim.y);
+        const long long r = id / gridDim.y;
+        const int qt = static_cast<int>(r % n_qt);
+        chunk = static_cast<int>(r / n_qt);
         q_row0 = qt * BM;
         const int b = bh / a.hq, h = bh - b * a.hq;
         kv_bh = b * a.hkv + h / a.group;
