@@ -10,8 +10,8 @@
 //     FP32 rounding after every addition, then divides by the count (correctly
 //     rounded).  Video tokens start after `prefix` prefix tokens, which take no
 //     part.  HBM-bound: Q and K are read once with 16-byte loads.
-//  2. vsa_score_topk_kernel: 32 query cubes per CTA against all key cubes,
-//     register-tiled (2 queries x 4 keys per thread) with operands staged
+//  2. vsa_score_topk_kernel: 16 query cubes per CTA against all key cubes,
+//     register-tiled (1 query x 4 keys per thread) with operands staged
 //     d-major in shared memory.  Every score is an FP32 sum over d = 0..D-1, in
 //     order, of FP32 products (no fused multiply-add, so both the product and the
 //     sum are rounded).  The k-th largest score of a row is found with a 32-step
@@ -142,23 +142,35 @@ __global__ void __launch_bounds__(kSelThreads) vsa_score_topk_kernel(
         }
     }
     const int ty = tid >> 4, tx = tid & 15;
+    // Key staging: lane = key (32 keys per warp), each lane one 32-byte sector of
+    // 8 consecutive dims per item, so the d-major stores of a warp fill 32
+    // consecutive words of one row (no bank conflicts) and every sector loaded
+    // is used whole.  Warp w takes keys 32*(w&1) .. +31 and dim groups (w>>1) + 4r.
+    const int sk_key = lane + 32 * (warp & 1), sk_g0 = warp >> 1;
+    constexpr int kItems = kSelKB * kSelD / 8 / kSelThreads;   // 4
     for (int kb = 0; kb < NC; kb += kSelKB) {
-        // Stage 64 key means d-major: eight 16-byte loads in flight per thread.
-        float4 v[kSelKB * kSelD / 4 / kSelThreads];
+        float4 v[2 * kItems];
+        const bool live = kb + sk_key < NC;
+        const float* krow = kbase + static_cast<long long>(kb + sk_key) * kSelD;
 #pragma unroll
-        for (int r = 0; r < kSelKB * kSelD / 4 / kSelThreads; ++r) {
-            const int i = tid + r * kSelThreads, k = i / (kSelD / 4), d4 = i % (kSelD / 4);
-            v[r] = (kb + k < NC) ? *reinterpret_cast<const float4*>(kbase + static_cast<long long>(kb + k) * kSelD + 4 * d4)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < kItems; ++r) {
+            const int g = sk_g0 + 4 * r;   // dims 8g .. 8g+7
+            v[2 * r] = live ? *reinterpret_cast<const float4*>(krow + 8 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[2 * r + 1] = live ? *reinterpret_cast<const float4*>(krow + 8 * g + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncthreads();
 #pragma unroll
-        for (int r = 0; r < kSelKB * kSelD / 4 / kSelThreads; ++r) {
-            const int i = tid + r * kSelThreads, k = i / (kSelD / 4), d4 = i % (kSelD / 4);
-            sk[(4 * d4 + 0) * SK + k] = v[r].x;
-            sk[(4 * d4 + 1) * SK + k] = v[r].y;
-            sk[(4 * d4 + 2) * SK + k] = v[r].z;
-            sk[(4 * d4 + 3) * SK + k] = v[r].w;
+        for (int r = 0; r < kItems; ++r) {
+            const int g = sk_g0 + 4 * r;
+            float* col = sk + (8 * g) * SK + sk_key;
+            col[0 * SK] = v[2 * r].x;
+            col[1 * SK] = v[2 * r].y;
+            col[2 * SK] = v[2 * r].z;
+            col[3 * SK] = v[2 * r].w;
+            col[4 * SK] = v[2 * r + 1].x;
+            col[5 * SK] = v[2 * r + 1].y;
+            col[6 * SK] = v[2 * r + 1].z;
+            col[7 * SK] = v[2 * r + 1].w;
         }
         __syncthreads();
         float acc[4];
