@@ -125,7 +125,8 @@ def set_wait_limit_ns(ns):
 
 
 def test_inject_fault(mode):
-    """Test hook: 1 makes attention launches skip their query load (timeout path), 0 restores."""
+    """Test hook: 1 makes attention launches skip their query load, 2 stops their K/V loads
+    after two rounds of the ring (timeout paths, mid-stream for 2); 0 restores."""
     _check("gbattn_test_inject_fault", load().gbattn_test_inject_fault(int(mode)))
 
 

@@ -102,7 +102,7 @@ struct AttnArgs {
     long long mask_sh;  // masked: elements between head slices (0 = shared)
     uint32_t* status;
     uint64_t wait_limit;
-    int fault;          // test hook: 1 = the TMA warp never loads Q (exercises the timeout path)
+    int fault;          // test hook: 1 = the TMA warp never loads Q; 2 = it stops after 2*NS K/V items
 };
 
 template <int D, int MODE>
@@ -562,6 +562,10 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             };
             int prow_next = page_row(0);
             for (int it = 0; it < 2 * n_tiles; ++it) {
+                if (a.fault == 2 && it >= 2 * C::NS) {   // test hook: stop mid-stream, drain, leave
+                    ok = false;
+                    break;
+                }
                 const int slot = it % C::NS;
                 const int prow_cur = prow_next;
                 if (MODE == kCausalPaged) prow_next = page_row(it + 1);
@@ -1221,7 +1225,7 @@ int sm_count_or_default() {
 using namespace gbattn;
 
 extern "C" int gbattn_test_inject_fault(int mode) {
-    if (mode < 0 || mode > 1) return GBATTN_ERR_SHAPE;
+    if (mode < 0 || mode > 2) return GBATTN_ERR_SHAPE;
     g_fault_mode = mode;
     return GBATTN_OK;
 }

@@ -91,9 +91,12 @@ uint64_t gbattn_launch_count(void);
  * exception-safe operator lifetimes and explicit rollback: "Integrate FP32 v37
  * prefill and exact E4M3 bridge", Purpose).  mode 1 makes every later
  * attention launch skip its query-tile load, so its first pipeline wait runs
- * out after gbattn_set_wait_limit_ns(); the kernel then records
- * GBATTN_DEV_WAIT_TIMEOUT, frees its tensor memory and returns.  mode 0
- * (default) restores normal operation.  Returns GBATTN_OK or GBATTN_ERR_SHAPE. */
+ * out after gbattn_set_wait_limit_ns(); mode 2 makes the load warp stop after
+ * the first two rounds of its K/V ring (waiting for the copies it issued), so
+ * the waits run out mid-stream with tensor-core work in flight.  Either way the
+ * kernel records GBATTN_DEV_WAIT_TIMEOUT, lets its copies and MMAs finish, frees
+ * its tensor memory and returns (outputs are then undefined).  mode 0 (default)
+ * restores normal operation.  Returns GBATTN_OK or GBATTN_ERR_SHAPE. */
 int gbattn_test_inject_fault(int mode);
 
 /*

@@ -54,6 +54,13 @@ def test_status_strings_and_version(lib):
     assert lib.gbattn_status_string(99) == b"unknown status"
 
 
+def test_fault_hook_modes(lib):
+    """The test hook takes modes 0..2 only (host-side state; nothing is launched)."""
+    for mode in (1, 2, 0):
+        assert lib.gbattn_test_inject_fault(mode) == 0
+    assert lib.gbattn_test_inject_fault(3) == 2 and lib.gbattn_test_inject_fault(-1) == 2
+
+
 P = ctypes.c_void_p(0x10000)      # aligned fake device addresses: never dereferenced
 P2 = ctypes.c_void_p(0x20000000)
 P3 = ctypes.c_void_p(0x40000000)
