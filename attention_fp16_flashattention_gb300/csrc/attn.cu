@@ -10,20 +10,25 @@
 // two-key-half blocks with a 4-bit quadrant mask of block_lists.py in the
 // FastVideo compare view).
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads at D=128, 320 at D=256, 448 with the paged converters):
 //   warp 0      TMA producer: Q once, then K and V tiles through an NS-slot ring
-//               in the order the MMA warp consumes them (K0, K1, V0, K2, V1, ...).
-//   warp 1      allocates tensor memory; one lane issues every tcgen05.mma:
-//               S = Q K_j^T (SMEM x SMEM), then O += P_j V_j (P from TMEM).
-//               S_{j+1} is computed while the softmax warps work on tile j.
+//               in the order the MMAs consume them (K0 .. K_{NSB-1}, V0, K_NSB,
+//               V1, ...).
+//   warp 1      allocates tensor memory and issues S = Q K_t^T (SMEM x SMEM);
+//               at D=128 only these, at D=256 also every PV, in order.
+//   warp 10     (D=128) issues O += P_j V_j (P from TMEM), so that neither MMA
+//               stream waits behind the other's barrier waits.  Each issuing
+//               warp is converged and one elected lane issues each group.
 //   warps 2..9  softmax: two threads per query row (TMEM lane = row), one per
 //               64-key half of the tile; they exchange the partial row max;
 //               exp2 with packed FP32 pairs, row sum, P -> FP16 into TMEM; lazy
 //               O rescaling (only when the running max grows by more than 2^8),
 //               each thread on its half of O; epilogue O / l.
+//   warps 10..13 (paged causal) convert E4M3 page rows to FP16 in shared memory.
 // Tensor memory (512 columns): NSB S buffers of 128 FP32 columns (3 for D=128,
 // 2 for D=256); P_j overwrites the first 64 columns of its S buffer as FP16
-// pairs; O [NSB*128, NSB*128 + D) FP32.  The MMA warp keeps QK NSB tiles ahead.
+// pairs; O [NSB*128, NSB*128 + D) FP32.  QK runs up to NSB tiles ahead; with
+// two issuing warps QK_t waits for PV_{t-NSB} (which read P from its buffer).
 //
 // Every wait is bounded in time (see WaitCtl): a wait that runs out records
 // GBATTN_DEV_WAIT_TIMEOUT in the device status word, the CTA stops, waits a
