@@ -167,6 +167,9 @@ struct SparseTiles {
     uint8_t mask[kMaxSparseTiles];
     uint8_t kv0[kMaxSparseTiles];   // real keys in each 64-key half (boundary cubes)
     uint8_t kv1[kMaxSparseTiles];
+    // What the softmax reads per tile, in one word: quadrant bits | real keys of
+    // the first half << 8 | real keys of the second half << 16.
+    uint32_t info[kMaxSparseTiles];
 };
 
 // Masked mode: every softmax warp stages the mask of its 32 rows x 64 keys of a
@@ -474,6 +477,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             __syncwarp();
             if (MODE == kSparseFull && a.cube_valid && qtile >= a.prefix / BM)
                 fill_tile_counts(st, ctrl, a);
+            __syncwarp();
+            const bool counts = MODE == kSparseFull && a.cube_valid;
+            for (int t = lane; t < ctrl->n_tiles; t += 32)
+                st->info[t] = st->mask[t] | (static_cast<uint32_t>(counts ? st->kv0[t] : 64) << 8) |
+                              (static_cast<uint32_t>(counts ? st->kv1[t] : 64) << 16);
         }
         __syncwarp();
     }
@@ -871,6 +879,16 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         for (int j = 0; j < n_tiles; ++j) {
             const int buf = j % C::NSB;
             const uint32_t sbuf = tl + buf * 128;
+            // Sparse modes: this half's visible-column limit (a hidden quadrant 0, a
+            // boundary cube its real-key count), read before S arrives so that its
+            // shared-memory latency stays off the path from S to P.
+            int lim_c = 64;
+            if (is_sparse(MODE)) {
+                const uint32_t ti = st->info[j];
+                const bool vis = (ti >> (row_half * 2 + half)) & 1u;
+                // plain VSA: all 64 keys or none (a limit the compiler can see)
+                lim_c = !vis ? 0 : MODE == kSparseFull ? static_cast<int>((ti >> (8 + 8 * half)) & 0xFFu) : 64;
+            }
             ok = wait_warp(&ctrl->s_full[buf], (j / C::NSB) & 1, w);
             if (!ok) break;
             tc_fence_after();
@@ -913,13 +931,10 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                         if (c >= lim_c) s[c] = __float_as_uint(-INFINITY);
                 }
             } else if (is_sparse(MODE)) {
-                // One column limit per tile half: a quadrant hidden from this row's cube
-                // hides all 64 keys, a boundary cube its padding keys.  (Two separate
-                // masking loops here had cost the full-layout kernel 45 registers and
-                // a quarter of its speed.)
-                const uint32_t mk = st->mask[j];
-                int lim_c = ((mk >> (row_half * 2 + half)) & 1u) ? 64 : 0;
-                if (MODE == kSparseFull && a.cube_valid && lim_c) lim_c = half ? st->kv1[j] : st->kv0[j];
+                // One column limit per tile half (read above): a quadrant hidden from
+                // this row's cube hides all 64 keys, a boundary cube its padding keys.
+                // (Two separate masking loops here had cost the full-layout kernel 45
+                // registers and a quarter of its speed.)
                 if (lim_c < 64) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
