@@ -37,9 +37,10 @@ def check_pairing(pairs, nc):
         assert np.all(np.diff(row[:, 0]) > 0)                       # listed by first cube
 
 
-@pytest.mark.parametrize("grid,topk", [((8, 32, 32), 16), ((4, 16, 20), 9), ((4, 12, 12), 4)])
-def test_pairing_valid_and_sparse_matches(gb, grid, topk):
-    q, k, v = inputs.vsa_inputs(1, 3, 128, seed=50 + topk, grid=grid)
+@pytest.mark.parametrize("B,grid,topk", [(1, (8, 32, 32), 16), (1, (4, 16, 20), 9),
+                                          (1, (4, 12, 12), 4), (2, (4, 16, 16), 8)])
+def test_pairing_valid_and_sparse_matches(gb, B, grid, topk):
+    q, k, v = inputs.vsa_inputs(B, 3, 128, seed=50 + topk, grid=grid)
     tq, tk, tv = t(q), t(k), t(v)
     idx = gb.vsa_select_blocks(tq, tk, topk)
     pairs = gb.vsa_pair_query_cubes(idx)
@@ -56,8 +57,9 @@ def test_pairing_valid_and_sparse_matches(gb, grid, topk):
     assert_close(lse.cpu().numpy(), rl, "lse")
 
 
-def test_pairing_with_prefix_and_boundary_cubes(gb):
-    q, k, v, valid = inputs.vsa_full_inputs(1, 2, 128, seed=57, grid=(5, 10, 9), prefix=128)
+@pytest.mark.parametrize("B", [1, 2])
+def test_pairing_with_prefix_and_boundary_cubes(gb, B):
+    q, k, v, valid = inputs.vsa_full_inputs(B, 2, 128, seed=57, grid=(5, 10, 9), prefix=128)
     tq, tk, tv, tval = t(q), t(k), t(v), t(valid)
     idx = gb.vsa_select_blocks(tq, tk, 5, prefix=128, cube_valid=tval)
     pairs = gb.vsa_pair_query_cubes(idx)
