@@ -42,7 +42,8 @@ def two_ways(gb, Hq, Hkv, Q, KV, ps, ks, vs, seed, q_real=None, codes="finite"):
     (6, 1, 320, 4096, 16, 0.0625, 0.125),          # small pages, several key chunks
     (4, 2, 128, 2048, 64, float(np.float16(0.3)), float(np.float16(0.7))),   # FP16-valued scales
     (6, 1, 192, 1536, 128, 1 / 3, 0.3),            # general scales (round-to-odd)
-    (6, 1, 64, 2080, 32, 0.0625, 0.125)])          # KV not a multiple of 128 (ragged last tile)
+    (6, 1, 64, 2080, 32, 0.0625, 0.125),           # KV not a multiple of 128 (ragged last tile)
+    (6, 1, 128, 1536, 256, 0.0625, 0.125)])        # pages of 256 tokens (two 128-key tiles each)
 def test_fused_equals_bridge_then_prefill(gb, Hq, Hkv, Q, KV, ps, ks, vs):
     _, _, _, _, of, lf, ob, lb = two_ways(gb, Hq, Hkv, Q, KV, ps, ks, vs, seed=90 + ps)
     assert torch.equal(of, ob)
