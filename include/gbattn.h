@@ -5,17 +5,22 @@
  * FP32 accumulation of Q K^T and P V, an FP32 online-softmax state and FP16
  * probabilities ("Integrate FP32 v37 prefill and exact E4M3 bridge",
  * Implementation: FP32 QK/PV accumulation and prefix/tail state, probabilities
- * and final output stored as FP16), in three variants:
+ * and final output stored as FP16), in these variants:
  *   - dense non-causal heads of width 128 (the video-DiT attention of "Share
- *     SM70 projection, attention and row reduction paths", Purpose);
+ *     SM70 projection, attention and row reduction paths", Purpose), also with
+ *     an additive FP16 mask (the mask term of the formula);
  *   - causal long prefill with shared-KV heads at width 256, the query block
  *     appended after a key prefix, optionally fed from a paged E4M3 cache
- *     through an exact E4M3 -> FP16 bridge ("Integrate FP32 v37 prefill and
- *     exact E4M3 bridge", Implementation);
+ *     through an exact E4M3 -> FP16 bridge, or reading the pages directly
+ *     ("Integrate FP32 v37 prefill and exact E4M3 bridge", Implementation);
+ *   - decode over a paged E4M3 cache: the newest tokens of ragged sequences
+ *     against their whole caches (same page, Validation: the E4M3 decode wave
+ *     kernels and the 256000-input decode);
  *   - VSA block-sparse attention: 64-token cubes, mean-pooled cube scores pick
  *     the top-k key cubes of every query cube, then attention runs over only
- *     those cubes ("Integrate H3 SM70 execution, metrics and VSA diagnostics",
- *     Purpose: top-k = 64).
+ *     those cubes, optionally with dense prefix tokens and padded boundary
+ *     cubes ("Integrate H3 SM70 execution, metrics and VSA diagnostics",
+ *     Purpose: top-k = 64, prefix-dense queries, boundary handling).
  *
  * Conventions shared by every entry point:
  *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
