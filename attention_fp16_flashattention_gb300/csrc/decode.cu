@@ -9,7 +9,7 @@
 // Work split (balanced whatever the lengths): a stream is one (sequence, KV
 // head, group of <= 8 query rows); its work is ceil(kv_len / 16) tiles of 16
 // cached tokens.  The streams' tiles are laid end to end and every warp of a
-// persistent grid (4 warps per SM) takes an equal contiguous range of them.
+// persistent grid (8 warps per SM) takes an equal contiguous range of them.
 //   * Each warp runs its own pipeline: a ring of 16-token stages filled by TMA
 //     (128-byte swizzle, one box per 128-byte half of the head width for K and
 //     V) issued by one elected lane, with the page-table entries of the next 32
@@ -39,10 +39,10 @@ namespace gbattn {
 namespace {
 
 constexpr int kTile = 16;        // tokens per tile (one MMA M block)
-// Warps per CTA, each with its own pipeline.  Four deep rings stream as fast as
-// eight shallower ones (the same bytes in flight) and halve the partial records
-// the merge reads; three or two warps cannot keep up with the conversion work.
-constexpr int kWarps = 4;
+// Warps per CTA, each with its own pipeline.  Two warps per scheduler hide each
+// other's conversion and MMA latency chains; eight warps with two stages hold
+// the same bytes in flight (128 KB per SM) as four with four.
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRows = 8;         // query rows per stream (MMA N)
 constexpr int kMaxSeqs = 4096;   // sequences per launch (prefix table in shared memory)
@@ -59,7 +59,7 @@ enum ScaleMode { kScaleFolded = 0, kScaleHalf = 1, kScaleGeneral = 2 };
 template <int D>
 struct Cfg {
     static constexpr int kHalves = D / 128;
-    static constexpr int kStages = D == 256 ? 4 : 8;          // 32 KB in flight per warp
+    static constexpr int kStages = D == 256 ? 2 : 4;          // 16 KB per warp
     static constexpr int kBox = kTile * 128;                     // one TMA box
     static constexpr int kStageBytes = 2 * kHalves * kBox;       // K halves, then V halves
     static constexpr int kSteps = D / 16;                        // QK k-steps, PV d-blocks
@@ -489,8 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // records of a row are those of the warps whose tile ranges meet its stream.
 // One CTA takes one row and a 32-wide slice of the head width: 8 lanes cover
 // the slice (one float4 each) and 64 lane groups take every 64th record, so
-// many record loads are in flight at once.  A rejected sequence (no tiles)
-// gets O = 0, lse = -inf.
+// many record loads are in flight at once.  Each lane group folds its records
+// in one pass (a running max, as in the online softmax), and the groups' results
+// are folded the same way.  A rejected sequence (no tiles) gets O = 0,
+// lse = -inf.
 template <int D>
 __global__ void __launch_bounds__(512) decode_merge_kernel(const float* __restrict__ part_o,
                                                            const float2* __restrict__ part_ml,
@@ -531,69 +533,68 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(const float* __restri
     // With at least as many tiles as warps every warp range is non-empty, and
     // the per-record emptiness test (two 64-bit divisions) is skipped.
     const bool all_busy = U >= W;
-    float mx = -INFINITY;
-    for (uint32_t w = w0 + tid; w <= w1; w += 512)
-        if (all_busy || warp_start(w, W, U) < warp_start(w + 1, W, U))
-            mx = fmaxf(mx, part_ml[(w + s_index) * kRows + n].x);
-#pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
-    if ((tid & 31) == 0) red[tid >> 5] = mx;
-    __syncthreads();
-    mx = red[0];
-#pragma unroll
-    for (int k = 1; k < 16; ++k) mx = fmaxf(mx, red[k]);
-
+    // One pass: every lane keeps its own running max, sum and weighted O slice
+    // over its records, and the lanes are then folded pairwise.
+    float mx = -INFINITY, lw = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    float lw = 0.0f;
-    if (mx != -INFINITY) {
-#pragma unroll 4
-        for (uint32_t w = w0 + rl; w <= w1; w += 64) {
-            if (!all_busy && warp_start(w, W, U) == warp_start(w + 1, W, U)) continue;
-            const long long rec = (w + s_index) * kRows + n;
-            const float2 ml = part_ml[rec];
-            const float wc = exp2f(ml.x - mx);
-            const float4 v = *reinterpret_cast<const float4*>(part_o + rec * D + slice * 32 + f4 * 4);
-            acc.x += wc * v.x;
-            acc.y += wc * v.y;
-            acc.z += wc * v.z;
-            acc.w += wc * v.w;
-            lw += wc * ml.y;
+#pragma unroll 8
+    for (uint32_t w = w0 + rl; w <= w1; w += 64) {
+        if (!all_busy && warp_start(w, W, U) == warp_start(w + 1, W, U)) continue;
+        const long long rec = (w + s_index) * kRows + n;
+        const float2 ml = part_ml[rec];
+        const float4 v = *reinterpret_cast<const float4*>(part_o + rec * D + slice * 32 + f4 * 4);
+        if (ml.x > mx) {   // a larger max: rescale what this lane holds
+            const float sc = mx == -INFINITY ? 0.0f : exp2f(mx - ml.x);
+            acc = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+            lw *= sc;
+            mx = ml.x;
         }
+        const float wc = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - mx);
+        acc = make_float4(acc.x + wc * v.x, acc.y + wc * v.y, acc.z + wc * v.z, acc.w + wc * v.w);
+        lw += wc * ml.y;
     }
-    // Sum over the 64 record lanes: 4 per warp by shuffles, then the 16 warps.
+    // (m1, l1, a1) <- the combination of (m1, l1, a1) and (m2, l2, a2)
+    auto fold = [](float& m1, float& l1, float4& a1, float m2, float l2, float4 a2) {
+        const float m = fmaxf(m1, m2);
+        const float s1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - m);
+        const float s2 = m2 == -INFINITY ? 0.0f : exp2f(m2 - m);
+        a1 = make_float4(a1.x * s1 + a2.x * s2, a1.y * s1 + a2.y * s2, a1.z * s1 + a2.z * s2,
+                         a1.w * s1 + a2.w * s2);
+        l1 = l1 * s1 + l2 * s2;
+        m1 = m;
+    };
+    // Fold the 64 record lanes: 4 per warp by shuffles, then the 16 warps.
 #pragma unroll
     for (int sh = 8; sh < 32; sh <<= 1) {
-        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, sh);
-        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, sh);
-        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, sh);
-        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, sh);
-        lw += __shfl_xor_sync(0xffffffffu, lw, sh);
+        const float4 ao = make_float4(__shfl_xor_sync(0xffffffffu, acc.x, sh),
+                                      __shfl_xor_sync(0xffffffffu, acc.y, sh),
+                                      __shfl_xor_sync(0xffffffffu, acc.z, sh),
+                                      __shfl_xor_sync(0xffffffffu, acc.w, sh));
+        const float lo = __shfl_xor_sync(0xffffffffu, lw, sh);
+        const float mo = __shfl_xor_sync(0xffffffffu, mx, sh);
+        fold(mx, lw, acc, mo, lo, ao);
     }
     const int wid = tid >> 5;
     if ((tid & 31) < 8) {
         part[wid][f4] = acc;
-        if (f4 == 0) lpart[wid] = lw;
+        if (f4 == 0) {
+            lpart[wid] = lw;
+            red[wid] = mx;
+        }
     }
     __syncthreads();
     if (tid >= 8) return;
-    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    float L = 0.0f;
+    float M = red[0], L = lpart[0];
+    float4 sacc = part[0][f4];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const float4 v = part[k][f4];
-        s.x += v.x;
-        s.y += v.y;
-        s.z += v.z;
-        s.w += v.w;
-        L += lpart[k];
-    }
+    for (int k = 1; k < 16; ++k) fold(M, L, sacc, red[k], lpart[k], part[k][f4]);
     const float inv = L > 0.0f ? out_mul / L : 0.0f;
     uint2 out;
-    out.x = pack_half2(s.x * inv, s.y * inv);
-    out.y = pack_half2(s.z * inv, s.w * inv);
+    out.x = pack_half2(sacc.x * inv, sacc.y * inv);
+    out.y = pack_half2(sacc.z * inv, sacc.w * inv);
     *reinterpret_cast<uint2*>(o + row * D + slice * 32 + f4 * 4) = out;
     if (lse && slice == 0 && f4 == 0)
-        lse[row] = L > 0.0f ? (mx + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 bool power_of_two_in(float s, int lo, int hi) {
