@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // are folded the same way.  A rejected sequence (no tiles) gets O = 0,
 // lse = -inf.
 template <int D>
-__global__ void __launch_bounds__(512) decode_merge_kernel(const float* __restrict__ part_o,
+__global__ void __launch_bounds__(512, 2) decode_merge_kernel(const float* __restrict__ part_o,
                                                            const float2* __restrict__ part_ml,
                                                            const uint32_t* __restrict__ prefix,
                                                            int B, int Hq, int Hkv, int nq,
@@ -537,21 +537,36 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(const float* __restri
     // over its records, and the lanes are then folded pairwise.
     float mx = -INFINITY, lw = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 8
-    for (uint32_t w = w0 + rl; w <= w1; w += 64) {
-        if (!all_busy && warp_start(w, W, U) == warp_start(w + 1, W, U)) continue;
-        const long long rec = (w + s_index) * kRows + n;
-        const float2 ml = part_ml[rec];
-        const float4 v = *reinterpret_cast<const float4*>(part_o + rec * D + slice * 32 + f4 * 4);
-        if (ml.x > mx) {   // a larger max: rescale what this lane holds
-            const float sc = mx == -INFINITY ? 0.0f : exp2f(mx - ml.x);
-            acc = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
-            lw *= sc;
-            mx = ml.x;
+    // Records are fetched 6 per lane group at a time, all loads issued before
+    // any of them is used, so one round of L2 latency covers 384 records.
+    constexpr int kBatch = 6;
+    for (uint32_t wb = w0 + rl; wb <= w1; wb += 64 * kBatch) {
+        float2 ml[kBatch];
+        float4 v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const uint32_t w = wb + 64 * j;
+            ml[j] = make_float2(-INFINITY, 0.0f);
+            v[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (w <= w1 && (all_busy || warp_start(w, W, U) < warp_start(w + 1, W, U))) {
+                const long long rec = (w + s_index) * kRows + n;
+                ml[j] = part_ml[rec];
+                v[j] = *reinterpret_cast<const float4*>(part_o + rec * D + slice * 32 + f4 * 4);
+            }
         }
-        const float wc = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - mx);
-        acc = make_float4(acc.x + wc * v.x, acc.y + wc * v.y, acc.z + wc * v.z, acc.w + wc * v.w);
-        lw += wc * ml.y;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (ml[j].x > mx) {   // a larger max: rescale what this lane holds
+                const float sc = mx == -INFINITY ? 0.0f : exp2f(mx - ml[j].x);
+                acc = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+                lw *= sc;
+                mx = ml[j].x;
+            }
+            const float wc = ml[j].x == -INFINITY ? 0.0f : exp2f(ml[j].x - mx);
+            acc = make_float4(acc.x + wc * v[j].x, acc.y + wc * v[j].y, acc.z + wc * v[j].z,
+                              acc.w + wc * v[j].w);
+            lw += wc * ml[j].y;
+        }
     }
     // (m1, l1, a1) <- the combination of (m1, l1, a1) and (m2, l2, a2)
     auto fold = [](float& m1, float& l1, float4& a1, float m2, float l2, float4 a2) {
