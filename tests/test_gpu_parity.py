@@ -99,6 +99,21 @@ def test_bridge_live_length_multi_head_and_bad_page(gb):
     assert np.array_equal(k[:, :48], rk[:, :48]) and np.array_equal(k[:, 64:], rk[:, 64:])
 
 
+@pytest.mark.parametrize("Hkv,D,kv_len,k_scale,v_scale", [
+    (1, 16, 333, 0.0625, 0.125),       # two 8-byte chunks per token row
+    (5, 48, 301, 1 / 3, 0.3),          # rows of 6 chunks, round-to-odd scaling
+    (2, 208, 259, float(np.float16(0.3)), 2.0 ** -14)])
+def test_bridge_head_widths_bit_exact(gb, Hkv, D, kv_len, k_scale, v_scale):
+    """Head widths whose rows are not a multiple of a warp's 32 chunks, several KV heads and
+    a live length that ends inside a page."""
+    kp, vp, table = inputs.paged_e4m3_inputs(Hkv, kv_len + 20, D, seed=D + Hkv, page_size=16)
+    ko, vo = gb.e4m3_paged_to_fp16(t(kp), t(vp), t(table), kv_len, k_scale, v_scale)
+    rk, rv = OE.paged_e4m3_to_fp16(kp, vp, table, kv_len, k_scale, v_scale)
+    assert np.array_equal(ko.cpu().numpy().view(np.uint16), rk)   # finite codes only
+    assert np.array_equal(vo.cpu().numpy().view(np.uint16), rv)
+    assert gb.device_status() == 0
+
+
 def test_bridge_full_size_bit_exact(gb):
     w = inputs.WORKLOADS["paged_e4m3"]
     kp, vp, table = workload("paged_e4m3")
