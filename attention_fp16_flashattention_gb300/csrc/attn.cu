@@ -465,6 +465,29 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         ctrl->abort = 0;
         mbar_init_fence();
     }
+    // The query tile's copy (one elected lane of the TMA warp).
+    auto issue_q = [&]() {
+        if (elect_one()) {
+            mbar_arrive_expect_tx(&ctrl->q_full, C::Q_BYTES);
+            if (is_sparse(MODE)) {   // two 64-row halves (a query-cube pair); tmM has 64-row boxes
+                const int r1 = rbase1 >= 0 ? rbase1 : rbase0;
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c) {
+                    tma_load_3d(sQ + c * C::CHUNK, &tmM, &ctrl->q_full, c * 64, rbase0, bh);
+                    tma_load_3d(sQ + c * C::CHUNK + C::HALF, &tmM, &ctrl->q_full, c * 64, r1, bh);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_3d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, bh);
+            }
+        }
+        __syncwarp();
+    };
+    const bool load_q = a.fault != 1;
+    // Sparse modes build the key-tile list first; the query tile does not depend
+    // on it, so its copy is issued before and is in flight while the list is built.
+    const bool early_q = is_sparse(MODE) && load_q;
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
@@ -472,6 +495,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             tma_prefetch_desc(&tmV);
             if (MODE == kMasked || is_sparse(MODE)) tma_prefetch_desc(&tmM);
         }
+        __syncwarp();   // the barriers thread 0 initialised are visible to the warp
+        if (early_q) issue_q();
         if (is_sparse(MODE)) {
             build_sparse_tiles<MODE == kSparseFull>(st, ctrl, a, bh, qtile, ca, cb);
             __syncwarp();
@@ -535,23 +560,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         // ================= TMA producer (whole warp; one elected lane issues)
         if (n_tiles > 0) {
             int last_it[4] = {-1, -1, -1, -1};
-            const bool load_q = a.fault != 1;
-            if (load_q && elect_one()) {
-                mbar_arrive_expect_tx(&ctrl->q_full, C::Q_BYTES);
-                if (is_sparse(MODE)) {   // two 64-row halves (a query-cube pair); tmM has 64-row boxes
-                    const int r1 = rbase1 >= 0 ? rbase1 : rbase0;
-#pragma unroll
-                    for (int c = 0; c < C::KCH; ++c) {
-                        tma_load_3d(sQ + c * C::CHUNK, &tmM, &ctrl->q_full, c * 64, rbase0, bh);
-                        tma_load_3d(sQ + c * C::CHUNK + C::HALF, &tmM, &ctrl->q_full, c * 64, r1, bh);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < C::KCH; ++c)
-                        tma_load_3d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, bh);
-                }
-            }
-            __syncwarp();
+            if (load_q && !early_q) issue_q();
             bool ok = true;
             // paged: lane j holds the cache row of box j (page_box tokens) of the
             // item after the one being issued; boxes cover the item's 128 keys.
@@ -633,6 +642,9 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                         drain_wait(MODE == kCausalPaged ? &ctrl->raw_full[s] : &ctrl->full[s],
                                    (last_it[s] / C::NS) & 1);
             }
+        } else if (early_q) {   // an empty key list (bad indices): nobody waits for Q
+            if (lane == 0) drain_wait(&ctrl->q_full, 0);
+            __syncwarp();
         }
     } else if (warp == 1) {
         // ================= MMA issuer (whole warp waits; one elected lane issues
