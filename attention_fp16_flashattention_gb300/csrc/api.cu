@@ -88,7 +88,7 @@ int encode_tmap_f16_mask(CUtensorMap* map, const void* base, uint64_t skv, uint6
     if (load_encoder() != GBATTN_OK) return GBATTN_ERR_CUDA;
     cuuint64_t dims[4] = {skv, sq, heads, batch};
     cuuint64_t strides[3] = {skv * 2, stride_h * 2, stride_b * 2};   // bytes, dims 1..3
-    cuuint32_t box[4] = {64, 32, 1, 1};
+    cuuint32_t box[4] = {64, 128, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

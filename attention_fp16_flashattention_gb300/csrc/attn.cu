@@ -10,7 +10,8 @@
 // two-key-half blocks with a 4-bit quadrant mask of block_lists.py in the
 // FastVideo compare view).
 //
-// Warp roles (352 threads at D=128, 320 at D=256, 448 with the paged converters):
+// Warp roles (352 threads at D=128, 384 with the mask warp, 320 at D=256, 448 with
+// the paged converters):
 //   warp 0      TMA producer: Q once, then K and V tiles through an NS-slot ring
 //               in the order the MMAs consume them (K0 .. K_{NSB-1}, V0, K_NSB,
 //               V1, ...).
@@ -24,6 +25,7 @@
 //               exp2 with packed FP32 pairs, row sum, P -> FP16 into TMEM; lazy
 //               O rescaling (only when the running max grows by more than 2^8),
 //               each thread on its half of O; epilogue O / l.
+//   warp 11     (masked) loads each tile's 128 x 128 mask block two tiles ahead.
 //   warps 10..13 (paged causal) convert E4M3 page rows to FP16 in shared memory.
 // Tensor memory (512 columns): NSB S buffers of 128 FP32 columns (3 for D=128,
 // 2 for D=256); P_j overwrites the first 64 columns of its S buffer as FP16
@@ -67,10 +69,11 @@ __host__ __device__ constexpr bool is_causal(int mode) { return mode == kCausal 
 __host__ __device__ constexpr bool dual_issue(int mode) { return !(mode == kCausal || mode == kCausalPaged); }
 constexpr int kPvWarp = 10;
 // threads per CTA: the PV issuer adds a warp (10); the paged mode adds four
-// converter warps (10..13)
+// converter warps (10..13), the masked mode a mask-loading warp (11)
 __host__ __device__ constexpr int threads_for(int mode) {
-    return mode == kCausalPaged ? 448 : (dual_issue(mode) ? 352 : 320);
+    return mode == kCausalPaged ? 448 : mode == kMasked ? 384 : (dual_issue(mode) ? 352 : 320);
 }
+constexpr int kMaskWarp = 11;
 constexpr int kConvThreads = 128;
 
 struct AttnArgs {
@@ -172,11 +175,11 @@ struct SparseTiles {
     uint32_t info[kMaxSparseTiles];
 };
 
-// Masked mode: every softmax warp stages the mask of its 32 rows x 64 keys of a
-// tile (4 KB, TMA, 128-byte swizzle) in two slots, two tiles ahead; the 16
-// slot barriers follow the stages.
-constexpr int kMaskSlotBytes = 32 * 128;
-constexpr int kMaskStageBytes = 8 * 2 * kMaskSlotBytes + 16 * 8;
+// Masked mode: the mask warp stages each tile's 128 rows x 128 keys of the mask
+// (two 64-key boxes of 16 KB, TMA, 128-byte swizzle) in two slots, two tiles
+// ahead; the slots' full and empty barriers follow them.
+constexpr int kMaskSlotBytes = 128 * 256;
+constexpr int kMaskStageBytes = 2 * kMaskSlotBytes + 4 * 8;
 
 template <int D, int MODE>
 constexpr int smem_bytes() {
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     uint8_t* sKV = smem + C::Q_BYTES;
     // masked mode: mask stages (1024-aligned) and their barriers after the ring
     uint8_t* sMask = sKV + C::NS * C::SLOT_BYTES;
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(sMask + 8 * 2 * kMaskSlotBytes);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sMask + 2 * kMaskSlotBytes);   // full[2], empty[2]
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(sKV + C::NS * C::SLOT_BYTES +
                                          (MODE == kMasked ? kMaskStageBytes : 0));
     Exchange* ex = reinterpret_cast<Exchange*>(reinterpret_cast<uint8_t*>(ctrl) + 256);
@@ -459,7 +462,10 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         for (int i = 0; i < C::NSB; ++i) mbar_init(&ctrl->pv_done[i], 1);
         for (int i = 0; i < 4; ++i) mbar_init(&ctrl->xchg[i], 64);
         if (MODE == kMasked)
-            for (int i = 0; i < 16; ++i) mbar_init(&mbar[i], 1);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&mbar[i], 1);                          // the slot's bytes landed
+                mbar_init(&mbar[2 + i], kSoftmaxThreads / 32);   // every softmax warp read it
+            }
         mbar_init(&ctrl->drain, 1);
         mbar_init(&ctrl->drain_pv, 1);
         ctrl->abort = 0;
@@ -831,6 +837,33 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             if (lane == 0) mbar_arrive(&ctrl->full[slot]);
         }
         (void)ok;
+    } else if (MODE == kMasked && warp == kMaskWarp) {
+        // ================= mask loader (masked mode): tile t's mask rows into slot
+        // t % 2 once every softmax warp has read tile t - 2 from it
+        const int mb_b = bh / a.hq, mb_h = bh - mb_b * a.hq;
+        bool ok = true;
+        int issued = 0;
+        for (int t = 0; t < n_tiles; ++t) {
+            if (t >= 2 && !wait_warp(&mbar[2 + (t & 1)], ((t >> 1) - 1) & 1, w)) {
+                ok = false;
+                break;
+            }
+            int f0, f1;
+            tile_keys(t, f0, f1);
+            if (elect_one()) {
+                uint8_t* dst = sMask + (t & 1) * kMaskSlotBytes;
+                mbar_arrive_expect_tx(&mbar[t & 1], kMaskSlotBytes);
+                tma_load_4d(dst, &tmM, &mbar[t & 1], f0, q_row0, a.mask_sh ? mb_h : 0,
+                            a.mask_sb ? mb_b : 0);
+                tma_load_4d(dst + kMaskSlotBytes / 2, &tmM, &mbar[t & 1], f1, q_row0,
+                            a.mask_sh ? mb_h : 0, a.mask_sb ? mb_b : 0);
+            }
+            __syncwarp();
+            issued = t + 1;
+        }
+        if (!ok && lane == 0)   // copies in flight must land before the CTA exits
+            for (int t = max(0, issued - 2); t < issued; ++t) drain_wait(&mbar[t & 1], (t >> 1) & 1);
+        __syncwarp();
     } else {
         // ================= softmax / correction / epilogue (warps 2..9)
         // Two threads share each query row: warps 2..5 own key columns 0..63 of
@@ -865,29 +898,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         float m_run = -INFINITY, l = 0.0f;
         uint32_t xphase = 0;
         bool ok = true;
-        // Masked mode: this warp's 32 rows x 64 keys of the mask for tile t
-        // arrive by TMA in slot t % 2 (issued two tiles ahead by one lane).
-        const int sw = warp - 2;
-        uint8_t* mslots = sMask + sw * 2 * kMaskSlotBytes;
-        uint64_t* mb = mbar + sw * 2;
-        const int mb_b = bh / a.hq, mb_h = bh - mb_b * a.hq;
-        int m_issued = 0;
-        auto mask_issue = [&](int t) {
-            int f0, f1;
-            tile_keys(t, f0, f1);
-            const int kh = half ? f1 : f0;
-            if (elect_one()) {
-                mbar_arrive_expect_tx(&mb[t & 1], kMaskSlotBytes);
-                tma_load_4d(mslots + (t & 1) * kMaskSlotBytes, &tmM, &mb[t & 1], kh,
-                            q_row0 + quarter * 32, a.mask_sh ? mb_h : 0, a.mask_sb ? mb_b : 0);
-            }
-            __syncwarp();
-            ++m_issued;
-        };
-        if (MODE == kMasked && n_tiles > 0) {
-            mask_issue(0);
-            if (n_tiles > 1) mask_issue(1);
-        }
+        // Masked mode: tile t's mask arrives in slot t % 2, this thread's row of
+        // its half at [half][row][128 bytes] (staged by the mask warp).
         for (int j = 0; j < n_tiles; ++j) {
             const int buf = j % C::NSB;
             const uint32_t sbuf = tl + buf * 128;
@@ -913,10 +925,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             tile_keys(j, k0, k1);
             if (MODE == kMasked) {
                 // y = scale * s + mask, then hidden keys -> -inf.
-                ok = wait_warp(&mb[j & 1], (j >> 1) & 1, w);
+                ok = wait_warp(&mbar[j & 1], (j >> 1) & 1, w);
                 if (!ok) break;
                 const uint64_t sc2 = f2_pack(a.scale, a.scale);
-                const uint8_t* mrow = mslots + (j & 1) * kMaskSlotBytes + lane * 128;
+                const uint8_t* mrow =
+                    sMask + (j & 1) * kMaskSlotBytes + half * (kMaskSlotBytes / 2) + row * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 mv = *reinterpret_cast<const uint4*>(mrow + ((c ^ (lane & 7)) << 4));
@@ -933,7 +946,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                         s[2 * i + 1] = __float_as_uint(x1);
                     }
                 }
-                if (j + 2 < n_tiles) mask_issue(j + 2);   // into the slot just read
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&mbar[2 + (j & 1)]);   // this warp is done with the slot
                 // keys past the end and rows past the end hidden through one column limit
                 const int kh = half ? k1 : k0;
                 const int lim_c = row_g >= a.seq_q ? 0 : a.seq_k - kh;
@@ -1041,9 +1055,6 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             }
             tc_fence_before();
             mbar_arrive(&ctrl->p_full[buf]);
-        }
-        if (MODE == kMasked && !ok && lane == 0) {   // mask copies in flight must land first
-            for (int t = max(0, m_issued - 2); t < m_issued; ++t) drain_wait(&mb[t & 1], (t >> 1) & 1);
         }
         if (ok && n_tiles > 0) {
             ok = wait_warp(&ctrl->pv_done[(n_tiles - 1) % C::NSB], ((n_tiles - 1) / C::NSB) & 1, w);
