@@ -21,6 +21,10 @@ def test_work_model_closed_forms():
     assert bench.causal_flops(1, 6, 1024, 4096, 256) == 22_551_724_032
     assert bench.vsa_flops(1, 24, 32768, 128, 64) == 1_649_267_441_664
     assert bench.bridge_bytes(131072, 1, 256, 32) == 201_342_976
+    # decode: 417,843 cached tokens of K and V bytes, 13,060 page-table entries, Q and O in FP16
+    lens = (131072, 122887, 98313, 65571)
+    assert bench.decode_bytes(lens, 4, 6, 1, 1, 256, 32) == \
+        2 * 417_843 * 256 + 4 * 13_060 + 2 * 2 * 24 * 256 == 214_012_432
 
 
 def _free_port():
