@@ -1,22 +1,34 @@
-"""Pins for the oracle's VSA pooling, scores and top-k (CPU only).
+"""Pins for the oracle's VSA pooling, exact scores, top-k and coarse branch (CPU only).
 
 * Pooling: a constant cube pools to that constant; exactly summable data
   gives the exact mean; general data stays within the recursive-summation
   error bound of the exact mean; and a case built so that only the
   sequential token order gives the stated result pins the order reading.
-* Scores: integer-valued inputs (exact in FP32) equal numpy's int64 matrix
-  product; general inputs stay within gamma_D * sum |q||k| of the exact dot
-  product; a case that only sequential, non-fused evaluation reproduces pins
-  that reading.
-* Top-k: equal to a brute-force rank count; ties go to the lower index;
-  top-k = all returns every index; on data whose 64th/65th exact scores are
-  farther apart than the FP32 error bound the FP32 selection equals the
-  exact-arithmetic selection.
+* The exact grid: pooled FP16 data over the whole FP16 range (huge values,
+  subnormals, zeros, cancelling cubes, boundary counts) lies on the 2^-53
+  grid the exact scores use, limb by limb equal to the value as a fraction.
+* Exact scores: equal to sums of ``fractions.Fraction`` products on those
+  extreme inputs; integer inputs equal numpy's int64 matrix product; a case
+  that FP32 sequential scoring ranks the other way, and one that float64
+  scoring cannot separate, are ranked by the exact value.
+* Top-k: equal to a full sort by (exact score descending, index ascending)
+  on random and tie-heavy inputs (duplicate, zero and constant cubes); a
+  transposed selection is caught.
+* Coarse branch: equal to a pure-Python softmax over Fraction-exact scores;
+  scale 0 gives the mean pooled value, constant values give that constant,
+  one key cube gives its pooled value; the gated combination leaves prefix
+  and padding rows alone; a branch restricted to the selected cubes is caught.
 """
+
+from fractions import Fraction
+import math
+
+import pytest
 
 import numpy as np
 
-from oracle.vsa import cube_scores_fp32, pool_means_fp32, topk_blocks, vsa_select
+from oracle.vsa import (coarse_attention, exact_scores, exact_scores_float, gated_output,
+                        grid_limbs, pool_means_fp32, topk_blocks, topk_exact, vsa_select)
 
 U = 2.0 ** -24   # unit roundoff of FP32
 
@@ -57,36 +69,129 @@ def test_pool_sequential_order():
     assert pool_means_fp32(y, 64)[0, 0] == np.float32((1.0 + 63 * 2.0 ** -24) / 64.0)
 
 
-def test_scores_integer_inputs_match_int64_matmul():
+def _fraction_score(qv, kv):
+    return sum(Fraction(float(a)) * Fraction(float(b)) for a, b in zip(qv, kv))
+
+
+def _digits_value(parts, idx):
+    top, d3, d2, d1, d0 = (int(p[idx]) for p in parts)
+    return Fraction(top * 2 ** 92 + d3 * 2 ** 69 + d2 * 2 ** 46 + d1 * 2 ** 23 + d0, 2 ** 106)
+
+
+def _pooled_extremes(seed):
+    """Pooled FP16 data over the whole FP16 range: huge values, subnormals, zeros,
+    cancelling cubes, boundary counts that are not powers of two."""
+    rng = np.random.default_rng(seed)
+    nc, D = 12, 128
+    mag = 2.0 ** rng.integers(-24, 16, (nc * 64, D))
+    x = (rng.choice([-1.0, 1.0], (nc * 64, D)) * mag * rng.uniform(1, 2, (nc * 64, D)))
+    x = np.clip(x, -65504, 65504).astype(np.float16)
+    x[:64] = 0                                        # an all-zero cube
+    x[64:128:2] = -x[65:128:2]                        # a cube that nearly cancels
+    counts = rng.integers(1, 65, nc)
+    counts[3] = 64
+    return x, counts
+
+
+def test_pooled_means_lie_on_the_exact_grid():
+    for seed in range(3):
+        x, counts = _pooled_extremes(seed)
+        m = pool_means_fp32(x[None], 64, counts)
+        a0, a1, a2 = grid_limbs(m)
+        back = (a0 + a1.astype(object) * 2 ** 23 + a2.astype(object) * 2 ** 46)
+        for i in np.ndindex(m.shape):
+            assert Fraction(int(back[i]), 2 ** 53) == Fraction(float(m[i]))
+        assert np.all(np.abs(np.stack([a0, a1, a2])) < 2 ** 23)
+
+
+def test_grid_limbs_rejects_values_off_the_grid():
+    for bad in (2.0 ** -60, 2.0 ** 16, np.inf, np.nan):
+        with pytest.raises(ValueError):
+            grid_limbs(np.array([bad], np.float32))
+
+
+def test_exact_scores_equal_fraction_sums():
+    for seed in range(2):
+        x, counts = _pooled_extremes(seed)
+        y, _ = _pooled_extremes(seed + 10)
+        qm = pool_means_fp32(x[None], 64, counts)
+        km = pool_means_fp32(y[None], 64, counts)
+        parts = exact_scores(qm, km)
+        for i in range(qm.shape[1]):
+            for j in range(km.shape[1]):
+                assert _digits_value(parts, (0, i, j)) == _fraction_score(qm[0, i], km[0, j])
+        assert np.all((parts[1] >= 0) & (parts[1] < 2 ** 23))
+
+
+def test_exact_scores_integer_inputs_match_int64_matmul():
     rng = np.random.default_rng(2)
     qi = rng.integers(-50, 50, (3, 20, 128))
     ki = rng.integers(-50, 50, (3, 30, 128))
-    s = cube_scores_fp32(qi.astype(np.float32), ki.astype(np.float32))
+    s = exact_scores_float(qi.astype(np.float32), ki.astype(np.float32))
     ref = np.einsum("hqd,hkd->hqk", qi, ki)
-    assert np.array_equal(s.astype(np.int64), ref)
+    assert np.array_equal(s, ref.astype(np.float64))
 
 
-def test_scores_within_error_bound():
-    rng = np.random.default_rng(3)
-    q = rng.standard_normal((2, 16, 128)).astype(np.float32)
-    k = rng.standard_normal((2, 24, 128)).astype(np.float32)
-    s = cube_scores_fp32(q, k).astype(np.float64)
-    qd, kd = q.astype(np.float64), k.astype(np.float64)
-    exact = np.einsum("hqd,hkd->hqk", qd, kd)
-    g = 128 * U / (1 - 128 * U)
-    bound = g * np.einsum("hqd,hkd->hqk", np.abs(qd), np.abs(kd))
-    assert np.all(np.abs(s - exact) <= bound)
+def _brute_exact_topk(qm, km, topk):
+    out = []
+    for i in range(qm.shape[0]):
+        sc = [(-_fraction_score(qm[i], km[j]), j) for j in range(km.shape[0])]
+        out.append(sorted(j for _, j in sorted(sc)[:topk]))
+    return np.array(out, dtype=np.int32)
 
 
-def test_scores_sequential_unfused_order():
-    # products: 1, then 127 products equal to 2^-25 (0.5 ulp of 1): sequential
-    # FP32 adds round each tie back to 1; a fused or reordered sum would not.
-    q = np.full((1, 128), 2.0 ** -13, dtype=np.float32)
-    k = np.full((1, 128), 2.0 ** -12, dtype=np.float32)
-    q[0, 0] = 1.0
-    k[0, 0] = 1.0
-    assert cube_scores_fp32(q, k)[0, 0] == np.float32(1.0)
-    assert cube_scores_fp32(q[:, ::-1].copy(), k[:, ::-1].copy())[0, 0] > np.float32(1.0)
+def test_topk_exact_equals_full_sort_random_and_ties():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((6 * 64, 16)).astype(np.float16)
+    k = rng.standard_normal((40 * 64, 16)).astype(np.float16)
+    k[5 * 64:6 * 64] = k[2 * 64:3 * 64]                 # duplicate cube: exact tie
+    k[7 * 64:9 * 64] = 0                                # zero cubes: exact ties
+    k[20 * 64:21 * 64] = k[30 * 64:31 * 64]
+    qm, km = pool_means_fp32(q, 64), pool_means_fp32(k, 64)
+    for topk in (1, 9, 40):
+        assert np.array_equal(topk_exact(qm, km, topk), _brute_exact_topk(qm, km, topk))
+    const = np.full((3 * 64, 16), 0.5, np.float16)      # every score equal: lowest indices
+    cm = pool_means_fp32(const, 64)
+    assert np.array_equal(topk_exact(cm, cm, 2), [[0, 1]] * 3)
+
+
+def test_exact_order_is_not_fp32_order():
+    # key 1: products 1, 2^-25, 2^-25 (exact 1 + 2^-24); key 0: products 1, 2^-25
+    # (exact 1 + 2^-25).  Sequential FP32 rounds both to 1.0 (a tie, so key 0),
+    # the exact scores rank key 1 first.
+    q = np.zeros((1, 128), np.float32)
+    q[0, :3] = [1.0, 2.0 ** -13, 2.0 ** -13]
+    k = np.zeros((2, 128), np.float32)
+    k[0, :2] = [1.0, 2.0 ** -12]
+    k[1, :3] = [1.0, 2.0 ** -12, 2.0 ** -12]
+    assert np.array_equal(topk_exact(q, k, 1), [[1]])
+    seq = np.float32(0)
+    for d in range(128):
+        seq = np.float32(seq + np.float32(q[0, d] * k[0, d]))
+    assert seq == np.float32(1.0)
+
+
+def test_planted_fp64_score_is_caught():
+    # exact scores 2^10 + 2^-60 (key 1) and 2^10 (key 0): float64 cannot tell them
+    # apart and would keep key 0 on the index tie-break.
+    q = np.zeros((1, 128), np.float32)
+    q[0, :2] = [2.0 ** 5, 2.0 ** -30]
+    k = np.zeros((2, 128), np.float32)
+    k[0, 0] = 2.0 ** 5
+    k[1, :2] = [2.0 ** 5, 2.0 ** -30]
+    fp64 = topk_blocks(np.einsum("qd,kd->qk", q.astype(np.float64), k.astype(np.float64)), 1)
+    assert np.array_equal(fp64, [[0]])
+    assert np.array_equal(topk_exact(q, k, 1), [[1]])
+
+
+def test_planted_transposed_selection_is_caught():
+    rng = np.random.default_rng(7)
+    qm = pool_means_fp32(rng.standard_normal((5 * 64, 8)).astype(np.float16), 64)
+    km = pool_means_fp32(rng.standard_normal((11 * 64, 8)).astype(np.float16), 64)
+    want = _brute_exact_topk(qm, km, 3)
+    assert np.array_equal(topk_exact(qm, km, 3), want)
+    wrong = topk_exact(km, qm, 3)                        # ranks query cubes per key cube
+    assert wrong.shape != want.shape or not np.array_equal(wrong, want)
 
 
 def _brute_topk(s, k):
@@ -98,15 +203,12 @@ def _brute_topk(s, k):
     return np.array(out).reshape(s.shape[:-1] + (k,))
 
 
-def test_topk_matches_rank_count_random_and_ties():
+def test_topk_blocks_matches_rank_count_random_and_ties():
     rng = np.random.default_rng(4)
     s = rng.standard_normal((3, 7, 40)).astype(np.float32)
     assert np.array_equal(topk_blocks(s, 9), _brute_topk(s, 9))
     t = rng.integers(0, 4, (3, 7, 40)).astype(np.float32)      # heavy ties
     assert np.array_equal(topk_blocks(t, 9), _brute_topk(t, 9))
-    z = np.zeros((1, 2, 40), np.float32)
-    assert np.array_equal(topk_blocks(z, 5)[0, 0], np.arange(5))
-    assert np.array_equal(topk_blocks(s, 40)[1, 2], np.arange(40))
 
 
 def test_duplicate_key_cubes_prefer_lower_index():
@@ -121,32 +223,76 @@ def test_duplicate_key_cubes_prefer_lower_index():
     assert np.all(np.diff(idx, axis=-1) > 0)
 
 
-def test_fp32_selection_equals_exact_selection_away_from_ties():
-    rng = np.random.default_rng(6)
-    q = (rng.standard_normal((2, 16 * 64, 32)) * 0.5 + 0.3).astype(np.float16)
-    k = (rng.standard_normal((2, 96 * 64, 32)) * 0.5 + 0.3).astype(np.float16)
-    idx = vsa_select(q, k, 64, 20)
-    qd = q.astype(np.float64).reshape(2, 16, 64, 32).mean(axis=2)
-    kd = k.astype(np.float64).reshape(2, 96, 64, 32).mean(axis=2)
-    exact = np.einsum("hqd,hkd->hqk", qd, kd)
-    checked = 0
+# ------------------------------------------------------------------ coarse branch
+def _brute_coarse(qm, km, vm, scale):
+    out = []
+    sc = float(np.float32(scale))
+    for i in range(qm.shape[0]):
+        logits = [sc * float(_fraction_score(qm[i], km[j])) for j in range(km.shape[0])]
+        mx = max(logits)
+        w = [math.exp(x - mx) for x in logits]
+        tot = sum(w)
+        out.append([sum(w[j] * float(vm[j, d]) for j in range(len(w))) / tot
+                    for d in range(vm.shape[1])])
+    return np.array(out)
+
+
+def test_coarse_attention_brute_force():
+    rng = np.random.default_rng(30)
+    q, k, v = (rng.standard_normal((1, 2, 7 * 64, 8)).astype(np.float16) for _ in range(3))
+    counts = np.array([64, 10, 64, 33, 1, 64, 50])
+    oc = coarse_attention(q, k, v, 64, 0.7, valid=counts)
     for h in range(2):
-        for i in range(16):
-            srt = np.sort(exact[h, i])[::-1]
-            margin = srt[19] - srt[20]
-            bound = 1e-5 * np.abs(qd[h, i]) @ np.abs(kd[h]).max(axis=0)
-            if margin > 4 * bound:
-                want = np.sort(np.argsort(-exact[h, i], kind="stable")[:20])
-                assert np.array_equal(idx[h, i], want)
-                checked += 1
-    assert checked >= 24
+        qm, km, vm = (pool_means_fp32(x[0, h], 64, counts) for x in (q, k, v))
+        assert np.allclose(oc[0, h], _brute_coarse(qm, km, vm, 0.7), rtol=1e-12, atol=1e-14)
+
+
+def test_coarse_attention_special_cases():
+    rng = np.random.default_rng(31)
+    q, k, v = (rng.standard_normal((1, 1, 5 * 64, 8)).astype(np.float16) for _ in range(3))
+    vm = pool_means_fp32(v[0, 0], 64).astype(np.float64)
+    # scale 0: uniform weights over all key cubes -> the mean of the pooled values
+    assert np.allclose(coarse_attention(q, k, v, 64, 0.0)[0, 0], vm.mean(axis=0)[None], atol=1e-15)
+    # constant values: every output is that constant
+    vc = np.full_like(v, 0.375)
+    assert np.allclose(coarse_attention(q, k, vc, 64, 0.9), 0.375, atol=1e-15)
+    # one key cube: the output is its pooled value
+    one = coarse_attention(q, k[:, :, :64], v[:, :, :64], 64, 0.9)
+    assert np.allclose(one[0, 0], np.broadcast_to(vm[0], (5, 8)), atol=1e-15)
+
+
+def test_gated_output_layout():
+    rng = np.random.default_rng(32)
+    prefix, nc, D = 64, 3, 4
+    S = prefix + nc * 64
+    fine = rng.standard_normal((1, 1, S, D))
+    counts = np.array([64, 20, 7])
+    for c in range(nc):
+        fine[:, :, prefix + c * 64 + counts[c]:prefix + (c + 1) * 64] = 0
+    oc = rng.standard_normal((1, 1, nc, D))
+    g = rng.standard_normal((1, 1, S, D))
+    o = gated_output(fine, oc, g, 64, counts, prefix)
+    assert np.array_equal(o[:, :, :prefix], fine[:, :, :prefix])
+    for c in range(nc):
+        r = prefix + c * 64
+        assert np.allclose(o[0, 0, r:r + counts[c]], fine[0, 0, r:r + counts[c]] +
+                           g[0, 0, r:r + counts[c]] * oc[0, 0, c], atol=0)
+        assert np.all(o[0, 0, r + counts[c]:r + 64] == 0)
+    assert np.array_equal(gated_output(fine, oc, np.zeros_like(g), 64, counts, prefix), fine)
+
+
+def test_planted_coarse_over_selected_cubes_only_is_caught():
+    rng = np.random.default_rng(33)
+    q, k, v = (rng.standard_normal((1, 1, 6 * 64, 8)).astype(np.float16) for _ in range(3))
+    oc = coarse_attention(q, k, v, 64, 0.5)
+    idx = vsa_select(q, k, 64, 2)
+    qm, km, vm = (pool_means_fp32(x[0, 0], 64) for x in (q, k, v))
+    wrong = np.array([_brute_coarse(qm[i:i + 1], km[idx[0, 0, i]], vm[idx[0, 0, i]], 0.5)[0]
+                      for i in range(6)])
+    assert not np.allclose(wrong, oc[0, 0], atol=1e-6)
 
 
 # ------------------------------------------------------------------ boundary cubes and prefix
-import math  # noqa: E402
-
-import pytest  # noqa: E402
-
 from oracle import attention as A  # noqa: E402
 
 
