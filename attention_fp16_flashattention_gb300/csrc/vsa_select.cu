@@ -3,23 +3,28 @@
 // minimax_h3_fusions/query_pool.py and key_quant.py: FP32 tile means = FP32 sum
 // divided by the token count).
 //
-// Two kernels:
+// Four kernels, each launched as a programmatic dependent of the one before:
 //  1. vsa_pool_kernel: FP32 cube means of Q and K.  Each thread owns 8
 //     consecutive channels of one cube and adds the cube's real tokens (all 64,
 //     or the first valid-count slots of a boundary cube) in token order with
 //     FP32 rounding after every addition, then divides by the count (correctly
 //     rounded).  Video tokens start after `prefix` prefix tokens, which take no
-//     part.  HBM-bound: Q and K are read once with 16-byte loads.
-//  2. vsa_score_topk_kernel: 16 query cubes per CTA against all key cubes,
-//     register-tiled (1 query x 4 keys per thread) with operands staged
-//     d-major in shared memory.  Every score is an FP32 sum over d = 0..D-1, in
-//     order, of FP32 products (no fused multiply-add, so both the product and the
-//     sum are rounded).  The k-th largest score of a row is found with a 32-step
-//     bitwise search on order-preserving integer keys; equal scores at the
-//     threshold are taken from the lowest cube index up; the selection is
-//     written in ascending cube order.
+//     part.  HBM-bound: Q and K are read once with 16-byte loads.  It also
+//     writes each mean's Euclidean norm.
+//  2. vsa_score_kernel: FP32 scores of every (query cube, key cube) pair, a
+//     batched FFMA matrix product in 128 x 128 tiles.
+//  3. vsa_topk_kernel: the selection ranks key cubes by the EXACT dot product
+//     of the FP32 means.  One warp per query cube: the FP32 scores with a
+//     rigorous error bound decide almost every key; the few keys whose FP32
+//     score lies too close to the k-th value are ranked by exact integer scores
+//     (limbs of the means on their 2^-53 grid).  Ties go to the lower cube
+//     index; the selection is written in ascending cube order.
+//  4. the same kernel in its fallback form: rows with more undecided keys than
+//     one warp's in-place buffer holds (many equal scores) are ranked the same
+//     way with room for every key.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "host.h"
@@ -34,9 +39,12 @@ constexpr int kMaxChunks = 32;      // 32-key chunks per row: supports up to 102
 __global__ void __launch_bounds__(kPoolThreads) vsa_pool_kernel(
     const __half* __restrict__ q, const __half* __restrict__ k, long long n_bh, int n_cubes,
     long long seq, int prefix, int D, int block, const int32_t* __restrict__ cube_valid,
-    uint32_t* status, float* __restrict__ qm, float* __restrict__ km) {
+    uint32_t* status, float* __restrict__ qm, float* __restrict__ km, float* __restrict__ qn,
+    float* __restrict__ kn) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // score kernel may be placed
     const __half* x = blockIdx.y == 0 ? q : k;
     float* out = blockIdx.y == 0 ? qm : km;
+    float* out_n = blockIdx.y == 0 ? qn : kn;
     const int groups = D >> 3;   // 8 channels per thread
     const long long gid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     if (gid >= n_bh * n_cubes * groups) return;
@@ -88,166 +96,602 @@ __global__ void __launch_bounds__(kPoolThreads) vsa_pool_kernel(
     float4* dst = reinterpret_cast<float4*>(out + cube * D + g * 8);
     dst[0] = lo;
     dst[1] = hi;
+    // Euclidean norm of the cube mean (it scales the score error bound): the
+    // cube's 16 channel groups are 16 aligned lanes of one warp.
+    float n2 = lo.x * lo.x + lo.y * lo.y + lo.z * lo.z + lo.w * lo.w + hi.x * hi.x + hi.y * hi.y +
+               hi.z * hi.z + hi.w * hi.w;
+    const unsigned grp = 0xFFFFu << (threadIdx.x & 16u);
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) n2 += __shfl_xor_sync(grp, n2, off);
+    if (g == 0) out_n[cube] = sqrtf(n2);
 }
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-
-constexpr int kSelQ = 16;        // query cubes per CTA (about 75 KB of shared memory: 3 CTAs per SM)
-constexpr int kSelKB = 64;       // key cubes per staged block
-constexpr int kSelThreads = 256;
-constexpr int kSelD = 128;
-
-constexpr size_t sel_smem_bytes(int NC) {
-    return (static_cast<size_t>(kSelD) * kSelQ + static_cast<size_t>(kSelD) * (kSelKB + 4) +
-            static_cast<size_t>(kSelQ) * (NC + 1)) * sizeof(float);
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// grid: (ceil(NC / kSelQ), B*H); block: kSelThreads; dynamic smem sel_smem_bytes(NC).
-// Scores for 16 query cubes x all NC key cubes, each an FP32 sum over d in order of
-// FP32 products (no FMA): thread (ty, tx) accumulates query ty against keys
-// 4tx..4tx+3 of each 64-key block with both operands staged d-major.  Then each
-// warp selects the top-k of two query rows; CH = 32-key chunks per row.
-template <int CH>
-__global__ void __launch_bounds__(kSelThreads) vsa_score_topk_kernel(
-    const float* __restrict__ qm, const float* __restrict__ km, int NC, int topk,
-    int32_t* __restrict__ idx) {
-    extern __shared__ float sm[];
-    float* sq = sm;                                   // [D][kSelQ]
-    float* sk = sq + kSelD * kSelQ;                   // [D][kSelKB + 4]
-    float* ss = sk + kSelD * (kSelKB + 4);            // [kSelQ][NC + 1]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.y, q0 = blockIdx.x * kSelQ;
-    const float* qbase = qm + static_cast<long long>(bh) * NC * kSelD;
-    const float* kbase = km + static_cast<long long>(bh) * NC * kSelD;
-    const int SK = kSelKB + 4, SS = NC + 1;
-    // Stage Q (32 x 128) d-major: every thread issues its four 16-byte loads first.
-    {
-        float4 v[kSelQ * kSelD / 4 / kSelThreads];
-#pragma unroll
-        for (int r = 0; r < kSelQ * kSelD / 4 / kSelThreads; ++r) {
-            const int i = tid + r * kSelThreads, q = i / (kSelD / 4), d4 = i % (kSelD / 4);
-            v[r] = (q0 + q < NC) ? *reinterpret_cast<const float4*>(qbase + static_cast<long long>(q0 + q) * kSelD + 4 * d4)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int r = 0; r < kSelQ * kSelD / 4 / kSelThreads; ++r) {
-            const int i = tid + r * kSelThreads, q = i / (kSelD / 4), d4 = i % (kSelD / 4);
-            sq[(4 * d4 + 0) * kSelQ + q] = v[r].x;
-            sq[(4 * d4 + 1) * kSelQ + q] = v[r].y;
-            sq[(4 * d4 + 2) * kSelQ + q] = v[r].z;
-            sq[(4 * d4 + 3) * kSelQ + q] = v[r].w;
-        }
-    }
-    const int ty = tid >> 4, tx = tid & 15;
-    // Key staging: lane = key (32 keys per warp), each lane one 32-byte sector of
-    // 8 consecutive dims per item, so the d-major stores of a warp fill 32
-    // consecutive words of one row (no bank conflicts) and every sector loaded
-    // is used whole.  Warp w takes keys 32*(w&1) .. +31 and dim groups (w>>1) + 4r.
-    const int sk_key = lane + 32 * (warp & 1), sk_g0 = warp >> 1;
-    constexpr int kItems = kSelKB * kSelD / 8 / kSelThreads;   // 4
-    for (int kb = 0; kb < NC; kb += kSelKB) {
-        float4 v[2 * kItems];
-        const bool live = kb + sk_key < NC;
-        const float* krow = kbase + static_cast<long long>(kb + sk_key) * kSelD;
-#pragma unroll
-        for (int r = 0; r < kItems; ++r) {
-            const int g = sk_g0 + 4 * r;   // dims 8g .. 8g+7
-            v[2 * r] = live ? *reinterpret_cast<const float4*>(krow + 8 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[2 * r + 1] = live ? *reinterpret_cast<const float4*>(krow + 8 * g + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < kItems; ++r) {
-            const int g = sk_g0 + 4 * r;
-            float* col = sk + (8 * g) * SK + sk_key;
-            col[0 * SK] = v[2 * r].x;
-            col[1 * SK] = v[2 * r].y;
-            col[2 * SK] = v[2 * r].z;
-            col[3 * SK] = v[2 * r].w;
-            col[4 * SK] = v[2 * r + 1].x;
-            col[5 * SK] = v[2 * r + 1].y;
-            col[6 * SK] = v[2 * r + 1].z;
-            col[7 * SK] = v[2 * r + 1].w;
-        }
-        __syncthreads();
-        float acc[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j] = 0.0f;
-#pragma unroll 8
-        for (int d = 0; d < kSelD; ++d) {
-            const float qv = sq[d * kSelQ + ty];
-            const float4 kv = *reinterpret_cast<const float4*>(sk + d * SK + 4 * tx);
-            acc[0] = __fadd_rn(acc[0], __fmul_rn(qv, kv.x));
-            acc[1] = __fadd_rn(acc[1], __fmul_rn(qv, kv.y));
-            acc[2] = __fadd_rn(acc[2], __fmul_rn(qv, kv.z));
-            acc[3] = __fadd_rn(acc[3], __fmul_rn(qv, kv.w));
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (kb + 4 * tx + j < NC) ss[ty * SS + kb + 4 * tx + j] = acc[j];
-    }
-    __syncthreads();
+// ---------------------------------------------------------------- exact scores
+//
+// Cube means of FP16 data are integer multiples of 2^-53 below 2^16 in
+// magnitude (an FP32 sum of FP16 values stays on the 2^-24 grid; a nonzero sum
+// over at most 64 tokens divided by the count is at least 2^-30, whose 24-bit
+// significand ends at 2^-53 or above).  So M = x * 2^53 is an integer below
+// 2^69, three signed 23-bit limbs, and sum_d Mq[d] Mk[d] -- the score times
+// 2^106 -- is an integer formed exactly from int64 sums of limb products
+// (each below 2^46; 128 dims x 3 products per position stay below 2^55).
 
-    // Top-k: warp w owns query rows 2w, 2w+1.  Key c*32 + lane -> key[c].
-    const int nchunks = (NC + 31) / 32;
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int r = 0; r < kSelQ / (kSelThreads / 32); ++r) {
-        const int ql = warp * (kSelQ / (kSelThreads / 32)) + r;
-        const int qc = q0 + ql;
-        if (qc >= NC) break;
-        uint32_t key[CH];
+constexpr uint32_t kLimbMask = (1u << 23) - 1u;
+
+struct ExactScore {
+    long long top;            // sign-carrying leading digit (weight 2^92)
+    unsigned long long mid;   // digits of weight 2^69, 2^46 (23 bits each)
+    unsigned long long low;   // digits of weight 2^23, 2^0
+};
+
+__device__ __forceinline__ bool exact_greater(const ExactScore& a, const ExactScore& b) {
+    if (a.top != b.top) return a.top > b.top;
+    if (a.mid != b.mid) return a.mid > b.mid;
+    return a.low > b.low;
+}
+__device__ __forceinline__ bool exact_equal(const ExactScore& a, const ExactScore& b) {
+    return a.top == b.top && a.mid == b.mid && a.low == b.low;
+}
+
+// The three limbs of x * 2^53 with x's sign.  Values off the grid (impossible
+// for cube means of FP16 data) lose their bits below 2^-53; non-finite values
+// count as 0 (their selection is unspecified, but stays a valid index list).
+__device__ __forceinline__ void grid_limbs(float x, int& a0, int& a1, int& a2) {
+    const uint32_t u = __float_as_uint(x);
+    const int E = static_cast<int>((u >> 23) & 0xFFu);
+    const uint32_t m = E == 255 ? 0u : ((u & 0x7FFFFFu) | (E ? 0x800000u : 0u));
+    const int sh = (E ? E : 1) - 150 + 53;   // |x| * 2^53 = m * 2^sh
+    auto limb = [&](int s) -> int {
+        if (s >= 23 || s <= -32) return 0;
+        const uint64_t v = s >= 0 ? (static_cast<uint64_t>(m) << s) : static_cast<uint64_t>(m >> -s);
+        return static_cast<int>(v & kLimbMask);
+    };
+    const int sg = (u >> 31) ? -1 : 1;
+    a0 = sg * limb(sh);
+    a1 = sg * limb(sh - 23);
+    a2 = sg * limb(sh - 46);
+}
+
+// Exact score of one query row against key row `krow` (128 FP32 means in global
+// memory), by the whole warp: lane l takes dims 4l..4l+3, whose query limbs it
+// holds in qa.  Every lane returns the same value.
+__device__ __forceinline__ ExactScore exact_score_warp(const int (&qa)[4][3], const float* krow) {
+    const int lane = threadIdx.x & 31;
+    const float4 kv = *reinterpret_cast<const float4*>(krow + 4 * lane);
+    const float kf[4] = {kv.x, kv.y, kv.z, kv.w};
+    long long c[5] = {0, 0, 0, 0, 0};
 #pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const int kc = c * 32 + lane;
-            key[c] = (c < nchunks && kc < NC) ? order_key(ss[ql * SS + kc]) : 0u;   // 0: below any score
-        }
-        // Threshold: the largest T such that at least topk keys are >= T.
-        uint32_t T = 0;
+    for (int e = 0; e < 4; ++e) {
+        int b0, b1, b2;
+        grid_limbs(kf[e], b0, b1, b2);
+        c[0] += static_cast<long long>(qa[e][0]) * b0;
+        c[1] += static_cast<long long>(qa[e][0]) * b1 + static_cast<long long>(qa[e][1]) * b0;
+        c[2] += static_cast<long long>(qa[e][0]) * b2 + static_cast<long long>(qa[e][1]) * b1 +
+                static_cast<long long>(qa[e][2]) * b0;
+        c[3] += static_cast<long long>(qa[e][1]) * b2 + static_cast<long long>(qa[e][2]) * b1;
+        c[4] += static_cast<long long>(qa[e][2]) * b2;
+    }
+#pragma unroll
+    for (int p = 0; p < 5; ++p)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) c[p] += __shfl_xor_sync(0xffffffffu, c[p], off);
+    // carry into 23-bit digits (arithmetic shifts are floor divisions)
+    long long t = c[0];
+    const unsigned long long d0 = static_cast<unsigned long long>(t) & kLimbMask;
+    t = (t >> 23) + c[1];
+    const unsigned long long d1 = static_cast<unsigned long long>(t) & kLimbMask;
+    t = (t >> 23) + c[2];
+    const unsigned long long d2 = static_cast<unsigned long long>(t) & kLimbMask;
+    t = (t >> 23) + c[3];
+    const unsigned long long d3 = static_cast<unsigned long long>(t) & kLimbMask;
+    ExactScore r;
+    r.top = (t >> 23) + c[4];
+    r.mid = (d3 << 23) | d2;
+    r.low = (d1 << 23) | d0;
+    return r;
+}
+
+// Candidate buffer of one warp: the keys whose place around the k-th score the
+// FP32 scores cannot decide, with their exact scores, and the chosen keys as
+// bits (at most 1024 keys).
+template <int CAP>
+struct Cands {
+    long long top[CAP];
+    unsigned long long mid[CAP];
+    unsigned long long low[CAP];
+    int key[CAP];
+    uint32_t chosen[32];
+    uint32_t hist[256];   // selection histogram
+    uint32_t list[32];    // keys of the bucket holding the k-th key
+};
+
+// ---------------------------------------------------------------- row selection
+//
+// One warp selects the topk keys of one query row (key c*32 + lane in chunk c).
+// Scores s are FP32 with |s - exact| <= e for every key (e covers the FP32
+// evaluation error of the dot product).  With s_k and s_k1 the k-th and
+// (k+1)-th largest FP32 scores, a key with s < s_k - 2e is below k keys
+// whose exact scores are all >= s_k - e (certainly out), and a key with
+// s > s_k1 + 2e lies above the exact (k+1)-th score (certainly in).  The keys
+// left between are ranked by their exact scores, ties to the lower index.
+template <int CH>
+struct RowClass {
+    uint32_t in_m[CH];    // ballot masks per chunk
+    uint32_t unc_m[CH];
+    int n_in, n_unc;
+};
+
+// The k-th largest of the row's order keys by radix selection: four passes
+// over 8-bit digits from the top, each a histogram of the keys that match the
+// digits chosen so far, then a suffix scan over the 256 bins (8 per lane) for
+// the digit holding the k-th key.
+template <int CH>
+__device__ __forceinline__ uint32_t kth_largest_key(const uint32_t (&key)[CH], const bool (&live)[CH],
+                                                    int k, uint32_t* hist) {
+    const int lane = threadIdx.x & 31;
+    uint32_t prefix = 0, pmask = 0;
 #pragma unroll 1
-        for (int bit = 31; bit >= 0; --bit) {
-            const uint32_t cand = T | (1u << bit);
-            int cnt = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
 #pragma unroll
-            for (int c = 0; c < CH; ++c) cnt += (c < nchunks && key[c] >= cand) ? 1 : 0;
-            cnt = __reduce_add_sync(0xffffffffu, cnt);
-            if (cnt >= topk) T = cand;
+        for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0u;
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+            if (live[c] && (key[c] & pmask) == prefix) atomicAdd(&hist[(key[c] >> shift) & 0xFFu], 1u);
+        __syncwarp();
+        const uint4 b0 = *reinterpret_cast<const uint4*>(hist + lane * 8);
+        const uint4 b1 = *reinterpret_cast<const uint4*>(hist + lane * 8 + 4);
+        const uint32_t bins[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        uint32_t mine = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mine += bins[i];
+        uint32_t suf = mine;   // keys in lanes >= this lane (digits >= 8 * lane)
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, suf, off);
+            if (lane + off < 32) suf += y;
         }
-        int greater = 0;
+        const uint32_t hit = __ballot_sync(0xffffffffu, suf >= static_cast<uint32_t>(k));
+        const int L = 31 - __clz(hit);   // the highest lane whose suffix still holds k keys
+        uint32_t above = __shfl_sync(0xffffffffu, suf - mine, L);   // keys in higher lanes
+        int digit = 0;
+        uint32_t gt = 0;
+        if (lane == L) {
+            uint32_t run = above;
+            bool found = false;
 #pragma unroll
-        for (int c = 0; c < CH; ++c) greater += (c < nchunks && key[c] > T) ? 1 : 0;
-        greater = __reduce_add_sync(0xffffffffu, greater);
-        int need = topk - greater;            // equal-to-threshold scores still to take
-        int32_t* out = idx + (static_cast<long long>(bh) * NC + qc) * topk;
-        int base = 0;
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            if (c < nchunks) {
-                const bool valid = c * 32 + lane < NC;
-                const bool eq = valid && key[c] == T;
-                const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
-                const int take = min(need, __popc(eqm));
-                const bool sel = valid && (key[c] > T || (eq && __popc(eqm & lt) < take));
-                need -= take;
-                const uint32_t selm = __ballot_sync(0xffffffffu, sel);
-                if (sel) out[base + __popc(selm & lt)] = c * 32 + lane;
-                base += __popc(selm);
+            for (int i = 7; i >= 0; --i) {
+                if (!found && run + bins[i] >= static_cast<uint32_t>(k)) {
+                    digit = 8 * lane + i;
+                    gt = run;
+                    found = true;
+                }
+                run += bins[i];
             }
         }
+        digit = __shfl_sync(0xffffffffu, digit, L);
+        gt = __shfl_sync(0xffffffffu, gt, L);
+        prefix |= static_cast<uint32_t>(digit) << shift;
+        pmask |= 0xFFu << shift;
+        k -= static_cast<int>(gt);
+        __syncwarp();
+    }
+    return prefix;
+}
+
+// The k-th largest order key in one histogram pass when the scores are spread
+// out: 256 equal buckets between the row's smallest and largest FP32 score
+// (bucket = floor((s - min) * 256 / (max - min)), a non-decreasing function of
+// s, so the buckets are in score order), a suffix scan over the buckets finds
+// the one holding the k-th key, and if it holds at most 32 keys they are
+// ranked directly.  Otherwise (many equal or clustered scores, or non-finite
+// ones) the radix selection decides.
+template <int CH>
+__device__ __forceinline__ uint32_t kth_largest_key_fast(const float (&s)[CH], const uint32_t (&key)[CH],
+                                                         const bool (&live)[CH], int k,
+                                                         uint32_t* hist, uint32_t* list) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+    for (int c = 0; c < CH; ++c)
+        if (live[c]) {
+            kmin = min(kmin, key[c]);
+            kmax = max(kmax, key[c]);
+        }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    const float smin = key_float(kmin), smax = key_float(kmax);
+    const float inv = 256.0f / (smax - smin);
+    if (!(inv <= 3.0e38f)) return kth_largest_key<CH>(key, live, k, hist);   // equal, inf or nan
+    auto bucket_of = [&](float x) { return min(255, __float2int_rz((x - smin) * inv)); };
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < CH; ++c)
+        if (live[c]) atomicAdd(&hist[bucket_of(s[c])], 1u);
+    __syncwarp();
+    const uint4 b0 = *reinterpret_cast<const uint4*>(hist + lane * 8);
+    const uint4 b1 = *reinterpret_cast<const uint4*>(hist + lane * 8 + 4);
+    const uint32_t bins[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    uint32_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mine += bins[i];
+    uint32_t suf = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, suf, off);
+        if (lane + off < 32) suf += y;
+    }
+    const uint32_t hit = __ballot_sync(0xffffffffu, suf >= static_cast<uint32_t>(k));
+    const int L = 31 - __clz(hit);
+    const uint32_t above = __shfl_sync(0xffffffffu, suf - mine, L);
+    int bucket = 0;
+    uint32_t gt = 0, nb = 0;
+    if (lane == L) {
+        uint32_t run = above;
+        bool found = false;
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+            if (!found && run + bins[i] >= static_cast<uint32_t>(k)) {
+                bucket = 8 * lane + i;
+                gt = run;
+                nb = bins[i];
+                found = true;
+            }
+            run += bins[i];
+        }
+    }
+    bucket = __shfl_sync(0xffffffffu, bucket, L);
+    gt = __shfl_sync(0xffffffffu, gt, L);
+    nb = __shfl_sync(0xffffffffu, nb, L);
+    __syncwarp();
+    if (nb > 32) return kth_largest_key<CH>(key, live, k, hist);
+    // the bucket's keys, then the one with rank k - gt among them (ties counted)
+    int base = 0;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const bool in = live[c] && bucket_of(s[c]) == bucket;
+        const uint32_t m = __ballot_sync(0xffffffffu, in);
+        if (in) list[base + __popc(m & lt)] = key[c];
+        base += __popc(m);
+    }
+    __syncwarp();
+    const int kk = k - static_cast<int>(gt);
+    const uint32_t mykey = lane < static_cast<int>(nb) ? list[lane] : 0u;
+    int greater = 0, equal = 0;
+    for (int j = 0; j < static_cast<int>(nb); ++j) {
+        const uint32_t v = list[j];
+        greater += v > mykey ? 1 : 0;
+        equal += v == mykey ? 1 : 0;
+    }
+    const bool is_kth = lane < static_cast<int>(nb) && greater < kk && kk <= greater + equal;
+    const uint32_t who = __ballot_sync(0xffffffffu, is_kth);
+    const uint32_t T = __shfl_sync(0xffffffffu, mykey, __ffs(who) - 1);
+    __syncwarp();
+    return T;
+}
+
+template <int CH>
+__device__ __forceinline__ void classify_row(const float (&s)[CH], int NC, int topk, float e,
+                                             RowClass<CH>& rc, uint32_t* hist, uint32_t* list) {
+    const int lane = threadIdx.x & 31;
+    const int nchunks = (NC + 31) / 32;
+    uint32_t key[CH];
+    bool live[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        live[c] = c < nchunks && c * 32 + lane < NC;
+        key[c] = live[c] ? order_key(s[c]) : 0u;
+    }
+    const uint32_t T = kth_largest_key_fast<CH>(s, key, live, topk, hist, list);
+    int ge = 0;
+    uint32_t below = 0;   // largest key value under T
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        if (live[c]) {
+            ge += key[c] >= T ? 1 : 0;
+            if (key[c] < T) below = max(below, key[c]);
+        }
+    }
+    ge = __reduce_add_sync(0xffffffffu, ge);
+    below = __reduce_max_sync(0xffffffffu, below);
+    const uint32_t T1 = ge > topk ? T : below;          // the (k+1)-th largest key
+    const float e2 = __fmul_ru(2.0f, e);
+    const float thr_out = __fsub_rd(key_float(T), e2);
+    const float thr_in = __fadd_ru(key_float(T1), e2);
+    int n_in = 0, n_unc = 0;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const bool in = live[c] && s[c] > thr_in;
+        const bool unc = live[c] && !in && !(s[c] < thr_out);
+        rc.in_m[c] = __ballot_sync(0xffffffffu, in);
+        rc.unc_m[c] = __ballot_sync(0xffffffffu, unc);
+        n_in += __popc(rc.in_m[c]);
+        n_unc += __popc(rc.unc_m[c]);
+    }
+    rc.n_in = n_in;
+    rc.n_unc = n_unc;
+}
+
+// Ranks the uncertain keys of a row by exact score and marks the best `need`
+// in cb->chosen.  q_at(d) gives the row's query mean at dim d; kbase points at
+// the key means of the head ([NC][128]).
+template <int CH, int CAP, typename QAt>
+__device__ __forceinline__ void resolve_exact(const RowClass<CH>& rc, int need, QAt q_at,
+                                              const float* kbase, Cands<CAP>* cb) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
+    int base = 0;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const uint32_t m = rc.unc_m[c];
+        if ((m >> lane) & 1u) cb->key[base + __popc(m & lt)] = c * 32 + lane;
+        base += __popc(m);
+    }
+    cb->chosen[lane] = 0u;
+    int qa[4][3];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) grid_limbs(q_at(4 * lane + e), qa[e][0], qa[e][1], qa[e][2]);
+    __syncwarp();
+    for (int i = 0; i < rc.n_unc; ++i) {
+        const ExactScore x = exact_score_warp(qa, kbase + static_cast<long long>(cb->key[i]) * 128);
+        if (lane == 0) {
+            cb->top[i] = x.top;
+            cb->mid[i] = x.mid;
+            cb->low[i] = x.low;
+        }
+    }
+    __syncwarp();
+    for (int i = lane; i < rc.n_unc; i += 32) {
+        const ExactScore xi{cb->top[i], cb->mid[i], cb->low[i]};
+        const int ki = cb->key[i];
+        int rank = 0;
+        for (int v = 0; v < rc.n_unc; ++v) {
+            const ExactScore xv{cb->top[v], cb->mid[v], cb->low[v]};
+            rank += (exact_greater(xv, xi) || (exact_equal(xv, xi) && cb->key[v] < ki)) ? 1 : 0;
+        }
+        if (rank < need) atomicOr(&cb->chosen[ki >> 5], 1u << (ki & 31));
+    }
+    __syncwarp();
+}
+
+// Writes the row's selection (certainly-in keys plus the chosen uncertain keys)
+// in ascending key order.
+template <int CH, int CAP>
+__device__ __forceinline__ void write_row(const RowClass<CH>& rc, const Cands<CAP>* cb, bool use_chosen,
+                                          int NC, int topk, int32_t* out, uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
+    const int nchunks = (NC + 31) / 32;
+    int base = 0;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        if (c < nchunks) {
+            const bool sel = ((rc.in_m[c] >> lane) & 1u) ||
+                             (use_chosen && ((cb->chosen[c] >> lane) & 1u));
+            const uint32_t m = __ballot_sync(0xffffffffu, sel);
+            const int p = base + __popc(m & lt);
+            if (sel && p < topk) out[p] = c * 32 + lane;
+            base += __popc(m);
+        }
+    }
+    if (base != topk && lane == 0) atomicOr(status, kDevBadIndex);   // never for finite inputs
+}
+
+// ---------------------------------------------------------------- score kernel
+//
+// Batched FP32 product S[bh] = Qm[bh] Km[bh]^T of the cube means ([NC][128]
+// each), one 128 x 128 tile of S per CTA.  256 threads, each an 8 x 8 register
+// tile (rows 4ty.., 64+4ty.., columns 4tx.., 64+4tx..); the two operand tiles
+// pass through shared memory eight dims at a time, stored dim-major so that
+// every operand read is a 16-byte load, with the next eight dims loaded into
+// registers (one 16-byte load per operand per thread) while the current ones
+// are multiplied.  Every score is a sequence of FFMAs over d = 0..127.
+// (Two CTAs fit on an SM.  A 4 x 8 thread tile with three CTAs per SM, for
+// fewer idle SMs in the last wave, measured slower: 54 against 47 us.)
+constexpr int kGT = 128;          // tile edge (query cubes x key cubes)
+constexpr int kGK = 8;            // dims per stage
+constexpr int kGThreads = 256;
+constexpr int kGP = kGT + 4;      // shared-memory pitch (conflict-free transposing stores)
+constexpr int kSelD = 128;
+
+__host__ __device__ constexpr int score_ld(int NC) { return (NC + kGT - 1) / kGT * kGT; }
+
+__global__ void __launch_bounds__(kGThreads, 2) vsa_score_kernel(const float* __restrict__ qm,
+                                                                 const float* __restrict__ km,
+                                                                 int NC, float* __restrict__ S) {
+    __shared__ __align__(16) float As[2][kGK][kGP];
+    __shared__ __align__(16) float Bs[2][kGK][kGP];
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the means come from the pool kernel
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int t = threadIdx.x;
+    const long long bh = blockIdx.z;
+    const int m0 = blockIdx.y * kGT, n0 = blockIdx.x * kGT;
+    const int LD = score_ld(NC);
+    const float* A = qm + bh * NC * kSelD;
+    const float* B = km + bh * NC * kSelD;
+    const int lr = t >> 1, lk = (t & 1) * 4;   // staging: row lr, dims lk..lk+3 of a stage
+    const bool a_live = m0 + lr < NC, b_live = n0 + lr < NC;
+    const float* a_src = A + static_cast<long long>(m0 + lr) * kSelD + lk;
+    const float* b_src = B + static_cast<long long>(n0 + lr) * kSelD + lk;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 ra = a_live ? *reinterpret_cast<const float4*>(a_src) : zero;
+    float4 rb = b_live ? *reinterpret_cast<const float4*>(b_src) : zero;
+    auto stage = [&](int buf) {
+        As[buf][lk + 0][lr] = ra.x; As[buf][lk + 1][lr] = ra.y;
+        As[buf][lk + 2][lr] = ra.z; As[buf][lk + 3][lr] = ra.w;
+        Bs[buf][lk + 0][lr] = rb.x; Bs[buf][lk + 1][lr] = rb.y;
+        Bs[buf][lk + 2][lr] = rb.z; Bs[buf][lk + 3][lr] = rb.w;
+    };
+    stage(0);
+    __syncthreads();
+    const int ty = t >> 4, tx = t & 15;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    constexpr int NCH = kSelD / kGK;
+#pragma unroll 1
+    for (int ch = 0; ch < NCH; ++ch) {
+        const int buf = ch & 1;
+        if (ch + 1 < NCH) {
+            ra = a_live ? *reinterpret_cast<const float4*>(a_src + (ch + 1) * kGK) : zero;
+            rb = b_live ? *reinterpret_cast<const float4*>(b_src + (ch + 1) * kGK) : zero;
+        }
+#pragma unroll
+        for (int kk = 0; kk < kGK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + 4 * ty]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + 4 * tx]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        if (ch + 1 < NCH) stage(buf ^ 1);
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = m0 + (i < 4 ? 4 * ty + i : 64 + 4 * ty + i - 4);
+        if (row >= NC) continue;
+        float* dst = S + (bh * NC + row) * LD + n0;
+        *reinterpret_cast<float4*>(dst + 4 * tx) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        *reinterpret_cast<float4*>(dst + 64 + 4 * tx) =
+            make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
     }
 }
+
+// ---------------------------------------------------------------- top-k kernels
+//
+// One warp per query row reads the row's FP32 scores and the cube norms, finds
+// the k-th / (k+1)-th values by radix selection, classifies every key against
+// the error bound and ranks the undecided ones by exact score.  The FP32 score
+// of two 128-dim vectors (FFMA, any order; the means' grid keeps every partial
+// sum on 2^-106 Z, so nothing underflows) is within gamma_128 sum|q||k| <=
+// 2^-17 (1 + 2^-16) |q| |k| of the exact one; the norms are FP32 too, within
+// 2^-17 relative, and e = 2^-15 |q^| max|k^| bounds the error with a factor of
+// about 4 to spare.
+// The main kernel (kTopkWarps warps per CTA, one row each) leaves rows with more
+// than kCap undecided keys to the fallback kernel (kFbWarps warps per CTA,
+// grid-stride over rows, room for every key of a row).
+constexpr int kCap = 32;
+constexpr int kTopkWarps = 8;
+constexpr int kFbWarps = 2;
+constexpr float kErrScale = 1.0f / 32768.0f;
+
+template <int CH, int CAP, bool FALLBACK>
+__global__ void __launch_bounds__(FALLBACK ? kFbWarps * 32 : kTopkWarps * 32, FALLBACK ? 1 : (CH > 16 ? 2 : 3)) vsa_topk_kernel(
+    const float* __restrict__ S, const float* __restrict__ qm, const float* __restrict__ km,
+    const float* __restrict__ qn, const float* __restrict__ kn, int NC, int topk, long long rows,
+    int32_t* __restrict__ deferred, int32_t* __restrict__ idx, uint32_t* status) {
+    extern __shared__ __align__(16) uint8_t topk_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kWarps = FALLBACK ? kFbWarps : kTopkWarps;
+    Cands<CAP>* cb = reinterpret_cast<Cands<CAP>*>(topk_smem) + warp;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // scores (and flags) of the kernel before
+    if (!FALLBACK) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int LD = score_ld(NC);
+    // main form: one row per warp; fallback form: warps stride over groups of 32
+    // rows, each lane loading one row's flag, and visit the flagged rows
+    const long long first = FALLBACK ? (static_cast<long long>(blockIdx.x) * kWarps + warp) * 32
+                                     : static_cast<long long>(blockIdx.x) * kWarps + warp;
+    const long long stride = FALLBACK ? static_cast<long long>(gridDim.x) * kWarps * 32 : rows;
+    for (long long base = first; base < rows; base += stride) {
+        uint32_t todo = 1u;
+        if (FALLBACK) {
+            const long long r = base + lane;
+            todo = __ballot_sync(0xffffffffu, r < rows && deferred[r] != 0);
+        }
+        for (; todo; todo &= todo - 1) {
+        const long long row = FALLBACK ? base + __ffs(todo) - 1 : base;
+        const long long bh = row / NC;
+        int32_t* out = idx + row * topk;
+        RowClass<CH> rc;
+        if (topk >= NC) {   // every key
+#pragma unroll
+            for (int c = 0; c < CH; ++c) rc.in_m[c] = __ballot_sync(0xffffffffu, c * 32 + lane < NC);
+            if (!FALLBACK && lane == 0) deferred[row] = 0;
+            write_row<CH, CAP>(rc, cb, false, NC, topk, out, status);
+            continue;
+        }
+        const float* srow = S + row * LD;
+        const float* nkh = kn + bh * NC;
+        float s[CH];
+        float nkmax = 0.0f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const bool live = c * 32 + lane < NC;
+            s[c] = live ? srow[c * 32 + lane] : 0.0f;
+            if (live) nkmax = fmaxf(nkmax, nkh[c * 32 + lane]);
+        }
+        nkmax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(nkmax)));   // >= 0
+        const float e = __fmul_ru(__fmul_ru(qn[row], nkmax), kErrScale);
+        classify_row<CH>(s, NC, topk, e, rc, cb->hist, cb->list);
+        const int need = topk - rc.n_in;
+        if (!FALLBACK && need > 0 && rc.n_unc > CAP) {   // left to the fallback kernel
+            if (lane == 0) deferred[row] = 1;
+            continue;
+        }
+        if (need > 0) {
+            const float* qrow = qm + row * kSelD;
+            resolve_exact<CH, CAP>(rc, need, [&](int d) { return qrow[d]; }, km + bh * NC * kSelD, cb);
+        }
+        if (!FALLBACK && lane == 0) deferred[row] = 0;
+        write_row<CH, CAP>(rc, cb, need > 0, NC, topk, out, status);
+        __syncwarp();
+        }
+    }
+}
+
+template <int CH, int CAP, int WARPS>
+constexpr size_t topk_smem_bytes() { return sizeof(Cands<CAP>) * WARPS; }
 
 }  // namespace
 }  // namespace gbattn
 
 using namespace gbattn;
 
+namespace {
+// Workspace of the selection, each part 256-byte aligned: FP32 cube means of Q
+// and K [rows][D], their norms [rows], one int32 "left to the fallback" flag per
+// row, and the FP32 scores [rows][score_ld(NC)] (rows = B*H*NC query cubes).
+struct SelectLayout {
+    size_t qm, km, qn, kn, flags, scores, total;
+};
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+SelectLayout select_layout(size_t rows, int NC, int D) {
+    SelectLayout L;
+    L.qm = 0;
+    L.km = L.qm + align256(rows * D * sizeof(float));
+    L.qn = L.km + align256(rows * D * sizeof(float));
+    L.kn = L.qn + align256(rows * sizeof(float));
+    L.flags = L.kn + align256(rows * sizeof(float));
+    L.scores = L.flags + align256(rows * sizeof(int32_t));
+    L.total = L.scores + rows * static_cast<size_t>(score_ld(NC)) * sizeof(float);
+    return L;
+}
+}  // namespace
+
 extern "C" size_t vsa_select_workspace_size(int B, int H, int S, int D, int block) {
     if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return 0;
-    const size_t nc = static_cast<size_t>(S / block);
-    return 2 * static_cast<size_t>(B) * H * nc * D * sizeof(float);
+    const int nc = S / block;
+    return select_layout(static_cast<size_t>(B) * H * nc, nc, D).total;
 }
 
 extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D,
@@ -276,32 +720,96 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     DeviceState dev;
     int rc = current_device(&dev);
     if (rc != GBATTN_OK) return rc;
+    if (dev.device < 0 || dev.device >= 64) return GBATTN_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    float* qm = static_cast<float*>(workspace);
-    float* km = qm + static_cast<size_t>(B) * H * NC * D;
     const long long n_bh = static_cast<long long>(B) * H;
-    const long long pool_threads = n_bh * NC * (D / 8);
+    const long long rows = n_bh * NC;
+    const SelectLayout L = select_layout(static_cast<size_t>(rows), NC, D);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* qm = reinterpret_cast<float*>(ws + L.qm);
+    float* km = reinterpret_cast<float*>(ws + L.km);
+    float* qn = reinterpret_cast<float*>(ws + L.qn);
+    float* kn = reinterpret_cast<float*>(ws + L.kn);
+    int32_t* deferred = reinterpret_cast<int32_t*>(ws + L.flags);
+    float* scores = reinterpret_cast<float*>(ws + L.scores);
+
+    static std::once_flag attr_once[64];
+    static int attr_rc[64];
+    std::call_once(attr_once[dev.device], [&] {
+        bool ok = cudaFuncSetAttribute(vsa_topk_kernel<32, 1024, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(topk_smem_bytes<32, 1024, kFbWarps>())) ==
+                  cudaSuccess;
+        ok &= cudaFuncSetAttribute(vsa_topk_kernel<16, 512, true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(topk_smem_bytes<16, 512, kFbWarps>())) ==
+              cudaSuccess;
+        attr_rc[dev.device] = ok ? GBATTN_OK : GBATTN_ERR_CUDA;
+    });
+    if (attr_rc[dev.device] != GBATTN_OK) {
+        cudaGetLastError();
+        return GBATTN_ERR_CUDA;
+    }
+
+    const long long pool_threads = rows * (D / 8);
     dim3 pgrid(static_cast<unsigned>((pool_threads + kPoolThreads - 1) / kPoolThreads), 2);
     vsa_pool_kernel<<<pgrid, kPoolThreads, 0, s>>>(static_cast<const __half*>(q),
                                                    static_cast<const __half*>(k), n_bh, NC, S,
                                                    prefix, D, block, cube_valid, dev.status, qm,
-                                                   km);
-    static std::once_flag attr_once[64];
-    if (dev.device >= 0 && dev.device < 64)
-        std::call_once(attr_once[dev.device], [] {
-            cudaFuncSetAttribute(vsa_score_topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(sel_smem_bytes(16 * 32)));
-            cudaFuncSetAttribute(vsa_score_topk_kernel<kMaxChunks>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(sel_smem_bytes(kMaxChunks * 32)));
-        });
-    dim3 sgrid((NC + kSelQ - 1) / kSelQ, B * H);
-    if (NC <= 16 * 32)
-        vsa_score_topk_kernel<16><<<sgrid, kSelThreads, sel_smem_bytes(NC), s>>>(qm, km, NC, topk, idx);
-    else
-        vsa_score_topk_kernel<kMaxChunks><<<sgrid, kSelThreads, sel_smem_bytes(NC), s>>>(qm, km, NC, topk,
-                                                                                       idx);
-    count_launches(2);
+                                                   km, qn, kn);
+    count_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+
+    // The other three kernels are programmatic dependent launches: their CTAs
+    // are placed as the previous grid retires and wait (griddepcontrol.wait)
+    // for all of its results.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float *cqm = qm, *ckm = km, *cqn = qn, *ckn = kn, *cs = scores;
+    auto launched = [&](cudaError_t e) {
+        count_launches(1);
+        if (e == cudaSuccess) return true;
+        cudaGetLastError();
+        return false;
+    };
+    const unsigned tiles = static_cast<unsigned>((NC + kGT - 1) / kGT);
+    cfg.gridDim = dim3(tiles, tiles, static_cast<unsigned>(n_bh));
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = 0;
+    if (!launched(cudaLaunchKernelEx(&cfg, vsa_score_kernel, cqm, ckm, NC, scores)))
+        return GBATTN_ERR_CUDA;
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + kTopkWarps - 1) / kTopkWarps));
+    cfg.blockDim = dim3(kTopkWarps * 32);
+    cudaError_t e;
+    if (NC <= 512) {
+        cfg.dynamicSmemBytes = topk_smem_bytes<16, kCap, kTopkWarps>();
+        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<16, kCap, false>, cs, cqm, ckm, cqn, ckn, NC,
+                               topk, rows, deferred, idx, dev.status);
+    } else {
+        cfg.dynamicSmemBytes = topk_smem_bytes<32, kCap, kTopkWarps>();
+        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<32, kCap, false>, cs, cqm, ckm, cqn, ckn, NC,
+                               topk, rows, deferred, idx, dev.status);
+    }
+    if (!launched(e)) return GBATTN_ERR_CUDA;
+    const long long fb_ctas = std::min<long long>((rows + 32 * kFbWarps - 1) / (32 * kFbWarps),
+                                                  2LL * dev.num_sms);
+    cfg.gridDim = dim3(static_cast<unsigned>(fb_ctas));
+    cfg.blockDim = dim3(kFbWarps * 32);
+    if (NC <= 512) {
+        cfg.dynamicSmemBytes = topk_smem_bytes<16, 512, kFbWarps>();
+        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<16, 512, true>, cs, cqm, ckm, cqn, ckn, NC,
+                               topk, rows, deferred, idx, dev.status);
+    } else {
+        cfg.dynamicSmemBytes = topk_smem_bytes<32, 1024, kFbWarps>();
+        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<32, 1024, true>, cs, cqm, ckm, cqn, ckn, NC,
+                               topk, rows, deferred, idx, dev.status);
+    }
+    if (!launched(e)) return GBATTN_ERR_CUDA;
     return launch_status();
 }
 
@@ -489,11 +997,15 @@ extern "C" int vsa_pair_query_cubes(const int32_t* idx, int B, int H, int n_cube
 // pool it cannot reach from here, or a latency-critical loop in which a
 // cudaMalloc (which may synchronise the device) is not acceptable.  For them,
 // vsa_select_blocks_noalloc runs the same selection with its scratch (the FP32
-// pooled cube means) in a fixed array of kNoAllocScratchBytes that lives in
-// this library's device image.  Every GPU that loads the library holds the
-// array until the process exits.
+// pooled cube means, their norms, one flag per query cube and the FP32 scores)
+// in a fixed array of
+// kNoAllocScratchBytes that lives in this library's device image.  Every GPU
+// that loads the library holds the array until the process exits.
 namespace {
-constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
+// 48 MiB + 192 KiB: the whole workspace of 16384 query cubes at 512 cubes per
+// head and D = 128 (B*H*S <= 1,048,576 tokens x heads at S = 32768, e.g. B=1,
+// H=32): means 16 MiB, norms and flags 192 KiB, scores 32 MiB.
+constexpr size_t kNoAllocScratchBytes = (48u << 20) + (192u << 10);
 
 static __device__ __align__(256) unsigned char g_select_scratch[kNoAllocScratchBytes];
 
@@ -533,8 +1045,10 @@ extern "C" int vsa_select_blocks_noalloc(const void* q, const void* k, int B, in
     void* scratch = nullptr;
     const int rc = scratch_address(&scratch);
     if (rc != GBATTN_OK) return rc;
-    // The pool kernel overwrites every scratch byte it later reads, so the
-    // previous call's contents need no clearing.
+    // Every scratch byte a call reads was written earlier in the same call (the
+    // pool kernel writes the means and norms, the score kernel every score read,
+    // the top-k kernel every row's flag), so the previous call's contents need
+    // no clearing.
     return vsa_select_blocks(q, k, B, H, S, D, block, topk, prefix, cube_valid, idx, scratch,
                              kNoAllocScratchBytes, stream);
 }

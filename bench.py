@@ -522,6 +522,57 @@ def bridge_back_to_back(torch, w, n=20, reps=5):
     return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / n
 
 
+def measure_small(gb, torch, dev, name, steps, warmup, pk, n=20):
+    """One of the two small configurations (dense_small, causal_small), timed on its own.
+
+    A call at these sizes takes tens of microseconds, about as long as the host
+    takes to issue it, so it is timed the way a serving loop runs it: n calls in a
+    row captured once as a CUDA graph, replayed `steps` times with CUDA events on
+    the launching stream; the per-call time is the replay time / n.  The calls
+    bracketed one by one with events (host launch gaps included) are reported
+    beside it."""
+    w = Workload(name, gb, torch, dev, host_inputs(name))
+    (_, fn), = w.calls()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    graph = torch.cuda.CUDAGraph()
+    n0 = gb.launch_count()
+    with torch.cuda.graph(graph):
+        for _ in range(n):
+            fn()
+    launches = (gb.launch_count() - n0) // n
+    graph.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t = [e0.elapsed_time(e1) / n for e0, e1 in evs]
+    single = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+    for e0, e1 in single:
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if gb.device_status() != 0:
+        raise RuntimeError(f"device status flags set during the {name} measurement")
+    ms = statistics.median(t)
+    ms_single = statistics.median(e0.elapsed_time(e1) for e0, e1 in single)
+    tflops = w.flops / (ms * 1e-3) / 1e12
+    return {"ms": ms, "cv": statistics.pstdev(t) / statistics.mean(t) if len(t) > 1 else 0.0,
+            "useful_flop": w.flops, "achieved": tflops, "unit": "TFLOP/s", "peak": pk["tc"],
+            "frac": tflops / pk["tc"], "peak_source": f"{pk['src']} bf16 burst (kernel timed alone)",
+            "launches_per_call": launches,
+            "timing": f"CUDA-graph replay of {n} calls in a row, {steps} replays, median",
+            "ms_one_call_with_host_launch": ms_single}
+
+
 def measure_masked(gb, torch, dev, steps, warmup, pk):
     """Dense attention with an additive mask (B1 H24 S8192 D128, one FP16 mask
     [8192][8192] shared by the heads), timed on its own; useful FLOP count only
@@ -703,6 +754,8 @@ def main():
                     help="the full VSA layout (prefix + boundary cubes) measured beside the step")
     ap.add_argument("--paged-fused", default="on", choices=["on", "off", "only"],
                     help="the paged prefill with the bridge fused in, beside bridge + prefill")
+    ap.add_argument("--small", default="on", choices=["on", "off"],
+                    help="the two small configurations (dense B1 H2 S256, causal Q1024/KV4096)")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count of the dense/VSA workloads (profiling runs)")
     args = ap.parse_args()
@@ -843,6 +896,17 @@ def main():
                                                 "achieved": gbs_b2b,
                                                 "frac": gbs_b2b / pk["hbm"],
                                                 "timing": "CUDA-graph replay of 20 calls in a row"}}
+    for w in wls:
+        if w.w["kind"] == "vsa":
+            t = per_call[f"{w.name}:vsa_select_blocks"]
+            S = w.q.shape[2]
+            sel_bytes = 2 * w.q.numel() * 2 + w.idx.numel() * 4   # Q and K read once, idx written
+            gbs = sel_bytes / (t * 1e-3) / 1e9
+            extra["select"] = {"ms": t, "achieved": gbs, "unit": "GB/s", "peak": pk["hbm"],
+                               "frac": gbs / pk["hbm"], "bytes_per_call": sel_bytes,
+                               "kernels": "vsa_pool_kernel + vsa_score_select_kernel + "
+                                          "vsa_select_fallback_kernel",
+                               "timing": "CUDA events around the call inside the step"}
     per_variant = {}
     for w in wls:
         t = sum(v for k, v in per_call.items() if k.startswith(w.name + ":"))
@@ -853,56 +917,71 @@ def main():
     # stream moves data while the compute stream runs the previous sub-workload.
     e2e = None
     if not args.no_e2e:
+        # Two device buffer sets per sub-workload, used on alternate steps: the
+        # inputs of step s+1 are copied while step s computes on the other set, and
+        # a set is refilled only after the compute two steps back has finished with
+        # it and its outputs have been read back.
+        sets = [wls, [Workload(n, gb, torch, dev, hosts[n]) for n in names]]
         h2d = 0
         d2h = 0
         ins, outs = {}, {}
-        for w in wls:
-            ins[w.name] = []
-            for dtens, i in w.h2d_pairs():
-                p = torch.from_numpy(np.ascontiguousarray(w.host[i])).pin_memory()
-                ins[w.name].append((p, dtens))
-                h2d += p.numel() * p.element_size()
-            outs[w.name] = []
-            for o in w.d2h():
-                outs[w.name].append((torch.empty(o.shape, dtype=o.dtype, pin_memory=True), o))
-                d2h += o.numel() * o.element_size()
+        for p_, ws_ in enumerate(sets):
+            for w in ws_:
+                ins[(p_, w.name)] = []
+                for dtens, i in w.h2d_pairs():
+                    hp = torch.from_numpy(np.ascontiguousarray(w.host[i])).pin_memory()
+                    ins[(p_, w.name)].append((hp, dtens))
+                    if p_ == 0:
+                        h2d += hp.numel() * hp.element_size()
+                outs[(p_, w.name)] = []
+                for o in w.d2h():
+                    outs[(p_, w.name)].append((torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
+                                               o))
+                    if p_ == 0:
+                        d2h += o.numel() * o.element_size()
         h2d_s = torch.cuda.Stream()     # inputs in
         d2h_s = torch.cuda.Stream()     # results out
         comp_s = stream
         ev = lambda: torch.cuda.Event()
-        last_done = {w.name: None for w in wls}     # compute of the previous step finished
-        last_read = {w.name: None for w in wls}     # outputs of the previous step copied back
+        last_done = {}                  # (set, workload): compute that last used the set
+        last_read = {}                  # (set, workload): its outputs copied back
+        n_step = [0]
 
         def e2e_step():
+            p_ = n_step[0] & 1
+            n_step[0] += 1
             ready = {}
-            for w in wls:                           # all input copies queue up front
+            for w in sets[p_]:                      # all input copies queue up front
+                key = (p_, w.name)
                 with torch.cuda.stream(h2d_s):
-                    if last_done[w.name] is not None:
-                        h2d_s.wait_event(last_done[w.name])   # previous step done with them
-                    for h, d in ins[w.name]:
+                    if key in last_done:
+                        h2d_s.wait_event(last_done[key])   # step s-2 done with this set
+                    for h, d in ins[key]:
                         d.copy_(h, non_blocking=True)
-                    ready[w.name] = ev()
-                    ready[w.name].record(h2d_s)
-            for w in wls:
-                comp_s.wait_event(ready[w.name])
-                if last_read[w.name] is not None:
-                    comp_s.wait_event(last_read[w.name])       # outputs read back
+                    ready[key] = ev()
+                    ready[key].record(h2d_s)
+            for w in sets[p_]:
+                key = (p_, w.name)
+                comp_s.wait_event(ready[key])
+                if key in last_read:
+                    comp_s.wait_event(last_read[key])       # step s-2 outputs read back
                 for _, fn in w.calls():
                     fn()
                 done = ev()
                 done.record(comp_s)
-                last_done[w.name] = done
+                last_done[key] = done
                 with torch.cuda.stream(d2h_s):
                     d2h_s.wait_event(done)
-                    for h, d in outs[w.name]:
+                    for h, d in outs[key]:
                         h.copy_(d, non_blocking=True)
                     rd = ev()
                     rd.record(d2h_s)
-                    last_read[w.name] = rd
+                    last_read[key] = rd
 
         e2e_step()
+        e2e_step()
         torch.cuda.synchronize()
-        n_e2e = max(3, args.steps // 3)
+        n_e2e = max(4, 2 * (args.steps // 6))
         barrier(world, dev)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -916,11 +995,18 @@ def main():
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
         wall_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+        if gb.device_status() != 0:
+            raise RuntimeError("device status flags set during the end-to-end steps")
         e2e = {"value": world * flops_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e_ms, "wall_ms_per_step": wall_ms, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h,
-               "overlap": "inputs copied on an H2D stream and results on a D2H stream while other sub-workloads compute"}
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "overlap": "two device buffer sets on alternate steps; inputs copied on an H2D "
+                          "stream and results on a D2H stream while the other set computes"}
+        del sets[1]
 
+    if args.small == "on" and args.workload == "all":
+        for n in ("dense_small", "causal_small"):
+            extra[n] = measure_small(gb, torch, dev, n, args.steps, args.warmup, pk)
     if args.decode == "on" and args.workload == "all":
         extra["decode"] = measure_decode(gb, torch, dev, args.steps, args.warmup, pk)
     if args.masked == "on" and args.workload == "all":

@@ -251,8 +251,15 @@ int attn_paged_decode_fwd(const void* q, const uint8_t* k_pages, const uint8_t* 
  *          the largest score, ties to the lower cube index, in ascending cube order.
  *   Pooled vector = FP32 sum over the cube's real tokens in token order / their count
  *   (FP32, RN); padding contents are never read.
- *   Score = FP32 sum over d = 0..D-1, in order, of FP32 products (no fused multiply-add).
+ *   Score = the exact dot product of the two FP32 pooled vectors (no rounding): FP32
+ *   scores with a rigorous error bound decide almost every key, and the keys whose
+ *   FP32 score lies within that bound of the k-th value are ranked by exact integer
+ *   scores.  (Inputs holding Inf or NaN give an unspecified but valid selection.)
  *   block == 64, D == 128, (S - prefix) % block == 0, 1 <= topk <= (S-prefix)/block <= 1024.
+ *   Workspace: vsa_select_workspace_size() bytes for rows = B*H*(S/block) query cubes:
+ *   the FP32 means of Q and K (rows*D*4 each), their norms and one int32 flag per row
+ *   (rows*4 each), and the FP32 scores (rows * (S/block rounded up to 128) * 4), each
+ *   part rounded up to 256 bytes.
  */
 size_t vsa_select_workspace_size(int B, int H, int S, int D, int block);
 int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D, int block,
@@ -266,12 +273,15 @@ int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D, 
  * allocations, code whose device memory is owned by a pool it cannot reach, or
  * a latency-critical loop where a cudaMalloc (which may synchronise the
  * device) is not acceptable.  It computes exactly what vsa_select_blocks
- * computes, with the scratch (the FP32 pooled cube means, 2*B*H*(S/block)*D*4
- * bytes) taken from a fixed 16 MiB array inside the library, which every GPU
- * that loads the library keeps until the process exits.
- *   - Sizes whose scratch exceeds 16 MiB are rejected with GBATTN_ERR_WORKSPACE
- *     before anything is queued (at D=128, block=64: B*H*S <= 262144 tokens,
- *     e.g. B=1, H=8, S=32768).
+ * computes, with the scratch (vsa_select_workspace_size() bytes: the FP32
+ * pooled cube means, their norms, one flag per query cube and the FP32 cube
+ * scores) taken from a fixed array of GBATTN_NOALLOC_SCRATCH_BYTES (48 MiB +
+ * 192 KiB) inside the library, which every GPU that loads the library keeps
+ * until the process exits.
+ *   - Sizes whose vsa_select_workspace_size() exceeds that array are rejected
+ *     with GBATTN_ERR_WORKSPACE before anything is queued.  At D=128, block=64
+ *     and S = 32768 (512 cubes per head) the limit is B*H <= 32, i.e.
+ *     B*H*S <= 1,048,576 tokens x heads.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -282,7 +292,7 @@ int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D, 
  *     time on one device (for example on two streams) race on it: order them
  *     on one stream or synchronise between them.
  */
-#define GBATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define GBATTN_NOALLOC_SCRATCH_BYTES ((48u << 20) + (192u << 10))
 int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S, int D, int block,
                               int topk, int prefix, const int32_t* cube_valid, int32_t* idx,
                               void* stream);

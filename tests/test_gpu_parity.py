@@ -260,6 +260,17 @@ def test_vsa_select_small_and_ties(gb):
     nc = q.shape[2] // 64
     idx = gb.vsa_select_blocks(t(q), t(k), topk=nc)
     assert np.array_equal(idx.cpu().numpy(), np.broadcast_to(np.arange(nc), idx.shape))
+    # every key cube equal (all 64 scores tie: more undecided keys than a warp ranks in
+    # place, so the fallback kernel decides), and half of them equal
+    k3 = np.broadcast_to(k[:, :, None, :64], (1, 3, nc, 64, 128)).reshape(k.shape).copy()
+    k4 = k.reshape(1, 3, nc, 64, 128).copy()
+    k4[:, :, ::2] = k3.reshape(1, 3, nc, 64, 128)[:, :, ::2]
+    k4 = k4.reshape(k.shape)
+    for kk in (k3, k4):
+        for topk in (5, 40):
+            idx = gb.vsa_select_blocks(t(q), t(kk), topk=topk)
+            assert np.array_equal(idx.cpu().numpy(), OV.vsa_select(q, kk, 64, topk)), topk
+    assert gb.device_status() == 0
 
 
 def test_vsa_select_full_size_bit_exact(gb):
