@@ -30,15 +30,15 @@ _SIGNATURES = {
     "gbattn_set_wait_limit_ns": (_i, [ctypes.c_uint64]),
     "gbattn_launch_count": (ctypes.c_uint64, []),
     "gbattn_test_inject_fault": (_i, [_i]),
-    "attn_dense_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "attn_dense_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _f, _vp]),
     "attn_dense_mask_fwd": (_i, [_vp, _vp, _vp, _vp, ctypes.c_longlong, ctypes.c_longlong, _vp, _vp,
                                  _i, _i, _i, _i, _i, _f, _vp]),
     "attn_causal_prefill_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
-    "attn_causal_prefill_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
-                                     _vp, _sz, _vp]),
+    "attn_causal_prefill_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp,
+                                     _vp, _f, _i, _vp, _sz, _vp]),
     "e4m3_paged_to_fp16": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _vp, _vp, _vp]),
     "attn_causal_prefill_paged_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
-                                           _i, _i, _i, _i, _f, _f, _f, _vp, _sz, _vp]),
+                                           _i, _i, _i, _i, _f, _f, _f, _i, _vp, _sz, _vp]),
     "attn_paged_decode_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "attn_paged_decode_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                    _i, _i, _f, _f, _f, _vp, _sz, _vp]),
@@ -48,6 +48,8 @@ _SIGNATURES = {
                             _f, _vp]),
     "vsa_pair_query_cubes": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
 }
+
+PROB_SPLIT = 1          # flags of the causal prefill calls (GBATTN_PROB_SPLIT)
 
 DEV_WAIT_TIMEOUT = 1
 DEV_BAD_PAGE = 2
@@ -107,6 +109,24 @@ def _need(t, name, dtype, ndim=None):
         raise ValueError(f"{name} must have {ndim} dimensions")
 
 
+def _need_view(t, name, dtype):
+    """A [B, H, S, D] CUDA view whose last dimension is contiguous (any other strides)."""
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError(f"{name} must be a 4-D view with a contiguous last dimension")
+
+
+def _strides(t):
+    """{batch, head, row} element strides of a [B, H, S, D] view, or None when dense."""
+    if t.is_contiguous():
+        return None
+    return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
 def _scale(scale, D):
     return float(1.0 / D ** 0.5) if scale is None else float(scale)
 
@@ -138,20 +158,27 @@ def device_status(stream=None):
 
 
 def attn_dense_fwd(q, k, v, o=None, lse=None, scale=None, stream=None):
-    """Dense non-causal attention. q [B,H,Sq,D], k/v [B,H,Skv,D] FP16 -> o [B,H,Sq,D]."""
+    """Dense non-causal attention. q [B,H,Sq,D], k/v [B,H,Skv,D] FP16 -> o [B,H,Sq,D].
+
+    q, k, v and o may be strided views with a contiguous last dimension (e.g. the
+    slices of a packed [B,S,3,H,D] QKV tensor, permuted to [B,H,S,D]); k and v
+    must share their strides."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _need(t, n, torch.float16, 4)
+        _need_view(t, n, torch.float16)
     B, H, Sq, D = q.shape
     Skv = k.shape[2]
     if tuple(k.shape) != (B, H, Skv, D) or tuple(v.shape) != tuple(k.shape):
         raise ValueError("k and v must be [B, H, Skv, D] matching q")
-    o = torch.empty_like(q) if o is None else o
-    _need(o, "o", torch.float16, 4)
+    if k.stride() != v.stride():
+        raise ValueError("k and v must have the same strides")
+    o = torch.empty((B, H, Sq, D), dtype=torch.float16, device=q.device) if o is None else o
+    _need_view(o, "o", torch.float16)
     if lse is not None:
         _need(lse, "lse", torch.float32)
     rc = load().attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Skv, D,
-                               _scale(scale, D), _stream(stream))
+                               _strides(q), _strides(k), _strides(o), _scale(scale, D),
+                               _stream(stream))
     _check("attn_dense_fwd", rc)
     return o
 
@@ -191,25 +218,33 @@ def attn_causal_prefill_workspace_size(B, Hq, Q_pad, KV, D):
 
 
 def attn_causal_prefill_fwd(q, k, v, q_real=None, o=None, lse=None, scale=None, workspace=None,
-                            stream=None):
-    """Causal prefill with shared-KV heads. q [B,Hq,Q_pad,D], k/v [B,Hkv,KV,D] FP16."""
+                            prob_split=False, stream=None):
+    """Causal prefill with shared-KV heads. q [B,Hq,Q_pad,D], k/v [B,Hkv,KV,D] FP16.
+
+    Strided views with a contiguous last dimension are accepted as for
+    attn_dense_fwd.  prob_split=True carries the probabilities into the PV
+    product as FP16 hi + lo (GBATTN_PROB_SPLIT)."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _need(t, n, torch.float16, 4)
+        _need_view(t, n, torch.float16)
     B, Hq, Qp, D = q.shape
     Hkv, KV = k.shape[1], k.shape[2]
     if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
         raise ValueError("k and v must be [B, Hkv, KV, D] matching q")
+    if k.stride() != v.stride():
+        raise ValueError("k and v must have the same strides")
     q_real = Qp if q_real is None else int(q_real)
-    o = torch.empty_like(q) if o is None else o
-    _need(o, "o", torch.float16, 4)
+    o = torch.empty((B, Hq, Qp, D), dtype=torch.float16, device=q.device) if o is None else o
+    _need_view(o, "o", torch.float16)
     if lse is not None:
         _need(lse, "lse", torch.float32)
     if workspace is None:
         nbytes = attn_causal_prefill_workspace_size(B, Hq, Qp, KV, D)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     rc = load().attn_causal_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
-                                        Qp, q_real, KV, D, _scale(scale, D), _ptr(workspace),
+                                        Qp, q_real, KV, D, _strides(q), _strides(k), _strides(o),
+                                        _scale(scale, D), PROB_SPLIT if prob_split else 0,
+                                        _ptr(workspace),
                                         workspace.numel() * workspace.element_size(),
                                         _stream(stream))
     _check("attn_causal_prefill_fwd", rc)
@@ -218,7 +253,7 @@ def attn_causal_prefill_fwd(q, k, v, q_real=None, o=None, lse=None, scale=None, 
 
 def attn_causal_prefill_paged_fwd(q, k_pages, v_pages, page_table, kv_len, k_scale, v_scale,
                                   q_real=None, o=None, lse=None, scale=None, workspace=None,
-                                  stream=None):
+                                  prob_split=False, stream=None):
     """Causal prefill over paged E4M3 K/V (the bridge fused in).  q [B,Hq,Q_pad,D] FP16;
     pages [P,page,Hkv,D] uint8; page_table int32 [B,max_pages] (or [max_pages] for B=1)."""
     import torch
@@ -244,8 +279,8 @@ def attn_causal_prefill_paged_fwd(q, k_pages, v_pages, page_table, kv_len, k_sca
     rc = load().attn_causal_prefill_paged_fwd(
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(table), _ptr(o), _ptr(lse), B, Hq, Hkv, Qp,
         q_real, int(kv_len), D, P, ps, table.shape[1], float(k_scale), float(v_scale),
-        _scale(scale, D), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream))
+        _scale(scale, D), PROB_SPLIT if prob_split else 0, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
     _check("attn_causal_prefill_paged_fwd", rc)
     return o
 

@@ -69,14 +69,15 @@ int load_encoder() {
 }
 }  // namespace
 
-int encode_tmap_f16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+int encode_tmap_f16_4d(CUtensorMap* map, const void* base, uint64_t D, uint64_t S, uint64_t H,
+                       uint64_t B, uint64_t row_stride, uint64_t head_stride, uint64_t batch_stride,
                        uint32_t box0, uint32_t box1) {
     if (load_encoder() != GBATTN_OK) return GBATTN_ERR_CUDA;
-    cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};   // bytes, dims 1 and 2
-    cuuint32_t box[3] = {box0, box1, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
+    cuuint64_t dims[4] = {D, S, H, B};
+    cuuint64_t strides[3] = {row_stride * 2, head_stride * 2, batch_stride * 2};   // bytes
+    cuuint32_t box[4] = {box0, box1, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -91,7 +91,8 @@ struct AttnArgs {
     float scale_log2;   // scale * log2(e)
     float scale;        // masked: the softmax scale itself
     __half* o;
-    float* lse;         // optional natural-log LSE
+    long long o_sb, o_sh, o_sr;   // element strides of O between batch entries, heads, rows
+    float* lse;         // optional natural-log LSE (dense [B*H][seq_q])
     float* part_o;      // causal, n_chunks > 1: [C][heads_q][seq_q][D] FP32, normalised
     float* part_lse;    // causal, n_chunks > 1: [C][heads_q][seq_q] log2-sum-exp2
     const int32_t* idx; // sparse: [heads][n_cubes][topk]
@@ -351,7 +352,12 @@ __device__ void fill_tile_counts(SparseTiles* st, const Ctrl* ctrl, const AttnAr
     }
 }
 
-template <int D, int MODE>
+// PS (causal modes only): the probabilities enter the PV product as two FP16
+// halves, hi = RNE(p) and lo = RNE(p - hi), about 22 bits of p, instead of one
+// FP16 value.  P_lo takes columns 64..127 of its S buffer (both threads of a
+// row have read their S halves before either writes), and PV issues a second
+// group of MMAs over it.
+template <int D, int MODE, bool PS = false>
 __global__ void __launch_bounds__(threads_for(MODE), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmM,
@@ -416,6 +422,9 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         kv_bh = bh;
         if (MODE == kDense || MODE == kMasked) n_tiles = (a.seq_k + BN - 1) / BN;
     }
+    // 4-D tensor-map coordinates (head, batch entry) of the query and key heads
+    const int qb = bh / a.hq, qh = bh - qb * a.hq;
+    const int kvb = kv_bh / a.hkv, kvh = kv_bh - kvb * a.hkv;
     // First token row of each 64-row half of the query tile.  A VSA video CTA
     // owns a pair of query cubes (ca, cb), not necessarily adjacent; cb < 0
     // leaves the second half empty.
@@ -479,13 +488,13 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                 const int r1 = rbase1 >= 0 ? rbase1 : rbase0;
 #pragma unroll
                 for (int c = 0; c < C::KCH; ++c) {
-                    tma_load_3d(sQ + c * C::CHUNK, &tmM, &ctrl->q_full, c * 64, rbase0, bh);
-                    tma_load_3d(sQ + c * C::CHUNK + C::HALF, &tmM, &ctrl->q_full, c * 64, r1, bh);
+                    tma_load_4d(sQ + c * C::CHUNK, &tmM, &ctrl->q_full, c * 64, rbase0, qh, qb);
+                    tma_load_4d(sQ + c * C::CHUNK + C::HALF, &tmM, &ctrl->q_full, c * 64, r1, qh, qb);
                 }
             } else {
 #pragma unroll
                 for (int c = 0; c < C::KCH; ++c)
-                    tma_load_3d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, bh);
+                    tma_load_4d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, qh, qb);
             }
         }
         __syncwarp();
@@ -555,6 +564,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             mma_ts(tmem + C::T_O, tmem + buf * 128 + k16 * 8,
                    sdesc_sw128(va + k16 * 2048, C::CHUNK, 1024), C::IDESC_PV,
                    (acc || k16 > 0) ? 1u : 0u);
+        if (PS) {   // O += P_lo V (columns 64.. of the buffer)
+#pragma unroll
+            for (int k16 = 0; k16 < BN / 16; ++k16)
+                mma_ts(tmem + C::T_O, tmem + buf * 128 + 64 + k16 * 8,
+                       sdesc_sw128(va + k16 * 2048, C::CHUNK, 1024), C::IDESC_PV, 1u);
+        }
     };
     // Ring positions (the TMA warp's load order, see ring_item) of K_t and V_j.
     auto pos_k = [&](int t) { return t < C::NSB ? t : C::NSB + 2 * (t - C::NSB) + 1; };
@@ -633,9 +648,9 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                     mbar_arrive_expect_tx(&ctrl->full[slot], C::SLOT_BYTES);
 #pragma unroll
                     for (int c = 0; c < C::KCH; ++c) {
-                        tma_load_3d(dst + c * C::CHUNK, m, &ctrl->full[slot], c * 64, k0, kv_bh);
-                        tma_load_3d(dst + c * C::CHUNK + C::HALF, m, &ctrl->full[slot], c * 64, k1,
-                                    kv_bh);
+                        tma_load_4d(dst + c * C::CHUNK, m, &ctrl->full[slot], c * 64, k0, kvh, kvb);
+                        tma_load_4d(dst + c * C::CHUNK + C::HALF, m, &ctrl->full[slot], c * 64, k1,
+                                    kvh, kvb);
                     }
                 }
                 __syncwarp();
@@ -1019,6 +1034,10 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                 const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
                 rs[i & 3] = f2_add(rs[i & 3], f2_pack(p0, p1));   // four independent sums
                 p2[i] = pack_half2(p0, p1);
+                if (PS) {   // keep p for its low half
+                    s[2 * i] = __float_as_uint(p0);
+                    s[2 * i + 1] = __float_as_uint(p1);
+                }
             }
             float r0, r1, r2, r3, r4, r5, r6, r7;
             f2_unpack(rs[0], r0, r1);
@@ -1029,6 +1048,15 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             // P_j over the first 64 columns of its S buffer; both threads of the
             // row have loaded their S halves (they passed the exchange above).
             tmem_st32(sbuf + half * 32, p2);
+            if (PS) {   // lo = RNE(p - hi); p - hi is exact in FP32
+                uint32_t lo2[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&p2[i]));
+                    lo2[i] = pack_half2(__uint_as_float(s[2 * i]) - h.x, __uint_as_float(s[2 * i + 1]) - h.y);
+                }
+                tmem_st32(sbuf + 64 + half * 32, lo2);
+            }
             tmem_st_wait();
             if (warp_need && j > 0) {   // rescale this thread's half of O after PV_{j-1}
                 ok = wait_warp(&ctrl->pv_done[(j - 1) % C::NSB], ((j - 1) / C::NSB) & 1, w);
@@ -1095,7 +1123,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                                              __uint_as_float(o[4 * e + 2]) * inv_l,
                                              __uint_as_float(o[4 * e + 3]) * inv_l);
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(a.o + orow * D + c0);
+                    uint4* dst = reinterpret_cast<uint4*>(a.o + qb * a.o_sb + qh * a.o_sh +
+                                                          row_g * a.o_sr + c0);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         uint32_t hw[4];
@@ -1132,7 +1161,8 @@ template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict__ part_o,
                                                          const float* __restrict__ part_lse,
                                                          int n_chunks, long long rows, int seq_q,
-                                                         int q_real, __half* __restrict__ o,
+                                                         int q_real, int hq, Strides os,
+                                                         __half* __restrict__ o,
                                                          float* __restrict__ lse) {
     const long long row = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -1166,20 +1196,22 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
             }
         }
     }
-    uint32_t* dst = reinterpret_cast<uint32_t*>(o + row * D + lane * PER);
+    const long long bh = row / seq_q;
+    const long long ob = bh / hq, oh = bh - ob * hq;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(o + ob * os.b + oh * os.h + i * os.r + lane * PER);
 #pragma unroll
     for (int e = 0; e < PER / 2; ++e) dst[e] = pack_half2(acc[2 * e], acc[2 * e + 1]);
     if (lse && lane == 0) lse[row] = total * 0.69314718055994531f;
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool PS = false>
 int set_smem_attr() {
     static std::once_flag once[64];
     static int rc[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GBATTN_ERR_CUDA;
     std::call_once(once[dev], [&] {
-        rc[dev] = cudaFuncSetAttribute(attn_fwd_kernel<D, MODE>,
+        rc[dev] = cudaFuncSetAttribute(attn_fwd_kernel<D, MODE, PS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem_bytes<D, MODE>()) == cudaSuccess
                       ? GBATTN_OK
@@ -1188,26 +1220,33 @@ int set_smem_attr() {
     return rc[dev];
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool PS = false>
 int launch_attn(const void* q, const void* k, const void* v, int seq_q, int seq_k, int heads_q,
-                int heads_kv, dim3 grid, AttnArgs args, cudaStream_t stream,
-                const CUtensorMap* mask_map = nullptr, const CUtensorMap* kv_maps = nullptr) {
+                const Strides& qs, const Strides& kvs, dim3 grid, AttnArgs args,
+                cudaStream_t stream, const CUtensorMap* mask_map = nullptr,
+                const CUtensorMap* kv_maps = nullptr) {
+    // 4-D maps (D, S, heads, batch) with the callers' strides; boxes past a head's
+    // last row read zeros and never cross into another head
+    const int batch = heads_q / args.hq;
     CUtensorMap tq, tk, tv;
-    if (encode_tmap_f16_3d(&tq, q, D, seq_q, heads_q, 64, BM) != GBATTN_OK)
+    if (encode_tmap_f16_4d(&tq, q, D, seq_q, args.hq, batch, qs.r, qs.h, qs.b, 64, BM) != GBATTN_OK)
         return GBATTN_ERR_CUDA;
     if (kv_maps) {   // paged E4M3 K and V
         tk = kv_maps[0];
         tv = kv_maps[1];
-    } else if (encode_tmap_f16_3d(&tk, k, D, seq_k, heads_kv, 64, 64) != GBATTN_OK ||
-               encode_tmap_f16_3d(&tv, v, D, seq_k, heads_kv, 64, 64) != GBATTN_OK) {
+    } else if (encode_tmap_f16_4d(&tk, k, D, seq_k, args.hkv, batch, kvs.r, kvs.h, kvs.b, 64, 64) !=
+                   GBATTN_OK ||
+               encode_tmap_f16_4d(&tv, v, D, seq_k, args.hkv, batch, kvs.r, kvs.h, kvs.b, 64, 64) !=
+                   GBATTN_OK) {
         return GBATTN_ERR_CUDA;
     }
     CUtensorMap tq64;   // sparse modes: query cubes load as two 64-row boxes
-    if (is_sparse(MODE) && encode_tmap_f16_3d(&tq64, q, D, seq_q, heads_q, 64, 64) != GBATTN_OK)
+    if (is_sparse(MODE) &&
+        encode_tmap_f16_4d(&tq64, q, D, seq_q, args.hq, batch, qs.r, qs.h, qs.b, 64, 64) != GBATTN_OK)
         return GBATTN_ERR_CUDA;
-    int rc = set_smem_attr<D, MODE>();
+    int rc = set_smem_attr<D, MODE, PS>();
     if (rc != GBATTN_OK) return rc;
-    attn_fwd_kernel<D, MODE><<<grid, threads_for(MODE), smem_bytes<D, MODE>(), stream>>>(
+    attn_fwd_kernel<D, MODE, PS><<<grid, threads_for(MODE), smem_bytes<D, MODE>(), stream>>>(
         tq, tk, tv, mask_map ? *mask_map : (is_sparse(MODE) ? tq64 : tq), args);
     count_launches(1);
     return launch_status();
@@ -1224,6 +1263,18 @@ AttnArgs base_args(const DeviceState& dev, float scale) {
     a.wait_limit = wait_limit_ns();
     a.group = 1;
     return a;
+}
+
+void set_out_strides(AttnArgs& a, const Strides& os) {
+    a.o_sb = os.b;
+    a.o_sh = os.h;
+    a.o_sr = os.r;
+}
+
+Strides dense_strides(int H, int S, int D) {
+    Strides t;
+    make_strides(nullptr, 2, H, S, D, false, &t);   // B=2 keeps the dense batch stride
+    return t;
 }
 
 // Key-range chunks per causal query tile: minimise (waves of CTAs) / chunks
@@ -1274,21 +1325,29 @@ extern "C" int gbattn_test_inject_fault(int mode) {
 }
 
 extern "C" int attn_dense_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                              int B, int H, int Sq, int Skv, int D, float scale, void* stream) {
+                              int B, int H, int Sq, int Skv, int D, const int64_t* q_strides,
+                              const int64_t* kv_strides, const int64_t* o_strides, float scale,
+                              void* stream) {
     if (!q || !k || !v || !o) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0) return GBATTN_ERR_SHAPE;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
     if (D != 128) return GBATTN_ERR_UNSUPPORTED;
+    Strides qs, kvs, os;
+    if (!make_strides(q_strides, B, H, Sq, D, false, &qs) ||
+        !make_strides(kv_strides, B, H, Skv, D, false, &kvs) ||
+        !make_strides(o_strides, B, H, Sq, D, true, &os))
+        return GBATTN_ERR_SHAPE;
     if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u))
         return GBATTN_ERR_ALIGN;
-    const size_t qb = static_cast<size_t>(B) * H * Sq * D * 2;
-    const size_t kb = static_cast<size_t>(B) * H * Skv * D * 2;
+    const size_t qb = strided_bytes(qs, B, H, Sq, D);
+    const size_t kb = strided_bytes(kvs, B, H, Skv, D);
+    const size_t ob = strided_bytes(os, B, H, Sq, D);
     const size_t lb = static_cast<size_t>(B) * H * Sq * 4;
-    if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kb) || overlaps(o, qb, v, kb) ||
+    if (overlaps(o, ob, q, qb) || overlaps(o, ob, k, kb) || overlaps(o, ob, v, kb) ||
         overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
-        overlaps(lse, lb, o, qb))
+        overlaps(lse, lb, o, ob))
         return GBATTN_ERR_ALIAS;
     DeviceState dev;
     int rc = current_device(&dev);
@@ -1301,9 +1360,10 @@ extern "C" int attn_dense_fwd(const void* q, const void* k, const void* v, void*
     a.hkv = H;
     a.n_chunks = 1;
     a.o = static_cast<__half*>(o);
+    set_out_strides(a, os);
     a.lse = lse;
     dim3 grid((Sq + BM - 1) / BM, B * H);
-    return launch_attn<128, kDense>(q, k, v, Sq, Skv, B * H, B * H, grid, a,
+    return launch_attn<128, kDense>(q, k, v, Sq, Skv, B * H, qs, kvs, grid, a,
                                     static_cast<cudaStream_t>(stream));
 }
 
@@ -1358,7 +1418,9 @@ extern "C" int attn_dense_mask_fwd(const void* q, const void* k, const void* v, 
     if (encode_tmap_f16_mask(&tm, mask, Skv, Sq, hm, bm, sh, sb) != GBATTN_OK)
         return GBATTN_ERR_CUDA;
     dim3 grid(B * H, (Sq + BM - 1) / BM);
-    return launch_attn<128, kMasked>(q, k, v, Sq, Skv, B * H, B * H, grid, a,
+    set_out_strides(a, dense_strides(H, Sq, D));
+    return launch_attn<128, kMasked>(q, k, v, Sq, Skv, B * H, dense_strides(H, Sq, D),
+                                     dense_strides(H, Skv, D), grid, a,
                                      static_cast<cudaStream_t>(stream), &tm);
 }
 
@@ -1370,7 +1432,9 @@ extern "C" size_t attn_causal_prefill_workspace_size(int B, int Hq, int Q_pad, i
 
 extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void* v, void* o,
                                        float* lse, int B, int Hq, int Hkv, int Q_pad, int Q_real,
-                                       int KV, int D, float scale, void* workspace,
+                                       int KV, int D, const int64_t* q_strides,
+                                       const int64_t* kv_strides, const int64_t* o_strides,
+                                       float scale, int flags, void* workspace,
                                        size_t workspace_bytes, void* stream) {
     if (!q || !k || !v || !o) return GBATTN_ERR_NULL;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Q_pad <= 0 || KV <= 0) return GBATTN_ERR_SHAPE;
@@ -1378,17 +1442,24 @@ extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void*
         KV % 32 != 0)
         return GBATTN_ERR_SHAPE;
     if (static_cast<long long>(B) * Hq > 65535) return GBATTN_ERR_SHAPE;
+    if (flags & ~GBATTN_PROB_SPLIT) return GBATTN_ERR_SHAPE;
     if (D != 256) return GBATTN_ERR_UNSUPPORTED;
+    Strides qs, kvs, os;
+    if (!make_strides(q_strides, B, Hq, Q_pad, D, false, &qs) ||
+        !make_strides(kv_strides, B, Hkv, KV, D, false, &kvs) ||
+        !make_strides(o_strides, B, Hq, Q_pad, D, true, &os))
+        return GBATTN_ERR_SHAPE;
     if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
         !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u))
         return GBATTN_ERR_ALIGN;
-    const size_t qb = static_cast<size_t>(B) * Hq * Q_pad * D * 2;
-    const size_t kb = static_cast<size_t>(B) * Hkv * KV * D * 2;
+    const size_t qb = strided_bytes(qs, B, Hq, Q_pad, D);
+    const size_t kb = strided_bytes(kvs, B, Hkv, KV, D);
+    const size_t ob = strided_bytes(os, B, Hq, Q_pad, D);
     const size_t lb = static_cast<size_t>(B) * Hq * Q_pad * 4;
-    if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kb) || overlaps(o, qb, v, kb) ||
+    if (overlaps(o, ob, q, qb) || overlaps(o, ob, k, kb) || overlaps(o, ob, v, kb) ||
         overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
-        overlaps(lse, lb, o, qb))
+        overlaps(lse, lb, o, ob))
         return GBATTN_ERR_ALIAS;
     DeviceState dev;
     int rc = current_device(&dev);
@@ -1398,7 +1469,7 @@ extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void*
         --chunks;
     const size_t wb = causal_workspace(chunks, B, Hq, Q_pad, D);
     if (wb > 0 && (overlaps(workspace, wb, q, qb) || overlaps(workspace, wb, k, kb) ||
-                   overlaps(workspace, wb, v, kb) || overlaps(workspace, wb, o, qb) ||
+                   overlaps(workspace, wb, v, kb) || overlaps(workspace, wb, o, ob) ||
                    overlaps(workspace, wb, lse, lb)))
         return GBATTN_ERR_ALIAS;
     AttnArgs a = base_args(dev, scale);
@@ -1412,6 +1483,7 @@ extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void*
     a.kv_prefix = KV - Q_real;
     a.n_chunks = chunks;
     a.o = static_cast<__half*>(o);
+    set_out_strides(a, os);
     a.lse = lse;
     const long long rows = static_cast<long long>(B) * Hq * Q_pad;
     if (chunks > 1) {
@@ -1420,11 +1492,13 @@ extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void*
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     dim3 grid(((Q_pad + BM - 1) / BM) * chunks, B * Hq);
-    rc = launch_attn<256, kCausal>(q, k, v, Q_pad, KV, B * Hq, B * Hkv, grid, a, s);
+    rc = (flags & GBATTN_PROB_SPLIT)
+             ? launch_attn<256, kCausal, true>(q, k, v, Q_pad, KV, B * Hq, qs, kvs, grid, a, s)
+             : launch_attn<256, kCausal>(q, k, v, Q_pad, KV, B * Hq, qs, kvs, grid, a, s);
     if (rc != GBATTN_OK || chunks == 1) return rc;
     const long long threads = rows * 32;
     attn_merge_kernel<256><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
-        a.part_o, a.part_lse, chunks, rows, Q_pad, Q_real, a.o, lse);
+        a.part_o, a.part_lse, chunks, rows, Q_pad, Q_real, Hq, os, a.o, lse);
     count_launches(1);
     return launch_status();
 }
@@ -1435,9 +1509,10 @@ extern "C" int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pag
                                              int Q_pad, int Q_real, int KV, int D,
                                              int num_phys_pages, int page_size, int max_pages,
                                              float k_scale, float v_scale, float scale,
-                                             void* workspace, size_t workspace_bytes,
+                                             int flags, void* workspace, size_t workspace_bytes,
                                              void* stream) {
     if (!q || !k_pages || !v_pages || !page_table || !o) return GBATTN_ERR_NULL;
+    if (flags & ~GBATTN_PROB_SPLIT) return GBATTN_ERR_SHAPE;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Q_pad <= 0 || KV <= 0 || num_phys_pages <= 0 ||
         page_size <= 0 || max_pages <= 0)
         return GBATTN_ERR_SHAPE;
@@ -1514,6 +1589,8 @@ extern "C" int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pag
     a.ks2 = __float2half2_rn(k_scale);
     a.vs2 = __float2half2_rn(v_scale);
     a.out_mul = mode == 0 ? v_scale : 1.0f;
+    const Strides qs = dense_strides(Hq, Q_pad, D);
+    set_out_strides(a, qs);
     const long long rows = static_cast<long long>(B) * Hq * Q_pad;
     if (chunks > 1) {
         a.part_o = static_cast<float*>(workspace);
@@ -1521,12 +1598,15 @@ extern "C" int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pag
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     dim3 grid(((Q_pad + BM - 1) / BM) * chunks, B * Hq);
-    rc = launch_attn<256, kCausalPaged>(q, nullptr, nullptr, Q_pad, KV, B * Hq, B * Hkv, grid, a, s,
-                                        nullptr, kv);
+    rc = (flags & GBATTN_PROB_SPLIT)
+             ? launch_attn<256, kCausalPaged, true>(q, nullptr, nullptr, Q_pad, KV, B * Hq, qs, qs,
+                                                    grid, a, s, nullptr, kv)
+             : launch_attn<256, kCausalPaged>(q, nullptr, nullptr, Q_pad, KV, B * Hq, qs, qs, grid,
+                                              a, s, nullptr, kv);
     if (rc != GBATTN_OK || chunks == 1) return rc;
     const long long threads = rows * 32;
     attn_merge_kernel<256><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
-        a.part_o, a.part_lse, chunks, rows, Q_pad, Q_real, a.o, lse);
+        a.part_o, a.part_lse, chunks, rows, Q_pad, Q_real, Hq, qs, a.o, lse);
     count_launches(1);
     return launch_status();
 }
@@ -1577,9 +1657,11 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
     a.o = static_cast<__half*>(o);
     a.lse = lse;
     dim3 grid(prefix / BM + (nc + 1) / 2, B * H);
+    const Strides ds = dense_strides(H, S, D);
+    set_out_strides(a, ds);
     if (prefix > 0 || cube_valid)
-        return launch_attn<128, kSparseFull>(q, k, v, S, S, B * H, B * H, grid, a,
+        return launch_attn<128, kSparseFull>(q, k, v, S, S, B * H, ds, ds, grid, a,
                                              static_cast<cudaStream_t>(stream));
-    return launch_attn<128, kSparse>(q, k, v, S, S, B * H, B * H, grid, a,
+    return launch_attn<128, kSparse>(q, k, v, S, S, B * H, ds, ds, grid, a,
                                      static_cast<cudaStream_t>(stream));
 }

@@ -146,7 +146,7 @@ class Workload:
                                                w["v_scale"], k_out=self.kf, v_out=self.vf)),
                 ("attn_causal_prefill_fwd(paged)",
                  lambda: gb.attn_causal_prefill_fwd(self.q, self.kf[None], self.vf[None], o=self.o,
-                                                    workspace=self.ws))]
+                                                    workspace=self.ws, prob_split=True))]
 
     # host <-> device traffic of the end-to-end variant
     def h2d_pairs(self):
@@ -701,24 +701,30 @@ def measure_paged_fused(gb, torch, dev, steps, warmup, pk):
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def fused():
+    def fused(split):
         gb.attn_causal_prefill_paged_fwd(dq, dk, dv, dt, w["KV"], w["k_scale"], w["v_scale"], o=o,
-                                         workspace=ws)
+                                         workspace=ws, prob_split=split)
 
-    def two_pass():
+    def two_pass(split):
         gb.e4m3_paged_to_fp16(dk, dv, dt, w["KV"], w["k_scale"], w["v_scale"], k_out=kf, v_out=vf)
-        gb.attn_causal_prefill_fwd(dq, kf[None], vf[None], o=o, workspace=ws)
+        gb.attn_causal_prefill_fwd(dq, kf[None], vf[None], o=o, workspace=ws, prob_split=split)
+
+    def prefill_only(split):
+        gb.attn_causal_prefill_fwd(dq, kf[None], vf[None], o=o, workspace=ws, prob_split=split)
 
     res = {}
-    for name, fn in (("fused", fused), ("bridge_then_prefill", two_pass)):
+    for name, fn, split in (("fused", fused, True), ("bridge_then_prefill", two_pass, True),
+                            ("fused_fp16_p", fused, False),
+                            ("bridge_then_prefill_fp16_p", two_pass, False),
+                            ("prefill", prefill_only, True), ("prefill_fp16_p", prefill_only, False)):
         for _ in range(warmup):
-            fn()
+            fn(split)
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)]
         for e0, e1 in evs:
             e0.record(stream)
-            fn()
+            fn(split)
             e1.record(stream)
         torch.cuda.synchronize()
         res[name] = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
@@ -727,10 +733,18 @@ def measure_paged_fused(gb, torch, dev, steps, warmup, pk):
     flops = causal_flops(w["B"], w["Hq"], w["Q"], w["KV"], w["D"])
     tf = flops / (res["fused"] * 1e-3) / 1e12
     peak = pk["tc_sust"] or pk["tc"]
+    tf_p = lambda key: flops / (res[key] * 1e-3) / 1e12
     return {"kernel": "attn_fwd_kernel<256,causal_paged>+merge", "bound": "tensor", "achieved": tf,
             "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
             "peak_source": f"{pk['src']} bf16 sustained (fp16 dense rate = bf16 rate)",
+            "probabilities": "FP16 hi + lo (the path that meets the stated tolerance); *_fp16_p: "
+                             "the pages' single FP16 P",
             "ms_fused": res["fused"], "ms_bridge_then_prefill": res["bridge_then_prefill"],
+            "ms_fused_fp16_p": res["fused_fp16_p"],
+            "ms_bridge_then_prefill_fp16_p": res["bridge_then_prefill_fp16_p"],
+            "prefill_alone": {"ms": res["prefill"], "tflops": tf_p("prefill"),
+                              "ms_fp16_p": res["prefill_fp16_p"],
+                              "tflops_fp16_p": tf_p("prefill_fp16_p")},
             "config": {k2: v2 for k2, v2 in w.items() if k2 != "seed"}}
 
 

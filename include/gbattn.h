@@ -26,8 +26,17 @@
  *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
  *     library allocates no memory; scratch space is passed in as
  *     `workspace`, sized by the matching *_workspace_size() query.
- *   - Tensors are dense, row-major, in the layout each call states, with
- *     16-byte aligned base addresses.
+ *   - Tensors are row-major in the layout each call states, with 16-byte
+ *     aligned base addresses.  They are dense, except where a call takes
+ *     strides: a `*_strides` argument is NULL (dense) or a host array of three
+ *     int64 element strides {batch, head, row} of a [B][H][S][D] view whose D
+ *     elements are contiguous.  Strides are positive multiples of 8 elements
+ *     below 2^38, the row stride is at least D; a dimension of extent 1 may
+ *     carry any stride.  So a packed QKV tensor [B][S][3][H][D] passes its
+ *     three slices without a copy (row stride 3*H*D, head stride D, batch
+ *     stride 3*S*H*D).  An output's strides must not map two elements to one
+ *     address.  Overlap checks use each tensor's whole address span, so an
+ *     output interleaved between an input's rows is rejected too.
  *   - `stream` is a cudaStream_t passed as void*; all GPU work is queued on it
  *     and the call returns without waiting.  Inputs must stay unchanged and
  *     outputs unread until that work completes.
@@ -73,6 +82,16 @@ enum gbattn_device_flag {
                                      that sequence's rows were written as O = 0, lse = -inf */
 };
 
+/* Flags of the causal prefill calls. */
+enum gbattn_flag {
+    GBATTN_PROB_SPLIT = 1 /* probabilities enter the P V product as two FP16 halves, hi = RNE(p)
+                             and lo = RNE(p - hi) (about 22 bits of p, one more group of
+                             tensor-core MMAs per key tile), instead of the pages' single FP16
+                             value; the output error then no longer carries the FP16 rounding of
+                             P, which for large |V| (the E4M3 cache's values reach 448 * scale)
+                             can exceed a few 1e-3 where a row's output cancels */
+};
+
 /* Library version (major*10000 + minor*100 + patch). */
 int gbattn_version(void);
 
@@ -108,14 +127,17 @@ int gbattn_test_inject_fault(int mode);
  * Dense non-causal attention, head width D == 128.
  * Cites: "Share SM70 projection, attention and row reduction paths", Purpose
  * (D128 attention interfaces); FastVideo compare view, minimax_h3_prefix.cu
- * (BHSD operands, contiguous 128-wide heads, LSE output).
- *   q, o : [B][H][Sq][D]  FP16     k, v : [B][H][Skv][D] FP16
- *   lse  : optional [B][H][Sq] FP32, natural-log sum of exp of the scaled scores
+ * (BHSD operands with a contiguous 128-wide last dimension, strided rows
+ * allowed, LSE output).
+ *   q, o : [B][H][Sq][D]  FP16     k, v : [B][H][Skv][D] FP16 (k and v share kv_strides)
+ *   q_strides, kv_strides, o_strides: {batch, head, row} element strides or NULL (dense)
+ *   lse  : optional dense [B][H][Sq] FP32, natural-log sum of exp of the scaled scores
  *   scale: finite, > 0 (typically 1/sqrt(D))
  * Sizes: B, H, Sq, Skv >= 1; B*H <= 65535; Sq, Skv < 2^31.
  */
 int attn_dense_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                   int B, int H, int Sq, int Skv, int D, float scale, void* stream);
+                   int B, int H, int Sq, int Skv, int D, const int64_t* q_strides,
+                   const int64_t* kv_strides, const int64_t* o_strides, float scale, void* stream);
 
 /*
  * Causal prefill with shared-KV heads, head width D == 256.
@@ -124,6 +146,8 @@ int attn_dense_fwd(const void* q, const void* k, const void* v, void* o, float* 
  * 32, real-query causal offsets kept when queries are padded, FP32 prefix/tail
  * state and final merge, bounded workspace).
  *   q, o : [B][Hq][Q_pad][D] FP16   k, v : [B][Hkv][KV][D] FP16   lse: optional [B][Hq][Q_pad]
+ *   q_strides, kv_strides, o_strides: {batch, head, row} element strides or NULL (dense)
+ *   flags: 0 or GBATTN_PROB_SPLIT.
  *   Query head h reads KV head h / (Hq/Hkv).  Query i < Q_real sits at absolute
  *   position KV - Q_real + i and sees keys j <= that position.  Rows i >= Q_real
  *   are written as zeros (lse = -inf).
@@ -137,7 +161,9 @@ int attn_dense_fwd(const void* q, const void* k, const void* v, void* o, float* 
 size_t attn_causal_prefill_workspace_size(int B, int Hq, int Q_pad, int KV, int D);
 int attn_causal_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int Hq, int Hkv, int Q_pad, int Q_real, int KV, int D,
-                            float scale, void* workspace, size_t workspace_bytes, void* stream);
+                            const int64_t* q_strides, const int64_t* kv_strides,
+                            const int64_t* o_strides, float scale, int flags, void* workspace,
+                            size_t workspace_bytes, void* stream);
 
 /*
  * Causal prefill reading K and V straight from paged E4M3 caches (the bridge fused into the
@@ -149,7 +175,8 @@ int attn_causal_prefill_fwd(const void* q, const void* k, const void* v, void* o
  *   Computes exactly what e4m3_paged_to_fp16 followed by attn_causal_prefill_fwd computes: the
  *   keys and values are RNE_fp16(decode(byte) * scale), formed in shared memory from the
  *   cached bytes.  Same query positions, padding and split-KV workspace rules as
- *   attn_causal_prefill_fwd (attn_causal_prefill_workspace_size applies).
+ *   attn_causal_prefill_fwd (attn_causal_prefill_workspace_size applies).  flags: 0 or
+ *   GBATTN_PROB_SPLIT.
  *   D == 256; page_size a power of two >= 16; KV <= max_pages * page_size, KV % 32 == 0;
  *   num_phys_pages * page_size < 2^31.  A page-table entry outside [0, num_phys_pages) sets
  *   GBATTN_DEV_BAD_PAGE (that page reads physical page 0).
@@ -158,7 +185,7 @@ int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pages, const u
                                   const int32_t* page_table, void* o, float* lse, int B, int Hq,
                                   int Hkv, int Q_pad, int Q_real, int KV, int D,
                                   int num_phys_pages, int page_size, int max_pages, float k_scale,
-                                  float v_scale, float scale, void* workspace,
+                                  float v_scale, float scale, int flags, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
 /*

@@ -74,30 +74,50 @@ MIS = ctypes.c_void_p(0x10008)    # 8-byte aligned only
 MIS2 = ctypes.c_void_p(0x10002)   # not 4-byte aligned
 
 
+def _st(*v):
+    return (ctypes.c_int64 * 3)(*v)
+
+
 def test_dense_validation(lib):
     f = lib.attn_dense_fwd
-    assert f(None, P2, P3, P4, None, 1, 1, 128, 128, 128, 0.1, None) == NULL
-    assert f(P, P2, P3, P4, None, 0, 1, 128, 128, 128, 0.1, None) == SHAPE
-    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 64, 0.1, None) == UNSUPPORTED
-    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 128, 0.0, None) == SCALE
-    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 128, float("nan"), None) == SCALE
-    assert f(MIS, P2, P3, P4, None, 1, 1, 128, 128, 128, 0.1, None) == ALIGN
-    assert f(P, P2, P3, P, None, 1, 1, 128, 128, 128, 0.1, None) == ALIAS
-    assert f(P, P2, P3, ctypes.c_void_p(0x10000 + 4096), None, 1, 1, 128, 128, 128, 0.1,
+    # q, k, v, o, lse, B, H, Sq, Skv, D, q_strides, kv_strides, o_strides, scale, stream
+    N = None
+    assert f(None, P2, P3, P4, None, 1, 1, 128, 128, 128, N, N, N, 0.1, None) == NULL
+    assert f(P, P2, P3, P4, None, 0, 1, 128, 128, 128, N, N, N, 0.1, None) == SHAPE
+    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 64, N, N, N, 0.1, None) == UNSUPPORTED
+    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 128, N, N, N, 0.0, None) == SCALE
+    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 128, N, N, N, float("nan"), None) == SCALE
+    assert f(MIS, P2, P3, P4, None, 1, 1, 128, 128, 128, N, N, N, 0.1, None) == ALIGN
+    assert f(P, P2, P3, P, None, 1, 1, 128, 128, 128, N, N, N, 0.1, None) == ALIAS
+    assert f(P, P2, P3, ctypes.c_void_p(0x10000 + 4096), None, 1, 1, 128, 128, 128, N, N, N, 0.1,
              None) == ALIAS
-    assert f(P, P2, P3, P4, None, 256, 256, 128, 128, 128, 0.1, None) == SHAPE
+    assert f(P, P2, P3, P4, None, 256, 256, 128, 128, 128, N, N, N, 0.1, None) == SHAPE
+    # strides: {batch, head, row} elements
+    packed = _st(3 * 2 * 128 * 128, 128, 3 * 2 * 128)            # [B,S,3,H,D] slice, H=2
+    assert f(P, P2, P3, P4, None, 1, 2, 128, 128, 128, packed, packed, N, 0.1, None) in (CUDA, OK)
+    assert f(P, P2, P3, P4, None, 1, 2, 128, 128, 128, _st(0, 128 * 128, 100), N, N, 0.1,
+             None) == SHAPE                                       # row stride < D
+    assert f(P, P2, P3, P4, None, 1, 2, 128, 128, 128, _st(0, 128 * 128, 132), N, N, 0.1,
+             None) == SHAPE                                       # not a multiple of 8
+    assert f(P, P2, P3, P4, None, 1, 2, 128, 128, 128, N, N, _st(0, 128, 128), 0.1,
+             None) == SHAPE                                       # output heads overlap
+    assert f(P, P2, P3, P4, None, 1, 2, 128, 128, 128, N, N, _st(0, 128, 256), 0.1,
+             None) in (CUDA, OK)                                  # interleaved heads: fine
+    assert f(P, P2, P3, P4, None, 1, 2, 128, 128, 128, N, N, _st(0, 0, 256), 0.1,
+             None) == SHAPE                                       # zero stride
     # valid arguments, no GPU here -> CUDA error, not a crash
-    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 128, 0.1, None) in (CUDA, OK)
+    assert f(P, P2, P3, P4, None, 1, 1, 128, 128, 128, N, N, N, 0.1, None) in (CUDA, OK)
 
 
 def test_causal_validation(lib):
     f = lib.attn_causal_prefill_fwd
-    args = lambda **kw: dict(dict(B=1, Hq=6, Hkv=1, Qp=1024, Qr=1024, KV=4096, D=256), **kw)
+    args = lambda **kw: dict(dict(B=1, Hq=6, Hkv=1, Qp=1024, Qr=1024, KV=4096, D=256, flags=0,
+                                  qs=None, os=None), **kw)
 
     def call(q=P, o=P4, ws=None, wsb=0, **kw):
         a = args(**kw)
         return f(q, P2, P3, o, None, a["B"], a["Hq"], a["Hkv"], a["Qp"], a["Qr"], a["KV"], a["D"],
-                 0.0625, ws, wsb, None)
+                 a["qs"], None, a["os"], 0.0625, a["flags"], ws, wsb, None)
     assert call(q=None) == NULL
     assert call(Hq=5, Hkv=2) == SHAPE             # Hq % Hkv
     assert call(Qp=1000, Qr=1000) == SHAPE        # Q_pad % 64
@@ -107,6 +127,10 @@ def test_causal_validation(lib):
     assert call(Qp=8192, Qr=8192, KV=4096) == SHAPE   # Q_real > KV
     assert call(D=128) == UNSUPPORTED
     assert call(o=P) == ALIAS
+    assert call(flags=2) == SHAPE                 # unknown flag
+    assert call(os=_st(0, 256, 256)) == SHAPE     # output heads overlap
+    assert call(flags=1) in (CUDA, OK)
+    assert call(qs=_st(0, 256, 6 * 256), os=_st(0, 256, 6 * 256)) in (CUDA, OK)   # token-major
     assert call() in (CUDA, OK)
 
 

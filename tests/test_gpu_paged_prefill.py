@@ -18,7 +18,7 @@ def t(x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
 
-def two_ways(gb, Hq, Hkv, Q, KV, ps, ks, vs, seed, q_real=None, codes="finite"):
+def two_ways(gb, Hq, Hkv, Q, KV, ps, ks, vs, seed, q_real=None, codes="finite", split=False):
     q = inputs.causal_inputs(1, Hq, Hkv, Q, 32, 256, seed)[0]
     if codes == "finite":
         kp, vp, table = inputs.paged_e4m3_inputs(Hkv, KV, 256, seed, page_size=ps)
@@ -28,10 +28,12 @@ def two_ways(gb, Hq, Hkv, Q, KV, ps, ks, vs, seed, q_real=None, codes="finite"):
         table = tb[0]
     tq, tk, tv, tt = t(q), t(kp), t(vp), t(table)
     lse_f = torch.empty((1, Hq, Q), dtype=torch.float32, device="cuda")
-    of = gb.attn_causal_prefill_paged_fwd(tq, tk, tv, tt, KV, ks, vs, q_real=q_real, lse=lse_f)
+    of = gb.attn_causal_prefill_paged_fwd(tq, tk, tv, tt, KV, ks, vs, q_real=q_real, lse=lse_f,
+                                          prob_split=split)
     kf, vf = gb.e4m3_paged_to_fp16(tk, tv, tt, KV, ks, vs)
     lse_b = torch.empty((1, Hq, Q), dtype=torch.float32, device="cuda")
-    ob = gb.attn_causal_prefill_fwd(tq, kf[None], vf[None], q_real=q_real, lse=lse_b)
+    ob = gb.attn_causal_prefill_fwd(tq, kf[None], vf[None], q_real=q_real, lse=lse_b,
+                                    prob_split=split)
     torch.cuda.synchronize()
     assert gb.device_status() == 0
     return q, kp, vp, table, of, lse_f, ob, lse_b
@@ -45,9 +47,11 @@ def two_ways(gb, Hq, Hkv, Q, KV, ps, ks, vs, seed, q_real=None, codes="finite"):
     (6, 1, 64, 2080, 32, 0.0625, 0.125),           # KV not a multiple of 128 (ragged last tile)
     (6, 1, 128, 1536, 256, 0.0625, 0.125)])        # pages of 256 tokens (two 128-key tiles each)
 def test_fused_equals_bridge_then_prefill(gb, Hq, Hkv, Q, KV, ps, ks, vs):
-    _, _, _, _, of, lf, ob, lb = two_ways(gb, Hq, Hkv, Q, KV, ps, ks, vs, seed=90 + ps)
-    assert torch.equal(of, ob)
-    assert torch.equal(lf, lb)
+    for split in (False, True):
+        _, _, _, _, of, lf, ob, lb = two_ways(gb, Hq, Hkv, Q, KV, ps, ks, vs, seed=90 + ps,
+                                              split=split)
+        assert torch.equal(of, ob), split
+        assert torch.equal(lf, lb), split
 
 
 def test_fused_padded_queries_and_nan_codes_past_the_end(gb):
@@ -78,6 +82,20 @@ def test_fused_matches_oracle(gb):
     assert np.all(np.abs(lf.cpu().numpy() - rl) <= 2e-3 + 1e-2 * np.abs(rl))
 
 
+def test_fused_prob_split_matches_oracle_on_uniform_codes(gb):
+    """The workload's code distribution (uniform over the finite E4M3 codes, |v| up
+    to 56) with hi + lo probabilities, at the stated tolerance on every row."""
+    q, kp, vp, table, of, lf, _, _ = two_ways(gb, 6, 1, 512, 4096, 32, 0.0625, 0.125, seed=96,
+                                              split=True)
+    kb, vb = OE.paged_e4m3_to_fp16(kp, vp, table, 4096, 0.0625, 0.125)
+    k = fp16_bits_to_f64(kb).astype(np.float16)[None]
+    v = fp16_bits_to_f64(vb).astype(np.float16)[None]
+    ro, rl = OA.causal_prefill_attention(q, k, v, inputs.softmax_scale(256), 512)
+    got = of.float().cpu().numpy()
+    assert np.all(np.abs(got - ro) <= 2e-3 + 1e-2 * np.abs(ro))
+    assert np.all(np.abs(lf.cpu().numpy() - rl) <= 2e-3 + 1e-2 * np.abs(rl))
+
+
 def test_fused_bad_page_flagged(gb):
     q = inputs.causal_inputs(1, 6, 1, 64, 32, 256, 99)[0]
     kp, vp, table = inputs.paged_e4m3_inputs(1, 512, 256, 99)
@@ -94,9 +112,11 @@ def test_fused_full_workload_equals_bridge_then_prefill(gb):
     q = inputs.causal_inputs(w["B"], w["Hq"], w["Hkv"], w["Q"], 32, w["D"], w["seed"])[0]
     kp, vp, table = inputs.paged_e4m3_inputs(w["Hkv"], w["KV"], w["D"], w["seed"], w["page_size"])
     tq, tk, tv, tt = t(q), t(kp), t(vp), t(table)
-    of = gb.attn_causal_prefill_paged_fwd(tq, tk, tv, tt, w["KV"], w["k_scale"], w["v_scale"])
     kf, vf = gb.e4m3_paged_to_fp16(tk, tv, tt, w["KV"], w["k_scale"], w["v_scale"])
-    ob = gb.attn_causal_prefill_fwd(tq, kf[None], vf[None])
-    torch.cuda.synchronize()
-    assert gb.device_status() == 0
-    assert torch.equal(of, ob)
+    for split in (False, True):
+        of = gb.attn_causal_prefill_paged_fwd(tq, tk, tv, tt, w["KV"], w["k_scale"], w["v_scale"],
+                                              prob_split=split)
+        ob = gb.attn_causal_prefill_fwd(tq, kf[None], vf[None], prob_split=split)
+        torch.cuda.synchronize()
+        assert gb.device_status() == 0
+        assert torch.equal(of, ob), split
