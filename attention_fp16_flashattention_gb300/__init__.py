@@ -44,8 +44,11 @@ _SIGNATURES = {
                                    _i, _i, _f, _f, _f, _vp, _sz, _vp]),
     "vsa_select_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "vsa_select_blocks": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
-    "vsa_sparse_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
-                            _f, _vp]),
+    "vsa_sparse_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                            _i, _i, _f, _vp]),
+    "vsa_select_coarse_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "vsa_select_blocks_coarse": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _f, _vp, _vp,
+                                      _vp, _sz, _vp]),
     "vsa_pair_query_cubes": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
 }
 
@@ -380,6 +383,42 @@ def vsa_select_blocks(q, k, topk, block=64, prefix=0, cube_valid=None, idx=None,
     return idx
 
 
+def vsa_select_coarse_workspace_size(B, H, S, D, block=64):
+    return int(load().vsa_select_coarse_workspace_size(B, H, S, D, block))
+
+
+def vsa_select_blocks_coarse(q, k, v, topk, block=64, prefix=0, cube_valid=None, scale=None,
+                             idx=None, coarse=None, workspace=None, stream=None):
+    """The selection plus the coarse branch: returns (idx int32 [B,H,cubes,topk], coarse FP32
+    [B,H,cubes,D]), coarse[i] = softmax over all key cubes of scale * pooled q_i . pooled k_j,
+    times the pooled values."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.float16, 4)
+    B, H, S, D = q.shape
+    if tuple(k.shape) != tuple(q.shape) or tuple(v.shape) != tuple(q.shape):
+        raise ValueError("q, k and v must have the same shape")
+    nc = (S - int(prefix)) // block
+    if cube_valid is not None:
+        _need(cube_valid, "cube_valid", torch.int32, 1)
+    if idx is None:
+        idx = torch.empty((B, H, nc, topk), dtype=torch.int32, device=q.device)
+    if coarse is None:
+        coarse = torch.empty((B, H, nc, D), dtype=torch.float32, device=q.device)
+    _need(idx, "idx", torch.int32)
+    _need(coarse, "coarse", torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(vsa_select_coarse_workspace_size(B, H, S, D, block), 16),
+                                dtype=torch.uint8, device=q.device)
+    rc = load().vsa_select_blocks_coarse(_ptr(q), _ptr(k), _ptr(v), B, H, S, D, block, int(topk),
+                                         int(prefix), _ptr(cube_valid), _scale(scale, D), _ptr(idx),
+                                         _ptr(coarse), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream(stream))
+    _check("vsa_select_blocks_coarse", rc)
+    return idx, coarse
+
+
 def vsa_pair_query_cubes(idx, pairs=None, stream=None):
     """Query-cube pairs for vsa_sparse_fwd.  idx int32 [B,H,cubes,topk] ->
     pairs int32 [B,H,ceil(cubes/2),2] (second entry -1 for a lone cube)."""
@@ -395,10 +434,12 @@ def vsa_pair_query_cubes(idx, pairs=None, stream=None):
 
 
 def vsa_sparse_fwd(q, k, v, idx, block=64, prefix=0, cube_valid=None, pairs=None, o=None,
-                   lse=None, scale=None, stream=None):
+                   lse=None, scale=None, coarse=None, gate=None, stream=None):
     """Block-sparse attention over the cubes in idx.  q/k/v [B,H,S,D] FP16: `prefix` dense
     prefix tokens, then cube-major video tokens; cube_valid int32 [cubes] or None; pairs from
-    vsa_pair_query_cubes or None (adjacent cubes)."""
+    vsa_pair_query_cubes or None (adjacent cubes).  coarse (FP32 [B,H,cubes,D] from
+    vsa_select_blocks_coarse) and gate (FP16 [B,H,S,D]) add gate * coarse[cube] to every real
+    video token's output."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.float16, 4)
@@ -409,12 +450,17 @@ def vsa_sparse_fwd(q, k, v, idx, block=64, prefix=0, cube_valid=None, pairs=None
         _need(pairs, "pairs", torch.int32, 4)
     B, H, S, D = q.shape
     topk = idx.shape[3]
+    if (coarse is None) != (gate is None):
+        raise ValueError("coarse and gate go together")
+    if coarse is not None:
+        _need(coarse, "coarse", torch.float32, 4)
+        _need(gate, "gate", torch.float16, 4)
     o = torch.empty_like(q) if o is None else o
     _need(o, "o", torch.float16, 4)
     if lse is not None:
         _need(lse, "lse", torch.float32)
     rc = load().vsa_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(pairs), int(prefix),
-                               _ptr(cube_valid),
+                               _ptr(cube_valid), _ptr(coarse), _ptr(gate),
                                _ptr(o), _ptr(lse), B, H, S, D, block, topk, _scale(scale, D),
                                _stream(stream))
     _check("vsa_sparse_fwd", rc)

@@ -106,6 +106,8 @@ struct AttnArgs {
     const int32_t* pairs;   // sparse: [heads][ceil(n_cubes/2)][2] query-cube pairs, or null
                             //         (cubes 2p, 2p+1); a second entry of -1 means none
     const int32_t* cube_valid;   // sparse: real tokens per cube, or null (all full)
+    const float* coarse;         // sparse: coarse-branch output [heads][n_cubes][D] FP32, or null
+    const __half* gate;          // sparse: gate [heads][seq_q][D] FP16 (with coarse)
     const __half* mask; // masked: additive mask, row stride seq_k
     long long mask_sb;  // masked: elements between batch slices (0 = shared)
     long long mask_sh;  // masked: elements between head slices (0 = shared)
@@ -1125,13 +1127,35 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                 } else {
                     uint4* dst = reinterpret_cast<uint4*>(a.o + qb * a.o_sb + qh * a.o_sh +
                                                           row_g * a.o_sr + c0);
+                    float y[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) y[e] = __uint_as_float(o[e]) * inv_l;
+                    if (is_sparse(MODE) && a.coarse && row_g >= a.prefix && !pad_row) {
+                        // coarse branch: o += gate * o_coarse[cube of the row]
+                        const int cube = static_cast<int>((row_g - a.prefix) >> 6);
+                        const float4* oc = reinterpret_cast<const float4*>(
+                            a.coarse + (static_cast<long long>(bh) * a.n_cubes + cube) * D + c0);
+                        const uint4* gt = reinterpret_cast<const uint4*>(
+                            a.gate + (static_cast<long long>(bh) * a.seq_q + row_g) * D + c0);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint4 gw = gt[e];
+                            const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w};
+                            const float4 c0v = oc[2 * e], c1v = oc[2 * e + 1];
+                            const float cv[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
+#pragma unroll
+                            for (int f = 0; f < 4; ++f) {
+                                const float2 g2 = __half22float2(*reinterpret_cast<const __half2*>(&gv[f]));
+                                y[8 * e + 2 * f] = fmaf(g2.x, cv[2 * f], y[8 * e + 2 * f]);
+                                y[8 * e + 2 * f + 1] = fmaf(g2.y, cv[2 * f + 1], y[8 * e + 2 * f + 1]);
+                            }
+                        }
+                    }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         uint32_t hw[4];
 #pragma unroll
-                        for (int f = 0; f < 4; ++f)
-                            hw[f] = pack_half2(__uint_as_float(o[8 * e + 2 * f]) * inv_l,
-                                               __uint_as_float(o[8 * e + 2 * f + 1]) * inv_l);
+                        for (int f = 0; f < 4; ++f) hw[f] = pack_half2(y[8 * e + 2 * f], y[8 * e + 2 * f + 1]);
                         dst[e] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     }
                 }
@@ -1613,10 +1637,10 @@ extern "C" int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pag
 
 
 extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
-                              const int32_t* pairs, int prefix, const int32_t* cube_valid, void* o,
-                              float* lse, int B, int H, int S, int D, int block, int topk,
-                              float scale, void* stream) {
-    if (!q || !k || !v || !idx || !o) return GBATTN_ERR_NULL;
+                              const int32_t* pairs, int prefix, const int32_t* cube_valid,
+                              const float* o_coarse, const void* gate, void* o, float* lse, int B,
+                              int H, int S, int D, int block, int topk, float scale, void* stream) {
+    if (!q || !k || !v || !idx || !o || (!o_coarse) != (!gate)) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || S <= 0 || topk <= 0 || prefix < 0 || prefix >= S)
         return GBATTN_ERR_SHAPE;
     if (D != 128 || block != 64) return GBATTN_ERR_UNSUPPORTED;
@@ -1624,7 +1648,8 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
     const int nc = (S - prefix) / block;
     if (topk > nc || topk > kMaxTopk) return GBATTN_ERR_SHAPE;
     if (prefix / BM + (nc + 1) / 2 > kMaxSparseTiles) return GBATTN_ERR_SHAPE;
-    if ((reinterpret_cast<uintptr_t>(cube_valid) & 3u) || (reinterpret_cast<uintptr_t>(pairs) & 3u))
+    if ((reinterpret_cast<uintptr_t>(cube_valid) & 3u) || (reinterpret_cast<uintptr_t>(pairs) & 3u) ||
+        !aligned16(o_coarse) || !aligned16(gate))
         return GBATTN_ERR_ALIGN;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
     if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
@@ -1634,9 +1659,12 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
     const size_t xb = static_cast<size_t>(B) * H * S * D * 2;
     const size_t ib = static_cast<size_t>(B) * H * nc * topk * 4;
     const size_t lb = static_cast<size_t>(B) * H * S * 4;
+    const size_t cb = static_cast<size_t>(B) * H * nc * D * 4;
     if (overlaps(o, xb, q, xb) || overlaps(o, xb, k, xb) || overlaps(o, xb, v, xb) ||
         overlaps(o, xb, idx, ib) || overlaps(lse, lb, q, xb) || overlaps(lse, lb, k, xb) ||
-        overlaps(lse, lb, v, xb) || overlaps(lse, lb, idx, ib) || overlaps(lse, lb, o, xb))
+        overlaps(lse, lb, v, xb) || overlaps(lse, lb, idx, ib) || overlaps(lse, lb, o, xb) ||
+        overlaps(o, xb, o_coarse, cb) || overlaps(o, xb, gate, xb) || overlaps(lse, lb, o_coarse, cb) ||
+        overlaps(lse, lb, gate, xb))
         return GBATTN_ERR_ALIAS;
     DeviceState dev;
     int rc = current_device(&dev);
@@ -1653,6 +1681,8 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
     a.idx = idx;
     a.prefix = prefix;
     a.cube_valid = cube_valid;
+    a.coarse = o_coarse;
+    a.gate = static_cast<const __half*>(gate);
     a.pairs = pairs;
     a.o = static_cast<__half*>(o);
     a.lse = lse;

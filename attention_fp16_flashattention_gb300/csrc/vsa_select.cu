@@ -40,11 +40,12 @@ __global__ void __launch_bounds__(kPoolThreads) vsa_pool_kernel(
     const __half* __restrict__ q, const __half* __restrict__ k, long long n_bh, int n_cubes,
     long long seq, int prefix, int D, int block, const int32_t* __restrict__ cube_valid,
     uint32_t* status, float* __restrict__ qm, float* __restrict__ km, float* __restrict__ qn,
-    float* __restrict__ kn) {
+    float* __restrict__ kn, const __half* __restrict__ v, float* __restrict__ vm) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // score kernel may be placed
-    const __half* x = blockIdx.y == 0 ? q : k;
-    float* out = blockIdx.y == 0 ? qm : km;
-    float* out_n = blockIdx.y == 0 ? qn : kn;
+    // blockIdx.y: 0 = Q, 1 = K, 2 = V (the coarse branch's pooled values, no norm)
+    const __half* x = blockIdx.y == 0 ? q : blockIdx.y == 1 ? k : v;
+    float* out = blockIdx.y == 0 ? qm : blockIdx.y == 1 ? km : vm;
+    float* out_n = blockIdx.y == 0 ? qn : blockIdx.y == 1 ? kn : nullptr;
     const int groups = D >> 3;   // 8 channels per thread
     const long long gid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     if (gid >= n_bh * n_cubes * groups) return;
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(kPoolThreads) vsa_pool_kernel(
     const unsigned grp = 0xFFFFu << (threadIdx.x & 16u);
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) n2 += __shfl_xor_sync(grp, n2, off);
-    if (g == 0) out_n[cube] = sqrtf(n2);
+    if (g == 0 && out_n) out_n[cube] = sqrtf(n2);
 }
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -597,9 +598,9 @@ constexpr float kErrScale = 1.0f / 32768.0f;
 
 template <int CH, int CAP, bool FALLBACK>
 __global__ void __launch_bounds__(FALLBACK ? kFbWarps * 32 : kTopkWarps * 32, FALLBACK ? 1 : (CH > 16 ? 2 : 3)) vsa_topk_kernel(
-    const float* __restrict__ S, const float* __restrict__ qm, const float* __restrict__ km,
+    float* __restrict__ S, const float* __restrict__ qm, const float* __restrict__ km,
     const float* __restrict__ qn, const float* __restrict__ kn, int NC, int topk, long long rows,
-    int32_t* __restrict__ deferred, int32_t* __restrict__ idx, uint32_t* status) {
+    int32_t* __restrict__ deferred, int32_t* __restrict__ idx, uint32_t* status, float coarse_l2) {
     extern __shared__ __align__(16) uint8_t topk_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int kWarps = FALLBACK ? kFbWarps : kTopkWarps;
@@ -622,24 +623,48 @@ __global__ void __launch_bounds__(FALLBACK ? kFbWarps * 32 : kTopkWarps * 32, FA
         const long long row = FALLBACK ? base + __ffs(todo) - 1 : base;
         const long long bh = row / NC;
         int32_t* out = idx + row * topk;
+        float* srow = S + row * LD;
+        float s[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) s[c] = c * 32 + lane < NC ? srow[c * 32 + lane] : 0.0f;
+        // Coarse branch: the row's softmax over all key cubes replaces its scores
+        // once the row is decided (a row left to the fallback keeps its scores
+        // for it).  p = 2^((s - max) * scale * log2 e) / sum.
+        auto write_probs = [&]() {
+            if (coarse_l2 <= 0.0f) return;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+                if (c * 32 + lane < NC) mx = fmaxf(mx, s[c]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            float p[CH], l = 0.0f;
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                p[c] = c * 32 + lane < NC ? exp2f((s[c] - mx) * coarse_l2) : 0.0f;
+                l += p[c];
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            const float inv = 1.0f / l;
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+                if (c * 32 + lane < NC) srow[c * 32 + lane] = p[c] * inv;
+        };
         RowClass<CH> rc;
         if (topk >= NC) {   // every key
 #pragma unroll
             for (int c = 0; c < CH; ++c) rc.in_m[c] = __ballot_sync(0xffffffffu, c * 32 + lane < NC);
             if (!FALLBACK && lane == 0) deferred[row] = 0;
             write_row<CH, CAP>(rc, cb, false, NC, topk, out, status);
+            write_probs();
             continue;
         }
-        const float* srow = S + row * LD;
         const float* nkh = kn + bh * NC;
-        float s[CH];
         float nkmax = 0.0f;
 #pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const bool live = c * 32 + lane < NC;
-            s[c] = live ? srow[c * 32 + lane] : 0.0f;
-            if (live) nkmax = fmaxf(nkmax, nkh[c * 32 + lane]);
-        }
+        for (int c = 0; c < CH; ++c)
+            if (c * 32 + lane < NC) nkmax = fmaxf(nkmax, nkh[c * 32 + lane]);
         nkmax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(nkmax)));   // >= 0
         const float e = __fmul_ru(__fmul_ru(qn[row], nkmax), kErrScale);
         classify_row<CH>(s, NC, topk, e, rc, cb->hist, cb->list);
@@ -654,6 +679,7 @@ __global__ void __launch_bounds__(FALLBACK ? kFbWarps * 32 : kTopkWarps * 32, FA
         }
         if (!FALLBACK && lane == 0) deferred[row] = 0;
         write_row<CH, CAP>(rc, cb, need > 0, NC, topk, out, status);
+        write_probs();
         __syncwarp();
         }
     }
@@ -661,6 +687,88 @@ __global__ void __launch_bounds__(FALLBACK ? kFbWarps * 32 : kTopkWarps * 32, FA
 
 template <int CH, int CAP, int WARPS>
 constexpr size_t topk_smem_bytes() { return sizeof(Cands<CAP>) * WARPS; }
+
+// ---------------------------------------------------------------- coarse branch
+//
+// O_c[bh] = P[bh] Vm[bh]: the probabilities of every query cube over all key
+// cubes ([NC][NC], row stride score_ld(NC)) times the pooled values ([NC][128]),
+// FP32 FFMA.  One 64 (query cubes) x 128 (dims) tile per CTA, 128 threads with
+// 8 x 8 register tiles (rows 4ty.., 32+4ty.., dims 4tx.., 64+4tx..); the key
+// dimension passes through shared memory eight keys at a time (P stored
+// key-major, Vm row-major), the next eight loaded into registers meanwhile.
+constexpr int kPvM = 64;
+constexpr int kPvThreads = 128;
+
+__global__ void __launch_bounds__(kPvThreads) vsa_coarse_pv_kernel(const float* __restrict__ P,
+                                                                   const float* __restrict__ vm,
+                                                                   int NC, float* __restrict__ oc) {
+    __shared__ __align__(16) float As[2][kGK][kPvM + 4];
+    __shared__ __align__(16) float Bs[2][kGK][kSelD];
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // probabilities of the top-k kernels
+    const int t = threadIdx.x;
+    const long long bh = blockIdx.y;
+    const int m0 = blockIdx.x * kPvM;
+    const int LD = score_ld(NC);
+    const int ar = t >> 1, ak = (t & 1) * 4;          // P: row ar, keys ak..ak+3 of a stage
+    const int bk = t >> 4, bd = (t & 15) * 4;         // Vm: key bk, dims bd.. and 64+bd..
+    const bool a_live = m0 + ar < NC;
+    const float* a_src = P + (bh * NC + m0 + ar) * LD + ak;
+    const float* b_src = vm + bh * NC * kSelD;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 ra, rb0, rb1;
+    auto load = [&](int kc) {
+        ra = (a_live && kc + ak < NC) ? *reinterpret_cast<const float4*>(a_src + kc) : zero;
+        const bool bl = kc + bk < NC;
+        rb0 = bl ? *reinterpret_cast<const float4*>(b_src + static_cast<long long>(kc + bk) * kSelD + bd) : zero;
+        rb1 = bl ? *reinterpret_cast<const float4*>(b_src + static_cast<long long>(kc + bk) * kSelD + 64 + bd)
+                 : zero;
+    };
+    auto stage = [&](int buf) {
+        As[buf][ak + 0][ar] = ra.x; As[buf][ak + 1][ar] = ra.y;
+        As[buf][ak + 2][ar] = ra.z; As[buf][ak + 3][ar] = ra.w;
+        *reinterpret_cast<float4*>(&Bs[buf][bk][bd]) = rb0;
+        *reinterpret_cast<float4*>(&Bs[buf][bk][64 + bd]) = rb1;
+    };
+    load(0);
+    stage(0);
+    __syncthreads();
+    const int ty = t >> 4, tx = t & 15;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    const int nch = (NC + kGK - 1) / kGK;
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+        const int buf = ch & 1;
+        if (ch + 1 < nch) load((ch + 1) * kGK);
+#pragma unroll
+        for (int kk = 0; kk < kGK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][32 + 4 * ty]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + 4 * tx]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        if (ch + 1 < nch) stage(buf ^ 1);
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = m0 + (i < 4 ? 4 * ty + i : 32 + 4 * ty + i - 4);
+        if (row >= NC) continue;
+        float* dst = oc + (bh * NC + row) * kSelD;
+        *reinterpret_cast<float4*>(dst + 4 * tx) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        *reinterpret_cast<float4*>(dst + 64 + 4 * tx) =
+            make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
+}
 
 }  // namespace
 }  // namespace gbattn
@@ -673,6 +781,7 @@ namespace {
 // row, and the FP32 scores [rows][score_ld(NC)] (rows = B*H*NC query cubes).
 struct SelectLayout {
     size_t qm, km, qn, kn, flags, scores, total;
+    size_t vm, total_coarse;   // the coarse branch adds the pooled values
 };
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 SelectLayout select_layout(size_t rows, int NC, int D) {
@@ -684,6 +793,8 @@ SelectLayout select_layout(size_t rows, int NC, int D) {
     L.flags = L.kn + align256(rows * sizeof(float));
     L.scores = L.flags + align256(rows * sizeof(int32_t));
     L.total = L.scores + rows * static_cast<size_t>(score_ld(NC)) * sizeof(float);
+    L.vm = align256(L.total);
+    L.total_coarse = L.vm + rows * D * sizeof(float);
     return L;
 }
 }  // namespace
@@ -694,11 +805,20 @@ extern "C" size_t vsa_select_workspace_size(int B, int H, int S, int D, int bloc
     return select_layout(static_cast<size_t>(B) * H * nc, nc, D).total;
 }
 
-extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D,
-                                 int block, int topk, int prefix, const int32_t* cube_valid,
-                                 int32_t* idx, void* workspace, size_t workspace_bytes,
-                                 void* stream) {
-    if (!q || !k || !idx) return GBATTN_ERR_NULL;
+extern "C" size_t vsa_select_coarse_workspace_size(int B, int H, int S, int D, int block) {
+    if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return 0;
+    const int nc = S / block;
+    return select_layout(static_cast<size_t>(B) * H * nc, nc, D).total_coarse;
+}
+
+namespace {
+// The selection (v == nullptr) or the selection plus the coarse branch.
+int select_impl(const void* q, const void* k, const void* v, int B, int H, int S, int D,
+                int block, int topk, int prefix, const int32_t* cube_valid, float scale,
+                int32_t* idx, float* o_coarse, void* workspace, size_t workspace_bytes,
+                void* stream) {
+    const bool coarse = v != nullptr;
+    if (!q || !k || !idx || (coarse && !o_coarse)) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || S <= 0 || topk <= 0 || prefix < 0 || prefix >= S)
         return GBATTN_ERR_SHAPE;
     if (D != 128 || block != 64) return GBATTN_ERR_UNSUPPORTED;
@@ -706,16 +826,23 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     const int NC = (S - prefix) / block;
     if (NC > kMaxChunks * 32 || topk > NC) return GBATTN_ERR_SHAPE;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
-    const size_t need = vsa_select_workspace_size(B, H, S, D, block);
+    if (coarse && !finite_positive(scale)) return GBATTN_ERR_SCALE;
+    const size_t need = coarse ? vsa_select_coarse_workspace_size(B, H, S, D, block)
+                               : vsa_select_workspace_size(B, H, S, D, block);
     if (!workspace || workspace_bytes < need) return GBATTN_ERR_WORKSPACE;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(workspace) ||
-        (reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(cube_valid) & 3u))
+    if (!aligned16(q) || !aligned16(k) || !aligned16(workspace) || !aligned16(v) ||
+        !aligned16(o_coarse) || (reinterpret_cast<uintptr_t>(idx) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cube_valid) & 3u))
         return GBATTN_ERR_ALIGN;
     const size_t in_bytes = static_cast<size_t>(B) * H * S * D * 2;
     const size_t idx_bytes = static_cast<size_t>(B) * H * NC * topk * 4;
+    const size_t oc_bytes = static_cast<size_t>(B) * H * NC * D * 4;
     if (overlaps(idx, idx_bytes, q, in_bytes) || overlaps(idx, idx_bytes, k, in_bytes) ||
         overlaps(workspace, need, q, in_bytes) || overlaps(workspace, need, k, in_bytes) ||
-        overlaps(workspace, need, idx, idx_bytes))
+        overlaps(workspace, need, idx, idx_bytes) || overlaps(idx, idx_bytes, v, in_bytes) ||
+        overlaps(workspace, need, v, in_bytes) || overlaps(o_coarse, oc_bytes, q, in_bytes) ||
+        overlaps(o_coarse, oc_bytes, k, in_bytes) || overlaps(o_coarse, oc_bytes, v, in_bytes) ||
+        overlaps(o_coarse, oc_bytes, idx, idx_bytes) || overlaps(o_coarse, oc_bytes, workspace, need))
         return GBATTN_ERR_ALIAS;
     DeviceState dev;
     int rc = current_device(&dev);
@@ -732,6 +859,8 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     float* kn = reinterpret_cast<float*>(ws + L.kn);
     int32_t* deferred = reinterpret_cast<int32_t*>(ws + L.flags);
     float* scores = reinterpret_cast<float*>(ws + L.scores);
+    float* vm = coarse ? reinterpret_cast<float*>(ws + L.vm) : nullptr;
+    const float coarse_l2 = coarse ? scale * 1.4426950408889634f : 0.0f;
 
     static std::once_flag attr_once[64];
     static int attr_rc[64];
@@ -752,11 +881,11 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     }
 
     const long long pool_threads = rows * (D / 8);
-    dim3 pgrid(static_cast<unsigned>((pool_threads + kPoolThreads - 1) / kPoolThreads), 2);
+    dim3 pgrid(static_cast<unsigned>((pool_threads + kPoolThreads - 1) / kPoolThreads), coarse ? 3 : 2);
     vsa_pool_kernel<<<pgrid, kPoolThreads, 0, s>>>(static_cast<const __half*>(q),
                                                    static_cast<const __half*>(k), n_bh, NC, S,
                                                    prefix, D, block, cube_valid, dev.status, qm,
-                                                   km, qn, kn);
+                                                   km, qn, kn, static_cast<const __half*>(v), vm);
     count_launches(1);
     if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
 
@@ -788,12 +917,12 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     cudaError_t e;
     if (NC <= 512) {
         cfg.dynamicSmemBytes = topk_smem_bytes<16, kCap, kTopkWarps>();
-        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<16, kCap, false>, cs, cqm, ckm, cqn, ckn, NC,
-                               topk, rows, deferred, idx, dev.status);
+        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<16, kCap, false>, scores, cqm, ckm, cqn, ckn, NC,
+                               topk, rows, deferred, idx, dev.status, coarse_l2);
     } else {
         cfg.dynamicSmemBytes = topk_smem_bytes<32, kCap, kTopkWarps>();
-        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<32, kCap, false>, cs, cqm, ckm, cqn, ckn, NC,
-                               topk, rows, deferred, idx, dev.status);
+        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<32, kCap, false>, scores, cqm, ckm, cqn, ckn, NC,
+                               topk, rows, deferred, idx, dev.status, coarse_l2);
     }
     if (!launched(e)) return GBATTN_ERR_CUDA;
     const long long fb_ctas = std::min<long long>((rows + 32 * kFbWarps - 1) / (32 * kFbWarps),
@@ -802,15 +931,42 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
     cfg.blockDim = dim3(kFbWarps * 32);
     if (NC <= 512) {
         cfg.dynamicSmemBytes = topk_smem_bytes<16, 512, kFbWarps>();
-        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<16, 512, true>, cs, cqm, ckm, cqn, ckn, NC,
-                               topk, rows, deferred, idx, dev.status);
+        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<16, 512, true>, scores, cqm, ckm, cqn, ckn, NC,
+                               topk, rows, deferred, idx, dev.status, coarse_l2);
     } else {
         cfg.dynamicSmemBytes = topk_smem_bytes<32, 1024, kFbWarps>();
-        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<32, 1024, true>, cs, cqm, ckm, cqn, ckn, NC,
-                               topk, rows, deferred, idx, dev.status);
+        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<32, 1024, true>, scores, cqm, ckm, cqn, ckn, NC,
+                               topk, rows, deferred, idx, dev.status, coarse_l2);
     }
     if (!launched(e)) return GBATTN_ERR_CUDA;
+    if (coarse) {
+        cfg.gridDim = dim3(static_cast<unsigned>((NC + kPvM - 1) / kPvM), static_cast<unsigned>(n_bh));
+        cfg.blockDim = dim3(kPvThreads);
+        cfg.dynamicSmemBytes = 0;
+        const float* cvm = vm;
+        if (!launched(cudaLaunchKernelEx(&cfg, vsa_coarse_pv_kernel, cs, cvm, NC, o_coarse)))
+            return GBATTN_ERR_CUDA;
+    }
     return launch_status();
+}
+}  // namespace
+
+extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D,
+                                 int block, int topk, int prefix, const int32_t* cube_valid,
+                                 int32_t* idx, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    return select_impl(q, k, nullptr, B, H, S, D, block, topk, prefix, cube_valid, 0.0f, idx,
+                       nullptr, workspace, workspace_bytes, stream);
+}
+
+extern "C" int vsa_select_blocks_coarse(const void* q, const void* k, const void* v, int B, int H,
+                                        int S, int D, int block, int topk, int prefix,
+                                        const int32_t* cube_valid, float scale, int32_t* idx,
+                                        float* o_coarse, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+    if (!v) return GBATTN_ERR_NULL;
+    return select_impl(q, k, v, B, H, S, D, block, topk, prefix, cube_valid, scale, idx, o_coarse,
+                       workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------ query-cube pairing

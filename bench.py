@@ -675,12 +675,71 @@ def measure_vsa_full(gb, torch, dev, steps, warmup, pk):
     t_sp = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     tf = flops / ((t_sel + t_sp) * 1e-3) / 1e12
     peak = pk["tc"] or pk["tc_sust"]
-    return {"kernel": "vsa_pool+vsa_score_topk+attn_fwd_kernel<128,sparse_full>", "bound": "tensor",
+    return {"kernel": "vsa_pool+vsa_score+vsa_topk+attn_fwd_kernel<128,sparse_full>", "bound": "tensor",
             "achieved": tf, "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
             "peak_source": f"{pk['src']} bf16 burst (timed alone; fp16 dense rate = bf16 rate)",
             "ms_select": t_sel, "ms_sparse": t_sp, "sparse_tflops": flops / (t_sp * 1e-3) / 1e12,
             "useful_flop": flops, "real_tokens": real, "slots": S,
             "config": {k2: v2 for k2, v2 in w.items() if k2 != "seed"},
+            "l2": "256 MB buffer rewritten between calls, outside the timed events"}
+
+
+def measure_vsa_coarse(gb, torch, dev, steps, warmup, pk):
+    """The VSA workload with the coarse branch: vsa_select_blocks_coarse (selection,
+    pooled V, cube-level attention over all key cubes) and the sparse attention
+    adding gate * coarse output, beside the selection and sparse attention alone.
+    Useful FLOP: the fine branch's selected pairs plus the coarse attention's
+    4 * D * cubes^2 per head.  A 256 MB buffer is rewritten between calls."""
+    w = inputs.WORKLOADS["vsa_video"]
+    q, k, v = host_inputs("vsa_video")
+    T = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    dq, dk, dv = T(q), T(k), T(v)
+    gate = torch.empty_like(dq).uniform_(-1.0, 1.0)
+    B, H, S, D = dq.shape
+    nc = S // 64
+    idx = torch.empty((B, H, nc, w["topk"]), dtype=torch.int32, device=dev)
+    oc = torch.empty((B, H, nc, D), dtype=torch.float32, device=dev)
+    pairs = torch.empty((B, H, (nc + 1) // 2, 2), dtype=torch.int32, device=dev)
+    ws = torch.empty(gb.vsa_select_coarse_workspace_size(B, H, S, D, 64), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty_like(dq)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    calls = {
+        "select_coarse": lambda: gb.vsa_select_blocks_coarse(dq, dk, dv, w["topk"], idx=idx,
+                                                             coarse=oc, workspace=ws),
+        "select": lambda: gb.vsa_select_blocks(dq, dk, w["topk"], idx=idx, workspace=ws),
+        "sparse_gated": lambda: (gb.vsa_pair_query_cubes(idx, pairs=pairs),
+                                 gb.vsa_sparse_fwd(dq, dk, dv, idx, pairs=pairs, o=o, coarse=oc,
+                                                   gate=gate)),
+        "sparse": lambda: (gb.vsa_pair_query_cubes(idx, pairs=pairs),
+                           gb.vsa_sparse_fwd(dq, dk, dv, idx, pairs=pairs, o=o)),
+    }
+    res = {}
+    for name, fn in calls.items():
+        for _ in range(warmup):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    if gb.device_status() != 0:
+        raise RuntimeError("device status flags set during the coarse-branch measurement")
+    flops = vsa_flops(B, H, S, D, w["topk"]) + 4.0 * D * nc * nc * B * H
+    t = res["select_coarse"] + res["sparse_gated"]
+    tf = flops / (t * 1e-3) / 1e12
+    peak = pk["tc"] or pk["tc_sust"]
+    return {"kernel": "vsa_pool+vsa_score+vsa_topk+vsa_coarse_pv+attn_fwd_kernel<128,sparse>",
+            "bound": "tensor", "achieved": tf, "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
+            "peak_source": f"{pk['src']} bf16 burst (timed alone; fp16 dense rate = bf16 rate)",
+            "ms_select_coarse": res["select_coarse"], "ms_select": res["select"],
+            "ms_sparse_gated": res["sparse_gated"], "ms_sparse": res["sparse"],
+            "useful_flop": flops,
             "l2": "256 MB buffer rewritten between calls, outside the timed events"}
 
 
@@ -766,6 +825,8 @@ def main():
                     help="dense attention with an additive mask measured beside the step")
     ap.add_argument("--vsa-full", default="on", choices=["on", "off", "only"],
                     help="the full VSA layout (prefix + boundary cubes) measured beside the step")
+    ap.add_argument("--vsa-coarse", default="on", choices=["on", "off", "only"],
+                    help="the VSA workload with the coarse (compression) branch")
     ap.add_argument("--paged-fused", default="on", choices=["on", "off", "only"],
                     help="the paged prefill with the bridge fused in, beside bridge + prefill")
     ap.add_argument("--small", default="on", choices=["on", "off"],
@@ -806,6 +867,13 @@ def main():
                                   n_gpus=world, steps=args.steps, warmup=args.warmup,
                                   **measure_paged_fused(gb, torch, dev, args.steps, args.warmup,
                                                         peaks()))))
+        return 0
+    if args.vsa_coarse == "only":
+        if rank == 0:
+            print(json.dumps(dict(metric="VSA with the coarse branch useful TFLOP/s", impl="ours",
+                                  n_gpus=world, steps=args.steps, warmup=args.warmup,
+                                  **measure_vsa_coarse(gb, torch, dev, args.steps, args.warmup,
+                                                       peaks()))))
         return 0
     if args.vsa_full == "only":
         if rank == 0:
@@ -1029,6 +1097,8 @@ def main():
         extra["paged_fused"] = measure_paged_fused(gb, torch, dev, args.steps, args.warmup, pk)
     if args.vsa_full == "on" and args.workload == "all":
         extra["vsa_full"] = measure_vsa_full(gb, torch, dev, args.steps, args.warmup, pk)
+    if args.vsa_coarse == "on" and args.workload == "all":
+        extra["vsa_coarse"] = measure_vsa_coarse(gb, torch, dev, args.steps, args.warmup, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -294,6 +294,26 @@ int vsa_select_blocks(const void* q, const void* k, int B, int H, int S, int D, 
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The selection plus the coarse ("compression") branch of VSA.
+ * Cites: "Integrate H3 SM70 execution, metrics and VSA diagnostics", Purpose (VSA with
+ * learned compression); FastVideo compare view, minimax_h3_fusions/kv_pool.py (the values
+ * pooled per tile like the keys: FP32 sum / count).  The pages do not print the attention
+ * that consumes the pooled values; this is the cube-level attention of the VSA design:
+ *   v     : [B][H][S][D] FP16, pooled like q and k (same prefix, cubes and counts)
+ *   o_coarse: FP32 [B][H][(S-prefix)/block][D]: for query cube i,
+ *           o_coarse[i] = sum_j softmax_j(scale * qm_i . km_j) vm_j over ALL key cubes j
+ *           (qm, km, vm the FP32 cube means; FP32 scores, softmax and accumulation).
+ *   idx and every other argument as for vsa_select_blocks; scale finite, > 0.
+ *   Workspace: vsa_select_coarse_workspace_size() (vsa_select_blocks' plus the pooled values).
+ * The gate that mixes o_coarse into the fine output is the caller's (see vsa_sparse_fwd).
+ */
+size_t vsa_select_coarse_workspace_size(int B, int H, int S, int D, int block);
+int vsa_select_blocks_coarse(const void* q, const void* k, const void* v, int B, int H, int S,
+                             int D, int block, int topk, int prefix, const int32_t* cube_valid,
+                             float scale, int32_t* idx, float* o_coarse, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
  * vsa_select_blocks for callers that cannot allocate device memory.  The pages
  * have no counterpart; this entry point exists for callers such as a plugin
  * whose host program fixed its memory at start-up and forbids later
@@ -339,13 +359,18 @@ int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S,
  *   video query in cube c attends exactly the real tokens of cubes idx[b][h][c][*]; a padding
  *   query slot gets O = 0, lse = -inf.  Padding slots of V must hold finite values (their
  *   weight is exactly zero).
+ *   o_coarse, gate: both NULL, or the coarse branch ("learned compression" of the same VSA
+ *   page): o_coarse FP32 [B][H][(S-prefix)/block][D] from vsa_select_blocks_coarse and gate
+ *   FP16 [B][H][S][D] (the caller's learned gate); every real video token then gets
+ *   O = O_fine + gate * o_coarse[its cube], elementwise, before the FP16 rounding (lse stays
+ *   the fine branch's).  Prefix tokens and padding slots are unchanged.
  *   block == 64, D == 128, prefix % 128 == 0, (S - prefix) % block == 0,
  *   1 <= topk <= min((S-prefix)/block, 512), prefix/128 + ceil(cubes/2) <= 512.
  */
 int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
-                   const int32_t* pairs, int prefix, const int32_t* cube_valid, void* o,
-                   float* lse, int B, int H, int S, int D, int block, int topk, float scale,
-                   void* stream);
+                   const int32_t* pairs, int prefix, const int32_t* cube_valid,
+                   const float* o_coarse, const void* gate, void* o, float* lse, int B, int H,
+                   int S, int D, int block, int topk, float scale, void* stream);
 
 /*
  * Pairs the video query cubes of every head for vsa_sparse_fwd, which runs two query cubes per

@@ -225,16 +225,30 @@ def test_select_and_sparse_validation(lib):
     assert f(P, P2, 1, 24, 32768, 128, 64, 64, 0, MIS2, P3, P4, ws, None) == ALIGN
     assert f(P, P2, 1, 24, 32768, 128, 64, 64, 0, None, P3, P4, ws, None) in (CUDA, OK)
     g = lib.vsa_sparse_fwd
-    # q, k, v, idx, pairs, prefix, cube_valid, o, lse, B, H, S, D, block, topk, scale, stream
+    # q, k, v, idx, pairs, prefix, cube_valid, coarse, gate, o, lse, B, H, S, D, block, topk,
+    # scale, stream
     I = ctypes.c_void_p(0x70000000)
-    assert g(P, P2, P3, P4, None, 0, None, None, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == NULL
-    assert g(P, P2, P3, I, None, 0, None, P, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == ALIAS
-    assert g(P, P2, P3, I, None, 0, None, P4, None, 1, 24, 32768, 128, 64, 600, 0.08, None) == SHAPE
-    assert g(P, P2, P3, I, None, 64, None, P4, None, 1, 24, 32768 + 64, 128, 64, 64, 0.08,
+    N = None
+    assert g(P, P2, P3, P4, N, 0, N, N, N, None, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == NULL
+    assert g(P, P2, P3, I, N, 0, N, N, N, P, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == ALIAS
+    assert g(P, P2, P3, I, N, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 600, 0.08, None) == SHAPE
+    assert g(P, P2, P3, I, N, 64, N, N, N, P4, None, 1, 24, 32768 + 64, 128, 64, 64, 0.08,
              None) == SHAPE                        # prefix must be whole 128-row query tiles
-    assert g(P, P2, P3, I, None, 128, MIS2, P4, None, 1, 24, 32768 + 128, 128, 64, 64, 0.08,
+    assert g(P, P2, P3, I, N, 128, MIS2, N, N, P4, None, 1, 24, 32768 + 128, 128, 64, 64, 0.08,
              None) == ALIGN
-    assert g(P, P2, P3, I, MIS2, 0, None, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == ALIGN
+    assert g(P, P2, P3, I, MIS2, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == ALIGN
+    C = ctypes.c_void_p(0x78000000)
+    assert g(P, P2, P3, I, N, 0, N, C, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08,
+             None) == NULL                         # coarse without a gate
+    assert g(P, P2, P3, I, N, 0, N, C, P4, P4, None, 1, 24, 32768, 128, 64, 64, 0.08,
+             None) == ALIAS                        # output over the gate
+    c = lib.vsa_select_blocks_coarse
+    ws = lib.vsa_select_coarse_workspace_size(1, 24, 32768, 128, 64)
+    assert ws == lib.vsa_select_workspace_size(1, 24, 32768, 128, 64) + 24 * 512 * 128 * 4
+    assert c(P, P2, None, 1, 24, 32768, 128, 64, 64, 0, N, 0.08, P3, C, P4, ws, None) == NULL
+    assert c(P, P2, I, 1, 24, 32768, 128, 64, 64, 0, N, 0.0, P3, C, P4, ws, None) == SCALE
+    assert c(P, P2, I, 1, 24, 32768, 128, 64, 64, 0, N, 0.08, P3, C, P4, ws - 1, None) == WORKSPACE
+    assert c(P, P2, I, 1, 24, 32768, 128, 64, 64, 0, N, 0.08, P3, P, P4, ws, None) == ALIAS
     h = lib.vsa_pair_query_cubes
     assert h(None, 1, 24, 512, 64, P4, None) == NULL
     assert h(I, 1, 24, 2048, 64, P4, None) == SHAPE     # more cubes than the pairing takes
