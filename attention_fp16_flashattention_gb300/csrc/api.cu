@@ -49,6 +49,11 @@ int current_device(DeviceState* out) {
 }
 
 uint64_t wait_limit_ns() { return g_wait_limit.load(); }
+
+namespace {
+std::atomic<int> g_fault_mode{0};   // test hook, see gbattn_test_inject_fault
+}
+int fault_mode() { return g_fault_mode.load(); }
 void count_launches(int n) { g_launches += static_cast<uint64_t>(n); }
 
 namespace {
@@ -159,3 +164,9 @@ extern "C" int gbattn_set_wait_limit_ns(uint64_t limit_ns) {
 }
 
 extern "C" uint64_t gbattn_launch_count(void) { return g_launches.load(); }
+
+extern "C" int gbattn_test_inject_fault(int mode) {
+    if (mode < 0 || mode > 2) return GBATTN_ERR_SHAPE;
+    g_fault_mode = mode;
+    return GBATTN_OK;
+}

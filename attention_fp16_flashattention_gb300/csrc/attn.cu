@@ -1276,11 +1276,10 @@ int launch_attn(const void* q, const void* k, const void* v, int seq_q, int seq_
     return launch_status();
 }
 
-int g_fault_mode = 0;   // test hook, see gbattn_test_inject_fault
 
 AttnArgs base_args(const DeviceState& dev, float scale) {
     AttnArgs a{};
-    a.fault = g_fault_mode;
+    a.fault = fault_mode();
     a.scale_log2 = scale * 1.4426950408889634f;
     a.scale = scale;
     a.status = dev.status;
@@ -1342,11 +1341,7 @@ int sm_count_or_default() {
 
 using namespace gbattn;
 
-extern "C" int gbattn_test_inject_fault(int mode) {
-    if (mode < 0 || mode > 2) return GBATTN_ERR_SHAPE;
-    g_fault_mode = mode;
-    return GBATTN_OK;
-}
+
 
 extern "C" int attn_dense_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                               int B, int H, int Sq, int Skv, int D, const int64_t* q_strides,

@@ -77,6 +77,7 @@ struct DecodeArgs {
     uint32_t* prefix_out; // [B + 1]: tiles of all streams of the sequences before b
     uint32_t* status;
     uint64_t wait_limit;
+    int fault;   // test hook: 1 = no stage is loaded, 2 = loads stop after two ring rounds
     int B, Hq, Hkv, nq, G, row_groups, num_phys, ps, max_pages, max_kv;
     float sl2;            // softmax scale * log2(e) (* k_scale when folded)
     float ks, vs;
@@ -253,10 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     const uint32_t n_tiles = u_end - u_beg;
+    // test hook: the waits for stages never loaded run out (bounded) mid-range
+    const uint32_t n_load = a.fault == 1 ? 0u
+                            : a.fault == 2 ? min(n_tiles, static_cast<uint32_t>(2 * C::kStages))
+                                           : n_tiles;
     long long src_cur = tile_src(u_beg + lane);          // tiles 0..31 of the range, one per lane
     long long src_next = tile_src(u_beg + 32 + lane);    // tiles 32..63
     uint32_t issued = 0;
-    for (; issued < static_cast<uint32_t>(C::kStages - 1) && issued < n_tiles; ++issued)
+    for (; issued < static_cast<uint32_t>(C::kStages - 1) && issued < n_load; ++issued)
         issue(issued, __shfl_sync(0xffffffffu, src_cur, issued));
 
     const int g = lane >> 2, c = lane & 3;
@@ -302,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool aborted = false;
     for (uint32_t k = 0; k < n_tiles; ++k) {
         // keep the ring kStages - 1 tiles ahead
-        if (issued < n_tiles) {
+        if (issued < n_load) {
             if ((issued & 31u) == 0) {
                 src_cur = src_next;
                 src_next = tile_src(u_beg + issued + 32 + lane);
@@ -755,6 +760,7 @@ extern "C" int attn_paged_decode_fwd(const void* q, const uint8_t* k_pages, cons
     a.prefix_out = reinterpret_cast<uint32_t*>(a.part_ml + n_rec * kRows);
     a.status = dev.status;
     a.wait_limit = wait_limit_ns();
+    a.fault = fault_mode();
     a.B = B;
     a.Hq = Hq;
     a.Hkv = Hkv;

@@ -22,6 +22,9 @@ struct DeviceState {
 int current_device(DeviceState* out);
 
 uint64_t wait_limit_ns();
+// Test hook of the bounded waits (gbattn_test_inject_fault): 0 normal, 1 nothing
+// loaded, 2 loads stop mid-stream.
+int fault_mode();
 void count_launches(int n);
 
 // Encode a 4-D FP16 tensor map over [B][H][S][D] heads with element strides

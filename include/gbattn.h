@@ -117,10 +117,13 @@ uint64_t gbattn_launch_count(void);
  * attention launch skip its query-tile load, so its first pipeline wait runs
  * out after gbattn_set_wait_limit_ns(); mode 2 makes the load warp stop after
  * the first two rounds of its K/V ring (waiting for the copies it issued), so
- * the waits run out mid-stream with tensor-core work in flight.  Either way the
- * kernel records GBATTN_DEV_WAIT_TIMEOUT, lets its copies and MMAs finish, frees
- * its tensor memory and returns (outputs are then undefined).  mode 0 (default)
- * restores normal operation.  Returns GBATTN_OK or GBATTN_ERR_SHAPE. */
+ * the waits run out mid-stream with tensor-core work in flight (in the fused
+ * paged prefill, the E4M3 converter warps' waits run out too).  In the paged
+ * decode, mode 1 makes every warp load no stage and mode 2 stop after two
+ * rounds of its own ring.  Either way the kernel records
+ * GBATTN_DEV_WAIT_TIMEOUT, lets its copies and MMAs finish, frees its tensor
+ * memory and returns (outputs are then undefined).  mode 0 (default) restores
+ * normal operation.  Returns GBATTN_OK or GBATTN_ERR_SHAPE. */
 int gbattn_test_inject_fault(int mode);
 
 /*

@@ -87,3 +87,77 @@ def test_mid_stream_timeout_causal_one_issuer(gb):
     ro, _ = OA.causal_prefill_attention(q, k, v, inputs.softmax_scale(256), 256)
     assert _close(gb.attn_causal_prefill_fwd(tq, tk, tv), ro)
     assert gb.device_status() == 0
+
+
+def test_mid_stream_timeout_sparse_and_full_layout(gb):
+    from oracle import vsa as OV
+    q, k, v = inputs.vsa_inputs(1, 2, 128, seed=65, grid=(4, 32, 32))
+    tq, tk, tv = (torch.from_numpy(x).cuda() for x in (q, k, v))
+    idx = gb.vsa_select_blocks(tq, tk, topk=8)
+    for mode in (1, 2):
+        assert gb.device_status() == 0
+        gb.set_wait_limit_ns(50_000_000)
+        gb.test_inject_fault(mode)
+        try:
+            gb.vsa_sparse_fwd(tq, tk, tv, idx)
+            flags = gb.device_status()
+        finally:
+            gb.test_inject_fault(0)
+            gb.set_wait_limit_ns(1_000_000_000)
+        assert flags & gb.DEV_WAIT_TIMEOUT, mode
+    ro, _ = OA.vsa_sparse_attention(q, k, v, OV.vsa_select(q, k, 64, 8), 64, inputs.softmax_scale(128))
+    assert _close(gb.vsa_sparse_fwd(tq, tk, tv, idx), ro)
+    # the full layout (prefix query tiles walk every prefix key tile)
+    q, k, v, valid = inputs.vsa_full_inputs(1, 2, 128, seed=66, grid=(5, 10, 9), prefix=256)
+    tq, tk, tv, tval = (torch.from_numpy(x).cuda() for x in (q, k, v, valid))
+    idx = gb.vsa_select_blocks(tq, tk, 5, prefix=256, cube_valid=tval)
+    call = lambda: gb.vsa_sparse_fwd(tq, tk, tv, idx, prefix=256, cube_valid=tval)
+    assert _mid_stream_abort(gb, call) & gb.DEV_WAIT_TIMEOUT
+    ro, _ = OA.vsa_sparse_attention(q, k, v, idx.cpu().numpy(), 64, inputs.softmax_scale(128),
+                                    valid=valid, prefix=256)
+    assert _close(call(), ro)
+    assert gb.device_status() == 0
+
+
+def test_mid_stream_timeout_paged_converter_warps(gb):
+    """The fused paged prefill: the load warp stops after two ring rounds, so the
+    E4M3 converter warps' waits for page bytes run out as well as the MMA and
+    softmax warps' waits."""
+    q = inputs.causal_inputs(1, 6, 1, 256, 32, 256, 67)[0]
+    kp, vp, table = inputs.paged_e4m3_inputs(1, 2048, 256, 67, page_size=32)
+    tq, tk, tv, tt = (torch.from_numpy(x).cuda() for x in (q, kp, vp, table))
+    for split in (False, True):
+        call = lambda: gb.attn_causal_prefill_paged_fwd(tq, tk, tv, tt, 2048, 0.0625, 0.125,
+                                                        prob_split=split)
+        assert _mid_stream_abort(gb, call) & gb.DEV_WAIT_TIMEOUT, split
+        kf, vf = gb.e4m3_paged_to_fp16(tk, tv, tt, 2048, 0.0625, 0.125)
+        ref = gb.attn_causal_prefill_fwd(tq, kf[None], vf[None], prob_split=split)
+        assert torch.equal(call(), ref)
+    assert gb.device_status() == 0
+
+
+def test_timeout_paged_decode(gb):
+    """The decode warps run their own rings: with nothing loaded (mode 1) or the
+    loads stopping after two ring rounds (mode 2) their waits run out, each warp
+    waits for the stages it issued and returns; the merge still completes."""
+    from oracle import decode as OD
+    # the tiles are split evenly over every warp of the GPU (8 per SM): about 7000
+    # tiles leave each warp more than two rounds of its ring for mode 2 to cut
+    q, kp, vp, table, lens = inputs.paged_decode_inputs(2, 6, 1, 1, (65536, 49152), 256, seed=68)
+    args = [torch.from_numpy(x).cuda() for x in (q, kp, vp, table, lens)]
+    for mode in (1, 2):
+        assert gb.device_status() == 0
+        gb.set_wait_limit_ns(50_000_000)
+        gb.test_inject_fault(mode)
+        try:
+            gb.attn_paged_decode_fwd(*args, 0.0625, 0.125)
+            flags = gb.device_status()
+        finally:
+            gb.test_inject_fault(0)
+            gb.set_wait_limit_ns(1_000_000_000)
+        assert flags & gb.DEV_WAIT_TIMEOUT, mode
+    o = gb.attn_paged_decode_fwd(*args, 0.0625, 0.125)
+    ro, _ = OD.paged_decode_attention(q, kp, vp, table, lens, 0.0625, 0.125,
+                                      inputs.softmax_scale(256))
+    assert _close(o, ro)
+    assert gb.device_status() == 0
