@@ -2,11 +2,14 @@
 
 Each .cu file is compiled in parallel to an object under ``_build/`` and the
 objects are linked into ``attention_fp16_flashattention_gb300/libgbattn.so``.
-A rebuild happens when any source or header is newer than the library.
+A rebuild happens unless the library was built from exactly the current
+sources, headers and flags (a SHA-256 over their contents is stored beside
+the library), so a library left over from other sources is never reused.
 """
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
 import subprocess
 
@@ -15,6 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgbattn.so")
+STAMP = LIB + ".sha256"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 
@@ -33,17 +37,28 @@ def _deps():
         glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "gbattn.h")]
 
 
+def _digest():
+    h = hashlib.sha256()
+    h.update(" ".join(ARCH + FLAGS).encode())
+    for p in sorted(_deps()):
+        h.update(os.path.relpath(p, ROOT).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def up_to_date():
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    with open(STAMP) as f:
+        return f.read().strip() == _digest()
 
 
 def build(force=False, verbose=False):
     """Compile and link the library; returns its path."""
     if not force and up_to_date():
         return LIB
+    digest = _digest()
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
 
@@ -65,6 +80,8 @@ def build(force=False, verbose=False):
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(digest + "\n")
     return LIB
 
 

@@ -1347,6 +1347,7 @@ extern "C" int attn_dense_fwd(const void* q, const void* k, const void* v, void*
                               int B, int H, int Sq, int Skv, int D, const int64_t* q_strides,
                               const int64_t* kv_strides, const int64_t* o_strides, float scale,
                               void* stream) {
+    CallRange nvtx_range("attn_dense_fwd");
     if (!q || !k || !v || !o) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0) return GBATTN_ERR_SHAPE;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
@@ -1390,6 +1391,7 @@ extern "C" int attn_dense_mask_fwd(const void* q, const void* k, const void* v, 
                                    long long mask_stride_b, long long mask_stride_h, void* o,
                                    float* lse, int B, int H, int Sq, int Skv, int D, float scale,
                                    void* stream) {
+    CallRange nvtx_range("attn_dense_mask_fwd");
     if (!q || !k || !v || !mask || !o) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0) return GBATTN_ERR_SHAPE;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
@@ -1455,6 +1457,7 @@ extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void*
                                        const int64_t* kv_strides, const int64_t* o_strides,
                                        float scale, int flags, void* workspace,
                                        size_t workspace_bytes, void* stream) {
+    CallRange nvtx_range("attn_causal_prefill_fwd");
     if (!q || !k || !v || !o) return GBATTN_ERR_NULL;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Q_pad <= 0 || KV <= 0) return GBATTN_ERR_SHAPE;
     if (Hq % Hkv != 0 || Q_pad % 64 != 0 || Q_real < 1 || Q_real > Q_pad || Q_real > KV ||
@@ -1530,6 +1533,7 @@ extern "C" int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pag
                                              float k_scale, float v_scale, float scale,
                                              int flags, void* workspace, size_t workspace_bytes,
                                              void* stream) {
+    CallRange nvtx_range("attn_causal_prefill_paged_fwd");
     if (!q || !k_pages || !v_pages || !page_table || !o) return GBATTN_ERR_NULL;
     if (flags & ~GBATTN_PROB_SPLIT) return GBATTN_ERR_SHAPE;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Q_pad <= 0 || KV <= 0 || num_phys_pages <= 0 ||
@@ -1635,6 +1639,7 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
                               const int32_t* pairs, int prefix, const int32_t* cube_valid,
                               const float* o_coarse, const void* gate, void* o, float* lse, int B,
                               int H, int S, int D, int block, int topk, float scale, void* stream) {
+    CallRange nvtx_range("vsa_sparse_fwd");
     if (!q || !k || !v || !idx || !o || (!o_coarse) != (!gate)) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || S <= 0 || topk <= 0 || prefix < 0 || prefix >= S)
         return GBATTN_ERR_SHAPE;

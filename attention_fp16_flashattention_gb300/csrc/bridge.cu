@@ -71,6 +71,7 @@ extern "C" int e4m3_paged_to_fp16(const uint8_t* k_pages, const uint8_t* v_pages
                                   const int32_t* page_table, int num_phys_pages, int page_size,
                                   int kv_len, int Hkv, int D, float k_scale, float v_scale,
                                   void* k_out, void* v_out, void* stream) {
+    CallRange nvtx_range("e4m3_paged_to_fp16");
     if (!k_pages || !v_pages || !page_table || !k_out || !v_out) return GBATTN_ERR_NULL;
     if (num_phys_pages <= 0 || page_size <= 0 || kv_len <= 0 || Hkv <= 0 || D <= 0)
         return GBATTN_ERR_SHAPE;

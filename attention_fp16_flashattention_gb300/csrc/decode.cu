@@ -691,6 +691,7 @@ extern "C" int attn_paged_decode_fwd(const void* q, const uint8_t* k_pages, cons
                                      int num_phys_pages, int page_size, int max_pages,
                                      int max_kv_len, float k_scale, float v_scale, float scale,
                                      void* workspace, size_t workspace_bytes, void* stream) {
+    CallRange nvtx_range("attn_paged_decode_fwd");
     if (!q || !k_pages || !v_pages || !page_table || !kv_lens || !o) return GBATTN_ERR_NULL;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || nq <= 0 || num_phys_pages <= 0 || page_size <= 0 ||
         max_pages <= 0 || max_kv_len <= 0)

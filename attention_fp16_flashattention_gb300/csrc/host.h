@@ -6,6 +6,12 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#ifndef GBATTN_NVTX
+#define GBATTN_NVTX 1
+#endif
+#if GBATTN_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
 
 #include "../../include/gbattn.h"
 
@@ -101,6 +107,18 @@ int encode_tmap_f16_mask(CUtensorMap* map, const void* base, uint64_t skv, uint6
 // 128-byte swizzle.  Returns GBATTN_OK or GBATTN_ERR_CUDA.
 int encode_tmap_u8_pages(CUtensorMap* map, const void* base, uint64_t D, uint64_t hkv,
                          uint64_t rows, uint32_t box_rows);
+
+// One NVTX range per C-ABI call (its name is the entry point's), so profiler
+// timelines show which call queued which kernels.  NVTX v3 is header-only and
+// costs a branch when no tool is attached; builds with GBATTN_NVTX=0 drop it.
+struct CallRange {
+#if GBATTN_NVTX
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+#else
+    explicit CallRange(const char*) {}
+#endif
+};
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -955,6 +955,7 @@ extern "C" int vsa_select_blocks(const void* q, const void* k, int B, int H, int
                                  int block, int topk, int prefix, const int32_t* cube_valid,
                                  int32_t* idx, void* workspace, size_t workspace_bytes,
                                  void* stream) {
+    CallRange nvtx_range("vsa_select_blocks");
     return select_impl(q, k, nullptr, B, H, S, D, block, topk, prefix, cube_valid, 0.0f, idx,
                        nullptr, workspace, workspace_bytes, stream);
 }
@@ -964,6 +965,7 @@ extern "C" int vsa_select_blocks_coarse(const void* q, const void* k, const void
                                         const int32_t* cube_valid, float scale, int32_t* idx,
                                         float* o_coarse, void* workspace, size_t workspace_bytes,
                                         void* stream) {
+    CallRange nvtx_range("vsa_select_blocks_coarse");
     if (!v) return GBATTN_ERR_NULL;
     return select_impl(q, k, v, B, H, S, D, block, topk, prefix, cube_valid, scale, idx, o_coarse,
                        workspace, workspace_bytes, stream);
@@ -1120,6 +1122,7 @@ __global__ void __launch_bounds__(kPairThreads) vsa_pair_kernel(const int32_t* _
 
 extern "C" int vsa_pair_query_cubes(const int32_t* idx, int B, int H, int n_cubes, int topk,
                                     int32_t* pairs, void* stream) {
+    CallRange nvtx_range("vsa_pair_query_cubes");
     if (!idx || !pairs) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || n_cubes <= 0 || topk <= 0 || topk > n_cubes) return GBATTN_ERR_SHAPE;
     if (n_cubes > kPairMaxCubes || static_cast<long long>(B) * H > 0x7FFFFFFFLL)
@@ -1194,6 +1197,7 @@ int scratch_address(void** out) {
 extern "C" int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S, int D,
                                          int block, int topk, int prefix,
                                          const int32_t* cube_valid, int32_t* idx, void* stream) {
+    CallRange nvtx_range("vsa_select_blocks_noalloc");
     if (!q || !k || !idx) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return GBATTN_ERR_SHAPE;
     const size_t need = vsa_select_workspace_size(B, H, S, D, block);
