@@ -692,12 +692,13 @@ constexpr size_t topk_smem_bytes() { return sizeof(Cands<CAP>) * WARPS; }
 //
 // O_c[bh] = P[bh] Vm[bh]: the probabilities of every query cube over all key
 // cubes ([NC][NC], row stride score_ld(NC)) times the pooled values ([NC][128]),
-// FP32 FFMA.  One 64 (query cubes) x 128 (dims) tile per CTA, 128 threads with
-// 8 x 8 register tiles (rows 4ty.., 32+4ty.., dims 4tx.., 64+4tx..); the key
+// FP32 FFMA.  One 32 (query cubes) x 128 (dims) tile per CTA, 64 threads with
+// 8 x 8 register tiles (rows 4ty.., 16+4ty.., dims 4tx.., 64+4tx..); the key
 // dimension passes through shared memory eight keys at a time (P stored
 // key-major, Vm row-major), the next eight loaded into registers meanwhile.
-constexpr int kPvM = 64;
-constexpr int kPvThreads = 128;
+// (64-row tiles gave 192 CTAs for 24 heads of 512 cubes, 0.4 waves: 76 us.)
+constexpr int kPvM = 32;
+constexpr int kPvThreads = 64;
 
 __global__ void __launch_bounds__(kPvThreads) vsa_coarse_pv_kernel(const float* __restrict__ P,
                                                                    const float* __restrict__ vm,
@@ -710,24 +711,26 @@ __global__ void __launch_bounds__(kPvThreads) vsa_coarse_pv_kernel(const float* 
     const int m0 = blockIdx.x * kPvM;
     const int LD = score_ld(NC);
     const int ar = t >> 1, ak = (t & 1) * 4;          // P: row ar, keys ak..ak+3 of a stage
-    const int bk = t >> 4, bd = (t & 15) * 4;         // Vm: key bk, dims bd.. and 64+bd..
+    const int bk = t >> 3, bd = (t & 7) * 4;          // Vm: key bk, dims bd + 32i (i < 4)
     const bool a_live = m0 + ar < NC;
     const float* a_src = P + (bh * NC + m0 + ar) * LD + ak;
     const float* b_src = vm + bh * NC * kSelD;
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 ra, rb0, rb1;
+    float4 ra, rb[4];
     auto load = [&](int kc) {
         ra = (a_live && kc + ak < NC) ? *reinterpret_cast<const float4*>(a_src + kc) : zero;
         const bool bl = kc + bk < NC;
-        rb0 = bl ? *reinterpret_cast<const float4*>(b_src + static_cast<long long>(kc + bk) * kSelD + bd) : zero;
-        rb1 = bl ? *reinterpret_cast<const float4*>(b_src + static_cast<long long>(kc + bk) * kSelD + 64 + bd)
-                 : zero;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            rb[i] = bl ? *reinterpret_cast<const float4*>(b_src + static_cast<long long>(kc + bk) * kSelD +
+                                                          32 * i + bd)
+                       : zero;
     };
     auto stage = [&](int buf) {
         As[buf][ak + 0][ar] = ra.x; As[buf][ak + 1][ar] = ra.y;
         As[buf][ak + 2][ar] = ra.z; As[buf][ak + 3][ar] = ra.w;
-        *reinterpret_cast<float4*>(&Bs[buf][bk][bd]) = rb0;
-        *reinterpret_cast<float4*>(&Bs[buf][bk][64 + bd]) = rb1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(&Bs[buf][bk][32 * i + bd]) = rb[i];
     };
     load(0);
     stage(0);
@@ -746,7 +749,7 @@ __global__ void __launch_bounds__(kPvThreads) vsa_coarse_pv_kernel(const float* 
 #pragma unroll
         for (int kk = 0; kk < kGK; ++kk) {
             const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][4 * ty]);
-            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][32 + 4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][16 + 4 * ty]);
             const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][4 * tx]);
             const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + 4 * tx]);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
@@ -761,7 +764,7 @@ __global__ void __launch_bounds__(kPvThreads) vsa_coarse_pv_kernel(const float* 
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int row = m0 + (i < 4 ? 4 * ty + i : 32 + 4 * ty + i - 4);
+        const int row = m0 + (i < 4 ? 4 * ty + i : 16 + 4 * ty + i - 4);
         if (row >= NC) continue;
         float* dst = oc + (bh * NC + row) * kSelD;
         *reinterpret_cast<float4*>(dst + 4 * tx) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
