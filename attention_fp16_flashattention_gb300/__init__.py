@@ -45,7 +45,8 @@ _SIGNATURES = {
     "vsa_select_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "vsa_select_blocks": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "vsa_sparse_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
-                            _i, _i, _f, _vp]),
+                            _i, _i, _f, _vp, _sz, _vp]),
+    "vsa_sparse_workspace_size": (_sz, []),
     "vsa_select_coarse_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "vsa_select_blocks_coarse": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _f, _vp, _vp,
                                       _vp, _sz, _vp]),
@@ -433,13 +434,36 @@ def vsa_pair_query_cubes(idx, pairs=None, stream=None):
     return pairs
 
 
+_SPARSE_COUNTERS = {}
+
+
+def sparse_counter(stream=None):
+    """The item counter vsa_sparse_fwd uses on `stream` (default: the current stream) when
+    it is given no workspace: zeroed device bytes, one buffer per stream, which every call
+    leaves at zero.  Calls on one stream run one after another, so they can share it; a
+    caller that replays a captured graph on another stream while that stream is busy
+    passes its own workspace instead."""
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    key = (s.device.index if s.device.index is not None else torch.cuda.current_device(),
+           s.cuda_stream)
+    buf = _SPARSE_COUNTERS.get(key)
+    if buf is None:
+        n = int(load().vsa_sparse_workspace_size())
+        buf = torch.zeros(n, dtype=torch.uint8, device=s.device)
+        torch.cuda.synchronize(s.device)
+        _SPARSE_COUNTERS[key] = buf
+    return buf
+
+
 def vsa_sparse_fwd(q, k, v, idx, block=64, prefix=0, cube_valid=None, pairs=None, o=None,
-                   lse=None, scale=None, coarse=None, gate=None, stream=None):
+                   lse=None, scale=None, coarse=None, gate=None, workspace=None, stream=None):
     """Block-sparse attention over the cubes in idx.  q/k/v [B,H,S,D] FP16: `prefix` dense
     prefix tokens, then cube-major video tokens; cube_valid int32 [cubes] or None; pairs from
     vsa_pair_query_cubes or None (adjacent cubes).  coarse (FP32 [B,H,cubes,D] from
     vsa_select_blocks_coarse) and gate (FP16 [B,H,S,D]) add gate * coarse[cube] to every real
-    video token's output."""
+    video token's output.  workspace: the item counter (zeroed, left zero by every call);
+    None takes this stream's (sparse_counter), False splits the items statically."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.float16, 4)
@@ -459,9 +483,13 @@ def vsa_sparse_fwd(q, k, v, idx, block=64, prefix=0, cube_valid=None, pairs=None
     _need(o, "o", torch.float16, 4)
     if lse is not None:
         _need(lse, "lse", torch.float32)
+    if workspace is None:
+        workspace = sparse_counter(stream)
+    ws = None if workspace is False else workspace
     rc = load().vsa_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(pairs), int(prefix),
                                _ptr(cube_valid), _ptr(coarse), _ptr(gate),
                                _ptr(o), _ptr(lse), B, H, S, D, block, topk, _scale(scale, D),
+                               _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                _stream(stream))
     _check("vsa_sparse_fwd", rc)
     return o

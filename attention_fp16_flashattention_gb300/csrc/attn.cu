@@ -54,6 +54,8 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kMaxSparseTiles = 512;
 constexpr int kMaxTopk = 512;
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s for draining after an abort
+constexpr size_t kSparseWorkspaceBytes = 16;    // the item counter (int32), padded
+constexpr uint64_t kItemWaitNs = 20000000000ull;   // 20 s: the scheduler's wait for a free item slot
 
 // kMasked: dense with an additive FP16 mask [Sq][Skv] per (batch, head) slice.
 // kSparseFull: kSparse with the full VSA layout (prefix queries, boundary cubes).
@@ -69,9 +71,14 @@ __host__ __device__ constexpr bool is_causal(int mode) { return mode == kCausal 
 __host__ __device__ constexpr bool dual_issue(int mode) { return !(mode == kCausal || mode == kCausalPaged); }
 constexpr int kPvWarp = 10;
 // threads per CTA: the PV issuer adds a warp (10); the paged mode adds four
-// converter warps (10..13), the masked mode a mask-loading warp (11)
+// converter warps (10..13), the masked mode a mask-loading warp (11), the VSA
+// modes a scheduler warp (11)
+// Persistent CTAs (one per SM, each running items until none is left) pay
+// where items are short and uneven: the VSA modes.  The other modes launch one
+// CTA per item; their item loop then runs once, with a compile-time bound.
+__host__ __device__ constexpr bool persistent(int mode) { return is_sparse(mode); }
 __host__ __device__ constexpr int threads_for(int mode) {
-    return mode == kCausalPaged ? 448 : mode == kMasked ? 384 : (dual_issue(mode) ? 352 : 320);
+    return mode == kCausalPaged ? 448 : mode == kMasked ? 384 : is_sparse(mode) ? 384 : (dual_issue(mode) ? 352 : 320);
 }
 constexpr int kMaskWarp = 11;
 constexpr int kConvThreads = 128;
@@ -114,7 +121,86 @@ struct AttnArgs {
     uint32_t* status;
     uint64_t wait_limit;
     int fault;          // test hook: 1 = the TMA warp never loads Q; 2 = it stops after 2*NS K/V items
+    int n_items;        // work items of the launch (query tiles, x key chunks for causal)
+    int items_x;        // items per head row of the item order (see decode_item)
+    int* sched;         // item counter (zero between launches), or null: static split
+    int nsm;            // host: SMs of the device
 };
+
+constexpr int kSmemMax = 232448;   // dynamic shared memory a CTA may opt into (227 KB)
+
+struct Ctrl {
+    uint64_t q_full[2];    // query buffer b loaded
+    uint64_t q_empty[2];   // the last QK of the item that used query buffer b is done
+    uint64_t full[4];
+    uint64_t empty[4];
+    uint64_t s_full[3];    // QK_g done (buffer g % NSB), g counting every tile of the CTA
+    uint64_t p_full[3];    // P_g written (buffer g % NSB)
+    uint64_t pv_done[3];   // PV_g done (barrier g % NSB).  QK_g is issued after
+                           // PV_{g-NSB}, so once S_g is visible the previous phase
+                           // of every barrier awaited below has completed.
+    uint64_t item_full[2];    // the scheduler warp wrote item slot s
+    uint64_t item_empty[2];   // every consumer warp is done with item slot s
+    uint64_t o_free;          // the softmax warps have read O of their last item out of TMEM
+    uint64_t drain;
+    uint64_t drain_pv;     // the PV issuer's own drain after an abort
+    uint64_t xchg[4];      // per row quarter: the two half-row threads exchange values
+    uint64_t raw_full[2];  // paged: E4M3 bytes of a slot landed (converters may read)
+    uint64_t conv_read[2]; // paged: every converter holds its bytes (the slot may be overwritten)
+    uint32_t tmem_base;
+    int abort;
+};
+
+// Values exchanged between the two threads that share a query row.
+struct Exchange {
+    float mx[2][2][128];   // [tile parity][column half][row] partial row max
+    float l[2][128];       // [column half][row] partial row sum (epilogue)
+};
+
+constexpr int kCtrlReserve = 512;
+constexpr int kCtrlBytes = kCtrlReserve + static_cast<int>(sizeof(Exchange));
+static_assert(sizeof(Ctrl) <= kCtrlReserve, "control block");
+
+// One work item: a 128-row query tile of one head (a VSA video item: a pair of
+// 64-row query cubes) and, for causal attention, one key chunk.
+struct Item {
+    int valid;      // 0: no more work for this CTA
+    int bh;         // query head (batch-major)
+    int kv_bh;      // key/value head
+    int q_row0;     // first query row (VSA: of the first cube)
+    int tile0;      // first 128-key tile (dense and causal)
+    int n_tiles;    // key tiles of the item
+    int chunk;      // causal key chunk
+    int rbase0;     // first token row of each 64-row query half (-1: no second cube)
+    int rbase1;
+};
+
+// The key tiles of a VSA item as its consumers read them.
+struct SparseSlot {
+    int key0[kMaxSparseTiles];   // first key of each 64-key tile half
+    int key1[kMaxSparseTiles];
+    // What the softmax reads per tile, in one word: quadrant bits | real keys of
+    // the first half << 8 | real keys of the second half << 16.
+    uint32_t info[kMaxSparseTiles];
+};
+
+// The scheduler warp's working space while it builds a VSA tile list.
+struct SparseScratch {
+    int list_a[kMaxTopk];
+    int list_b[kMaxTopk];
+    uint32_t bits_a[32];            // the two cube sets (at most 1024 cubes)
+    uint32_t bits_b[32];
+    uint8_t mask_hi[kMaxSparseTiles];   // quadrant bits of each tile's second half
+    uint8_t mask[kMaxSparseTiles];
+    uint8_t kv0[kMaxSparseTiles];   // real keys in each 64-key half (boundary cubes)
+    uint8_t kv1[kMaxSparseTiles];
+};
+
+// Masked mode: the mask warp stages each tile's 128 rows x 128 keys of the mask
+// (two 64-key boxes of 16 KB, TMA, 128-byte swizzle) in two slots, two tiles
+// ahead; the slots' full and empty barriers follow them.
+constexpr int kMaskSlotBytes = 128 * 256;
+constexpr int kMaskStageBytes = 2 * kMaskSlotBytes + 4 * 8;
 
 template <int D, int MODE>
 struct Cfg {
@@ -126,6 +212,15 @@ struct Cfg {
     static constexpr int KCH = D / 64;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int SLOT_BYTES = BN * D * 2;
+    // everything but the query buffers
+    static constexpr int REST = 1024 + NS * SLOT_BYTES + kCtrlBytes + 2 * static_cast<int>(sizeof(Item)) +
+                                (is_sparse(MODE) ? static_cast<int>(2 * sizeof(SparseSlot) + sizeof(SparseScratch)) : 0) +
+                                (MODE == kMasked ? kMaskStageBytes : 0);
+    // Two query buffers where they fit: the next item's query tile then loads
+    // while the last QKs of the current item still read theirs.
+    static constexpr int QB = persistent(MODE) && REST + 2 * Q_BYTES <= kSmemMax ? 2 : 1;
+    static constexpr int SMEM = REST + QB * Q_BYTES;
+    static_assert(SMEM <= kSmemMax, "shared memory budget");
     // TMEM columns: S buffer b at b*128 (P of that tile overwrites its first 64
     // columns as FP16 pairs), O after the S buffers.
     static constexpr uint32_t T_O = NSB * 128;
@@ -134,62 +229,16 @@ struct Cfg {
     static constexpr uint32_t IDESC_PV = idesc_f16(BM, D, false, true);
 };
 
-struct Ctrl {
-    uint64_t q_full;
-    uint64_t full[4];
-    uint64_t empty[4];
-    uint64_t s_full[3];    // QK_j done (buffer j % NSB)
-    uint64_t p_full[3];    // P_j written (buffer j % NSB)
-    uint64_t pv_done[3];   // PV_j done (barrier j % NSB).  QK_j is issued after
-                           // PV_{j-NSB}, so once S_j is visible the previous phase
-                           // of every barrier awaited below has completed.
-    uint64_t drain;
-    uint64_t drain_pv;     // the PV issuer's own drain after an abort
-    uint64_t xchg[4];      // per row quarter: the two half-row threads exchange values
-    uint64_t raw_full[2];  // paged: E4M3 bytes of a slot landed (converters may read)
-    uint64_t conv_read[2]; // paged: every converter holds its bytes (the slot may be overwritten)
-    uint32_t tmem_base;
-    int abort;
-    int n_tiles;
-};
-
-// Values exchanged between the two threads that share a query row.
-struct Exchange {
-    float mx[2][2][128];   // [tile parity][column half][row] partial row max
-    float l[2][128];       // [column half][row] partial row sum (epilogue)
-};
-
-constexpr int kCtrlBytes = 256 + static_cast<int>(sizeof(Exchange));
-static_assert(sizeof(Ctrl) <= 256, "control block");
-
-struct SparseTiles {
-    int list_a[kMaxTopk];
-    int list_b[kMaxTopk];
-    uint32_t bits_a[32];            // the two cube sets (at most 1024 cubes)
-    uint32_t bits_b[32];
-    uint8_t mask_hi[kMaxSparseTiles];   // quadrant bits of each tile's second half
-    int key0[kMaxSparseTiles];
-    int key1[kMaxSparseTiles];
-    uint8_t mask[kMaxSparseTiles];
-    uint8_t kv0[kMaxSparseTiles];   // real keys in each 64-key half (boundary cubes)
-    uint8_t kv1[kMaxSparseTiles];
-    // What the softmax reads per tile, in one word: quadrant bits | real keys of
-    // the first half << 8 | real keys of the second half << 16.
-    uint32_t info[kMaxSparseTiles];
-};
-
-// Masked mode: the mask warp stages each tile's 128 rows x 128 keys of the mask
-// (two 64-key boxes of 16 KB, TMA, 128-byte swizzle) in two slots, two tiles
-// ahead; the slots' full and empty barriers follow them.
-constexpr int kMaskSlotBytes = 128 * 256;
-constexpr int kMaskStageBytes = 2 * kMaskSlotBytes + 4 * 8;
-
 template <int D, int MODE>
 constexpr int smem_bytes() {
-    using C = Cfg<D, MODE>;
-    return 1024 + C::Q_BYTES + C::NS * C::SLOT_BYTES + kCtrlBytes +
-           (is_sparse(MODE) ? static_cast<int>(sizeof(SparseTiles)) : 0) +
-           (MODE == kMasked ? kMaskStageBytes : 0);
+    return Cfg<D, MODE>::SMEM;
+}
+
+// Consumer warps of an item slot: TMA, QK issuer, PV issuer (D=128), eight
+// softmax warps, and the mask warp or the four converter warps.
+__host__ __device__ constexpr int consumer_warps(int mode) {
+    return 2 + (dual_issue(mode) ? 1 : 0) + kSoftmaxThreads / 32 + (mode == kMasked ? 1 : 0) +
+           (mode == kCausalPaged ? kConvThreads / 32 : 0);
 }
 
 // Bounded wait that ignores the abort flag (used only to drain after an abort).
@@ -202,7 +251,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // Item order of the K/V ring = the MMA warp's consumption order with a QK
 // lookahead of L tiles: K_0 .. K_{L-1}, then (V_j, K_{j+L}) while j + L < n,
-// then the remaining V_j.
+// then the remaining V_j.  Items follow each other in the ring.
 __device__ __forceinline__ void ring_item(int it, int n, int L, int& tile, bool& is_v) {
     const int k0 = min(n, L);
     if (it < k0) { tile = it; is_v = false; return; }
@@ -217,6 +266,26 @@ __device__ __forceinline__ void ring_item(int it, int n, int L, int& tile, bool&
     is_v = true;
 }
 
+// Position in a ring of N buffers, advanced one step at a time: idx = count % N,
+// phase = (count / N) & 1, without a division in the loops.
+template <int N>
+struct Cursor {
+    int idx = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void step() {
+        if (++idx == N) {
+            idx = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Ring slot and phase of ring position pos (unsigned: a power-of-two ring is a mask).
+template <int N>
+__device__ __forceinline__ int slot_of(int pos) { return static_cast<int>(static_cast<unsigned>(pos) % N); }
+template <int N>
+__device__ __forceinline__ uint32_t phase_of(int pos) { return (static_cast<unsigned>(pos) / N) & 1u; }
+
 // Real tokens of video cube c (boundary cubes are padded); out-of-range counts
 // are flagged and clamped.
 __device__ __forceinline__ int cube_count(const AttnArgs& a, int c) {
@@ -229,14 +298,15 @@ __device__ __forceinline__ int cube_count(const AttnArgs& a, int c) {
     return n;
 }
 
-// Tile list of a CTA.  Prefix query tiles (qtile < prefix / BM) attend densely:
-// every 128-key prefix tile, then the video cubes two by two.  Video query-cube
-// pairs merge their two strictly ascending cube lists into tiles of two cubes;
-// entries that are out of range or not ascending are skipped and flagged.
-// Video keys sit at prefix + 64 * cube.
+// Tile list of a VSA item, built by the scheduler warp.  Prefix query tiles
+// (qtile < prefix / BM) attend densely: every 128-key prefix tile, then the
+// video cubes two by two.  Video query-cube pairs merge their two strictly
+// ascending cube lists into tiles of two cubes; entries that are out of range
+// or not ascending are skipped and flagged.  Video keys sit at prefix + 64 *
+// cube.  Returns the number of tiles (warp-uniform).
 template <bool kFull>
-__device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& a, int bh,
-                                   int qtile, int ca, int cb) {
+__device__ int build_sparse_tiles(SparseScratch* sc, SparseSlot* sl, const AttnArgs& a, int bh,
+                                  int qtile, int ca, int cb) {
     const int lane = threadIdx.x & 31;
     const int n_pre = kFull ? a.prefix / BM : 0;
     const int kbase = kFull ? a.prefix : 0;
@@ -244,48 +314,44 @@ __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& 
         const int nt = n_pre + (a.n_cubes + 1) / 2;
         for (int t = lane; t < nt; t += 32) {
             if (t < n_pre) {
-                st->key0[t] = t * BN;
-                st->key1[t] = t * BN + 64;
-                st->kv0[t] = st->kv1[t] = 64;
-                st->mask[t] = 0xF;
+                sl->key0[t] = t * BN;
+                sl->key1[t] = t * BN + 64;
+                sc->kv0[t] = sc->kv1[t] = 64;
+                sc->mask[t] = 0xF;
             } else {
                 const int c0 = 2 * (t - n_pre), c1 = c0 + 1;
-                st->key0[t] = a.prefix + 64 * c0;
-                st->kv0[t] = static_cast<uint8_t>(cube_count(a, c0));
+                sl->key0[t] = a.prefix + 64 * c0;
+                sc->kv0[t] = static_cast<uint8_t>(cube_count(a, c0));
                 if (c1 < a.n_cubes) {
-                    st->key1[t] = a.prefix + 64 * c1;
-                    st->kv1[t] = static_cast<uint8_t>(cube_count(a, c1));
-                    st->mask[t] = 0xF;
+                    sl->key1[t] = a.prefix + 64 * c1;
+                    sc->kv1[t] = static_cast<uint8_t>(cube_count(a, c1));
+                    sc->mask[t] = 0xF;
                 } else {   // odd cube count: the second half repeats the cube, masked
-                    st->key1[t] = st->key0[t];
-                    st->kv1[t] = st->kv0[t];
-                    st->mask[t] = 0x5;
+                    sl->key1[t] = sl->key0[t];
+                    sc->kv1[t] = sc->kv0[t];
+                    sc->mask[t] = 0x5;
                 }
             }
         }
-        if (lane == 0) ctrl->n_tiles = nt;
-        return;
+        return nt;
     }
     const int na = a.topk;
     const int nb = cb >= 0 ? a.topk : 0;
     const int32_t* la = a.idx + (static_cast<long long>(bh) * a.n_cubes + ca) * a.topk;
     const int32_t* lb = a.idx + (static_cast<long long>(bh) * a.n_cubes + (cb >= 0 ? cb : ca)) * a.topk;
-    for (int i = lane; i < na; i += 32) st->list_a[i] = la[i];
-    for (int i = lane; i < nb; i += 32) st->list_b[i] = lb[i];
+    for (int i = lane; i < na; i += 32) sc->list_a[i] = la[i];
+    for (int i = lane; i < nb; i += 32) sc->list_b[i] = lb[i];
+    sc->bits_a[lane] = 0u;
+    sc->bits_b[lane] = 0u;
     __syncwarp();
     // Set of each list: an entry counts when it lies in range and exceeds every
     // entry before it (a list that is not strictly ascending is flagged and its
     // offending entries skipped).
-    if (lane < 32) {
-        st->bits_a[lane] = 0u;
-        st->bits_b[lane] = 0u;
-    }
-    __syncwarp();
     bool bad = false;
     for (int lst = 0; lst < 2; ++lst) {
         const int n = lst == 0 ? na : nb;
-        const int* L = lst == 0 ? st->list_a : st->list_b;
-        uint32_t* bits = lst == 0 ? st->bits_a : st->bits_b;
+        const int* L = lst == 0 ? sc->list_a : sc->list_b;
+        uint32_t* bits = lst == 0 ? sc->bits_a : sc->bits_b;
         int run_max = -1;
         for (int base = 0; base < n; base += 32) {
             const int i = base + lane;
@@ -310,7 +376,7 @@ __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& 
     // Union in ascending cube order: word w of the sets belongs to lane w; a warp
     // prefix sum of the popcounts places every cube; consecutive cubes pair up
     // into 128-key tiles.
-    const uint32_t ua = st->bits_a[lane], ub = st->bits_b[lane], uu = ua | ub;
+    const uint32_t ua = sc->bits_a[lane], ub = sc->bits_b[lane], uu = ua | ub;
     const int cnt = __popc(uu);
     int incl = cnt;
 #pragma unroll
@@ -326,32 +392,103 @@ __device__ void build_sparse_tiles(SparseTiles* st, Ctrl* ctrl, const AttnArgs& 
         const uint32_t f = ((ua >> bit) & 1u) | (((ub >> bit) & 1u) << 1);
         const int t = pos >> 1;
         if ((pos & 1) == 0) {
-            st->key0[t] = kbase + c * 64;
-            st->mask[t] = static_cast<uint8_t>((f & 1) | ((f >> 1) << 2));
+            sl->key0[t] = kbase + c * 64;
+            sc->mask[t] = static_cast<uint8_t>((f & 1) | ((f >> 1) << 2));
             if (pos == nu - 1) {   // odd union: the second half repeats the cube, fully masked
-                st->key1[t] = kbase + c * 64;
-                st->mask_hi[t] = 0;
+                sl->key1[t] = kbase + c * 64;
+                sc->mask_hi[t] = 0;
             }
         } else {
-            st->key1[t] = kbase + c * 64;
-            st->mask_hi[t] = static_cast<uint8_t>(((f & 1) << 1) | ((f >> 1) << 3));
+            sl->key1[t] = kbase + c * 64;
+            sc->mask_hi[t] = static_cast<uint8_t>(((f & 1) << 1) | ((f >> 1) << 3));
         }
     }
     __syncwarp();
     const int nt = (nu + 1) / 2;
-    for (int t = lane; t < nt; t += 32) st->mask[t] |= st->mask_hi[t];
+    for (int t = lane; t < nt; t += 32) sc->mask[t] |= sc->mask_hi[t];
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, kDevBadIndex);
-    if (lane == 0) ctrl->n_tiles = nt;
+    return nt;
 }
 
-// Real keys of every tile half of a video query-cube pair (boundary cubes),
-// filled by the whole warp once the list is built; only with cube counts.
-__device__ void fill_tile_counts(SparseTiles* st, const Ctrl* ctrl, const AttnArgs& a) {
-    const int nt = ctrl->n_tiles;
-    for (int t = threadIdx.x & 31; t < nt; t += 32) {
-        st->kv0[t] = static_cast<uint8_t>(cube_count(a, (st->key0[t] - a.prefix) >> 6));
-        st->kv1[t] = static_cast<uint8_t>(cube_count(a, (st->key1[t] - a.prefix) >> 6));
+// The next item of a CTA (lane 0 draws, the warp gets it).  With a counter the
+// items go to whichever CTA asks first; every CTA draws once past the last
+// item, and the draw that sees the last of those values (n_items + grid - 1:
+// no CTA draws after it) puts the counter back to zero for the next launch.
+// A draw outside [0, n_items + grid) means the counter did not start at zero:
+// it is flagged and ends the CTA's work.  Without a counter, CTA c takes items
+// c, c + grid, c + 2 grid, ...
+__device__ __forceinline__ long long next_item(const AttnArgs& a, int k) {
+    long long id = 0;
+    if (a.sched) {
+        if ((threadIdx.x & 31) == 0) {
+            const int last = a.n_items + static_cast<int>(gridDim.x) - 1;
+            const int v = atomicAdd(a.sched, 1);
+            if (v == last) atomicExch(a.sched, 0);
+            if (v < 0 || v > last) atomicOr(a.status, kDevBadIndex);
+            id = (v < 0 || v > last) ? a.n_items : v;
+        }
+        id = __shfl_sync(0xffffffffu, id, 0);
+    } else {
+        id = static_cast<long long>(blockIdx.x) + static_cast<long long>(k) * gridDim.x;
     }
+    return id;
+}
+
+// Work decode of item id (everything but the VSA tile list).  The item order
+// is the order the CTAs of a one-item-per-CTA launch would start in.
+template <int MODE>
+__device__ Item decode_item(const AttnArgs& a, int id, int& qtile) {
+    Item it{};
+    it.valid = 1;
+    int bh;
+    if (MODE == kMasked) {
+        // heads fastest, so that the items of all heads of a query tile run
+        // together and share that tile's mask rows in L2
+        bh = id % a.heads_q;
+        qtile = id / a.heads_q;
+    } else if (MODE == kSparseFull) {
+        // the long prefix tiles of every head first, then each head's cube pairs
+        const int n_pre = a.prefix / BM;
+        const int n_pairs = a.items_x - n_pre;
+        const int pre_all = n_pre * a.heads_q;
+        if (id < pre_all) {
+            bh = id / n_pre;
+            qtile = id - bh * n_pre;
+        } else {
+            const int r = id - pre_all;
+            bh = r / n_pairs;
+            qtile = n_pre + (r - bh * n_pairs);
+        }
+    } else if (is_causal(MODE)) {
+        // heads fastest, then query tiles, then key chunks, so that the items in
+        // flight walk one key window together (and the query heads that share a
+        // KV head read each K/V tile from L2 at about the same time)
+        const int n_qt = a.items_x / a.n_chunks;
+        bh = id % a.heads_q;
+        const int r = id / a.heads_q;
+        qtile = r % n_qt;
+        it.chunk = r / n_qt;
+    } else {
+        qtile = id % a.items_x;
+        bh = id / a.items_x;
+    }
+    it.bh = bh;
+    it.q_row0 = qtile * BM;
+    it.kv_bh = bh;
+    if (is_causal(MODE)) {
+        const int b = bh / a.hq, h = bh - b * a.hq;
+        it.kv_bh = b * a.hkv + h / a.group;
+        const long long kend = min(static_cast<long long>(a.seq_k),
+                                   static_cast<long long>(a.kv_prefix) + it.q_row0 + BM);
+        const int T = static_cast<int>((kend + BN - 1) / BN);
+        it.tile0 = static_cast<int>(static_cast<long long>(it.chunk) * T / a.n_chunks);
+        it.n_tiles = static_cast<int>(static_cast<long long>(it.chunk + 1) * T / a.n_chunks) - it.tile0;
+    } else if (MODE == kDense || MODE == kMasked) {
+        it.n_tiles = (a.seq_k + BN - 1) / BN;
+    }
+    it.rbase0 = it.q_row0;
+    it.rbase1 = it.q_row0 + 64;
+    return it;
 }
 
 // PS (causal modes only): the probabilities enter the PV product as two FP16
@@ -359,6 +496,13 @@ __device__ void fill_tile_counts(SparseTiles* st, const Ctrl* ctrl, const AttnAr
 // FP16 value.  P_lo takes columns 64..127 of its S buffer (both threads of a
 // row have read their S halves before either writes), and PV issues a second
 // group of MMAs over it.
+//
+// Items: every role loops over the CTA's items until it gets an invalid one
+// (persistent VSA modes; the other modes run one item per CTA and their loop
+// has a compile-time bound of one).  Every role keeps running counts (tiles,
+// ring items, query buffer uses) across items, so each barrier's phases simply
+// continue; the first PV of an item overwrites O once the softmax warps have
+// read the previous item's O (o_free).
 template <int D, int MODE, bool PS = false>
 __global__ void __launch_bounds__(threads_for(MODE), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -368,94 +512,32 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sKV = smem + C::Q_BYTES;
+    uint8_t* sQ = smem;                              // C::QB query buffers
+    uint8_t* sKV = smem + C::QB * C::Q_BYTES;
     // masked mode: mask stages (1024-aligned) and their barriers after the ring
     uint8_t* sMask = sKV + C::NS * C::SLOT_BYTES;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sMask + 2 * kMaskSlotBytes);   // full[2], empty[2]
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(sKV + C::NS * C::SLOT_BYTES +
                                          (MODE == kMasked ? kMaskStageBytes : 0));
-    Exchange* ex = reinterpret_cast<Exchange*>(reinterpret_cast<uint8_t*>(ctrl) + 256);
-    SparseTiles* st = reinterpret_cast<SparseTiles*>(reinterpret_cast<uint8_t*>(ctrl) + kCtrlBytes);
+    Exchange* ex = reinterpret_cast<Exchange*>(reinterpret_cast<uint8_t*>(ctrl) + kCtrlReserve);
+    Item* items = reinterpret_cast<Item*>(reinterpret_cast<uint8_t*>(ctrl) + kCtrlBytes);
+    SparseSlot* slots = reinterpret_cast<SparseSlot*>(items + 2);
+    SparseScratch* scratch = reinterpret_cast<SparseScratch*>(slots + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Masked mode runs heads fastest (grid (B*H, tiles)) so that the CTAs of all
-    // heads of a query tile run together and share that tile's mask rows in L2.
-    int bh = MODE == kMasked ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
-    int qtile = MODE == kMasked ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
-    if (MODE == kSparseFull) {
-        // The long prefix tiles of every head launch first, then each head's cube pairs.
-        const int n_pre = a.prefix / BM;
-        const int n_pairs = static_cast<int>(gridDim.x) - n_pre;
-        const long long id = static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x;
-        const long long pre_all = static_cast<long long>(n_pre) * gridDim.y;
-        if (id < pre_all) {
-            bh = static_cast<int>(id / n_pre);
-            qtile = static_cast<int>(id - static_cast<long long>(bh) * n_pre);
-        } else {
-            const long long r = id - pre_all;
-            bh = static_cast<int>(r / n_pairs);
-            qtile = n_pre + static_cast<int>(r - static_cast<long long>(bh) * n_pairs);
-        }
-    }
-
-    // ---- work decode
-    int q_row0, kv_bh, n_tiles = 0, tile0 = 0, chunk = 0;
-    if (is_causal(MODE)) {
-        // Launch order: heads fastest, then query tiles, then key chunks, so that the
-        // CTAs in flight walk one key window together (and the query heads that share
-        // a KV head read each K/V tile from L2 at about the same time).
-        const long long id = static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x;
-        const int n_qt = static_cast<int>(gridDim.x) / a.n_chunks;
-        bh = static_cast<int>(id % gridDim.y);
-        const long long r = id / gridDim.y;
-        const int qt = static_cast<int>(r % n_qt);
-        chunk = static_cast<int>(r / n_qt);
-        q_row0 = qt * BM;
-        const int b = bh / a.hq, h = bh - b * a.hq;
-        kv_bh = b * a.hkv + h / a.group;
-        const long long kend = min(static_cast<long long>(a.seq_k),
-                                   static_cast<long long>(a.kv_prefix) + q_row0 + BM);
-        const int T = static_cast<int>((kend + BN - 1) / BN);
-        tile0 = static_cast<int>(static_cast<long long>(chunk) * T / a.n_chunks);
-        n_tiles = static_cast<int>(static_cast<long long>(chunk + 1) * T / a.n_chunks) - tile0;
-    } else {
-        q_row0 = qtile * BM;
-        kv_bh = bh;
-        if (MODE == kDense || MODE == kMasked) n_tiles = (a.seq_k + BN - 1) / BN;
-    }
-    // 4-D tensor-map coordinates (head, batch entry) of the query and key heads
-    const int qb = bh / a.hq, qh = bh - qb * a.hq;
-    const int kvb = kv_bh / a.hkv, kvh = kv_bh - kvb * a.hkv;
-    // First token row of each 64-row half of the query tile.  A VSA video CTA
-    // owns a pair of query cubes (ca, cb), not necessarily adjacent; cb < 0
-    // leaves the second half empty.
-    int ca = -1, cb = -1;
-    int rbase0 = q_row0, rbase1 = q_row0 + 64;
-    if (is_sparse(MODE) && qtile >= (MODE == kSparseFull ? a.prefix / BM : 0)) {
-        const int p = qtile - (MODE == kSparseFull ? a.prefix / BM : 0);
-        ca = 2 * p;
-        cb = 2 * p + 1 < a.n_cubes ? 2 * p + 1 : -1;
-        if (a.pairs) {
-            const int n_pairs = (a.n_cubes + 1) / 2;
-            const int x = a.pairs[(static_cast<long long>(bh) * n_pairs + p) * 2];
-            const int y = a.pairs[(static_cast<long long>(bh) * n_pairs + p) * 2 + 1];
-            if (x >= 0 && x < a.n_cubes && y >= -1 && y < a.n_cubes && x != y) {
-                ca = x;
-                cb = y;
-            } else if (threadIdx.x == 0) {
-                atomicOr(a.status, kDevBadIndex);
-            }
-        }
-        const int kb = MODE == kSparseFull ? a.prefix : 0;
-        rbase0 = kb + 64 * ca;
-        rbase1 = cb >= 0 ? kb + 64 * cb : -1;
-        q_row0 = rbase0;
-    }
+    // VSA items differ in length and need their tile lists built: a scheduler warp
+    // draws them and fills two item slots ahead of the consumers.  Every other
+    // item is a uniform query tile (and key chunk) that each warp decodes itself.
+    constexpr bool kSched = is_sparse(MODE);
+    constexpr bool kPersist = persistent(MODE);
+    constexpr int kSchedWarp = kSched ? threads_for(MODE) / 32 - 1 : -1;
 
     // ---- prologue
     if (threadIdx.x == 0) {
-        mbar_init(&ctrl->q_full, 1);
+        for (int i = 0; i < C::QB; ++i) {
+            mbar_init(&ctrl->q_full[i], 1);
+            mbar_init(&ctrl->q_empty[i], 1);
+        }
         for (int i = 0; i < C::NS; ++i) {
             // paged: the four converter warps complete a slot, not the TMA bytes
             mbar_init(&ctrl->full[i], MODE == kCausalPaged ? kConvThreads / 32 : 1);
@@ -469,63 +551,30 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         for (int i = 0; i < C::NSB; ++i) {
             mbar_init(&ctrl->s_full[i], 1);
             mbar_init(&ctrl->p_full[i], kSoftmaxThreads);
+            mbar_init(&ctrl->pv_done[i], 1);
         }
-        for (int i = 0; i < C::NSB; ++i) mbar_init(&ctrl->pv_done[i], 1);
         for (int i = 0; i < 4; ++i) mbar_init(&ctrl->xchg[i], 64);
         if (MODE == kMasked)
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&mbar[i], 1);                          // the slot's bytes landed
                 mbar_init(&mbar[2 + i], kSoftmaxThreads / 32);   // every softmax warp read it
             }
+        if (kSched)
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&ctrl->item_full[i], 1);
+                mbar_init(&ctrl->item_empty[i], consumer_warps(MODE));
+            }
+        mbar_init(&ctrl->o_free, kSoftmaxThreads / 32);
         mbar_init(&ctrl->drain, 1);
         mbar_init(&ctrl->drain_pv, 1);
         ctrl->abort = 0;
         mbar_init_fence();
     }
-    // The query tile's copy (one elected lane of the TMA warp).
-    auto issue_q = [&]() {
-        if (elect_one()) {
-            mbar_arrive_expect_tx(&ctrl->q_full, C::Q_BYTES);
-            if (is_sparse(MODE)) {   // two 64-row halves (a query-cube pair); tmM has 64-row boxes
-                const int r1 = rbase1 >= 0 ? rbase1 : rbase0;
-#pragma unroll
-                for (int c = 0; c < C::KCH; ++c) {
-                    tma_load_4d(sQ + c * C::CHUNK, &tmM, &ctrl->q_full, c * 64, rbase0, qh, qb);
-                    tma_load_4d(sQ + c * C::CHUNK + C::HALF, &tmM, &ctrl->q_full, c * 64, r1, qh, qb);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < C::KCH; ++c)
-                    tma_load_4d(sQ + c * C::CHUNK, &tmQ, &ctrl->q_full, c * 64, q_row0, qh, qb);
-            }
-        }
-        __syncwarp();
-    };
-    const bool load_q = a.fault != 1;
-    // Sparse modes build the key-tile list first; the query tile does not depend
-    // on it, so its copy is issued before and is in flight while the list is built.
-    const bool early_q = is_sparse(MODE) && load_q;
-    if (warp == 0) {
-        if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            if (MODE == kMasked || is_sparse(MODE)) tma_prefetch_desc(&tmM);
-        }
-        __syncwarp();   // the barriers thread 0 initialised are visible to the warp
-        if (early_q) issue_q();
-        if (is_sparse(MODE)) {
-            build_sparse_tiles<MODE == kSparseFull>(st, ctrl, a, bh, qtile, ca, cb);
-            __syncwarp();
-            if (MODE == kSparseFull && a.cube_valid && qtile >= a.prefix / BM)
-                fill_tile_counts(st, ctrl, a);
-            __syncwarp();
-            const bool counts = MODE == kSparseFull && a.cube_valid;
-            for (int t = lane; t < ctrl->n_tiles; t += 32)
-                st->info[t] = st->mask[t] | (static_cast<uint32_t>(counts ? st->kv0[t] : 64) << 8) |
-                              (static_cast<uint32_t>(counts ? st->kv1[t] : 64) << 16);
-        }
-        __syncwarp();
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        if (MODE == kMasked || is_sparse(MODE)) tma_prefetch_desc(&tmM);
     }
     if (warp == 1) {
         tmem_alloc(&ctrl->tmem_base, 512);
@@ -535,22 +584,41 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
-    if (is_sparse(MODE)) n_tiles = ctrl->n_tiles;
     const WaitCtl w{a.wait_limit, a.status, &ctrl->abort};
+    const bool load_q = a.fault != 1;
 
-    auto tile_keys = [&](int t, int& k0, int& k1) {
-        if (is_sparse(MODE)) {
-            k0 = st->key0[t];
-            k1 = st->key1[t];
+    // The CTA's k-th item.  VSA: from item slot k & 1 (false: the wait ended in
+    // an abort); otherwise item blockIdx.x + k * gridDim.x, decoded here.
+    auto get_item = [&](int k, Item& cur) -> bool {
+        if (kSched) {
+            if (!wait_warp(&ctrl->item_full[k & 1], (k >> 1) & 1, w)) return false;
+            cur = items[k & 1];
         } else {
-            k0 = (tile0 + t) * BN;
+            const long long id = static_cast<long long>(blockIdx.x) + static_cast<long long>(k) * gridDim.x;
+            int qtile = 0;
+            if (id < a.n_items) cur = decode_item<MODE>(a, static_cast<int>(id), qtile);
+            else cur.valid = 0;
+        }
+        return true;
+    };
+    auto item_release = [&](int k) {
+        if (kSched) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->item_empty[k & 1]);
+        }
+    };
+    auto tile_keys = [&](const Item& it, const SparseSlot* sl, int t, int& k0, int& k1) {
+        if (is_sparse(MODE)) {
+            k0 = sl->key0[t];
+            k1 = sl->key1[t];
+        } else {
+            k0 = (it.tile0 + t) * BN;
             k1 = k0 + 64;
         }
     };
-
-    // S_t = Q K_t^T into S buffer buf; O += P_j V_j with P_j read from S buffer buf.
-    auto issue_qk = [&](int slot, int buf) {
-        const uint32_t qa = smem_addr(sQ);
+    // S_g = Q K^T into S buffer buf; O += P V with P read from S buffer buf.
+    auto issue_qk = [&](int qbuf, int slot, int buf) {
+        const uint32_t qa = smem_addr(sQ + qbuf * C::Q_BYTES);
         const uint32_t ka = smem_addr(sKV + slot * C::SLOT_BYTES);
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16) {
@@ -573,151 +641,281 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                        sdesc_sw128(va + k16 * 2048, C::CHUNK, 1024), C::IDESC_PV, 1u);
         }
     };
-    // Ring positions (the TMA warp's load order, see ring_item) of K_t and V_j.
+    // Ring positions within an item of n tiles (the TMA warp's load order, see
+    // ring_item) of K_t and V_j.
     auto pos_k = [&](int t) { return t < C::NSB ? t : C::NSB + 2 * (t - C::NSB) + 1; };
-    auto pos_v = [&](int j) {
-        return min(n_tiles, C::NSB) + j + min(j, max(0, n_tiles - C::NSB));
-    };
+    auto pos_v = [&](int j, int n) { return min(n, C::NSB) + j + min(j, max(0, n - C::NSB)); };
 
-    if (warp == 0) {
+    if (kSched && warp == kSchedWarp) {
+        // ================= scheduler: draws items, decodes them (and builds the
+        // VSA tile lists) into the two item slots, one item ahead of the consumers
+        // (a slot frees when a whole item has run, so this wait has a long limit
+        // and sleeps between polls; an abort elsewhere still ends it)
+        const WaitCtl w_item{a.wait_limit > kItemWaitNs ? a.wait_limit : kItemWaitNs, a.status, &ctrl->abort};
+        bool ok = true, drawn_last = false;
+        for (int k = 0;; ++k) {
+            const long long id = next_item(a, k);
+            const bool live = id < a.n_items;
+            drawn_last = !live;
+            if (k >= 2) ok = wait_warp_sleep(&ctrl->item_empty[k & 1], ((k >> 1) - 1) & 1, w_item, 1000);
+            if (!ok) break;
+            Item* dst = items + (k & 1);
+            if (live) {
+                int qtile = 0;
+                Item it = decode_item<MODE>(a, static_cast<int>(id), qtile);
+                if (is_sparse(MODE)) {
+                    SparseSlot* sl = slots + (k & 1);
+                    const int n_pre = MODE == kSparseFull ? a.prefix / BM : 0;
+                    int ca = -1, cb = -1;
+                    if (qtile >= n_pre) {   // a pair of query cubes (ca, cb), not necessarily adjacent
+                        const int p = qtile - n_pre;
+                        ca = 2 * p;
+                        cb = 2 * p + 1 < a.n_cubes ? 2 * p + 1 : -1;
+                        if (a.pairs) {
+                            const int n_pairs = (a.n_cubes + 1) / 2;
+                            const int x = a.pairs[(static_cast<long long>(it.bh) * n_pairs + p) * 2];
+                            const int y = a.pairs[(static_cast<long long>(it.bh) * n_pairs + p) * 2 + 1];
+                            if (x >= 0 && x < a.n_cubes && y >= -1 && y < a.n_cubes && x != y) {
+                                ca = x;
+                                cb = y;
+                            } else if (lane == 0) {
+                                atomicOr(a.status, kDevBadIndex);
+                            }
+                        }
+                        const int kb = MODE == kSparseFull ? a.prefix : 0;
+                        it.rbase0 = kb + 64 * ca;
+                        it.rbase1 = cb >= 0 ? kb + 64 * cb : -1;
+                        it.q_row0 = it.rbase0;
+                    }
+                    const int nt = build_sparse_tiles<MODE == kSparseFull>(scratch, sl, a, it.bh, qtile, ca, cb);
+                    __syncwarp();
+                    const bool counts = MODE == kSparseFull && a.cube_valid;
+                    if (counts && qtile >= n_pre)   // real keys of every tile half (boundary cubes)
+                        for (int t = lane; t < nt; t += 32) {
+                            scratch->kv0[t] = static_cast<uint8_t>(cube_count(a, (sl->key0[t] - a.prefix) >> 6));
+                            scratch->kv1[t] = static_cast<uint8_t>(cube_count(a, (sl->key1[t] - a.prefix) >> 6));
+                        }
+                    __syncwarp();
+                    for (int t = lane; t < nt; t += 32)
+                        sl->info[t] = scratch->mask[t] |
+                                      (static_cast<uint32_t>(counts ? scratch->kv0[t] : 64) << 8) |
+                                      (static_cast<uint32_t>(counts ? scratch->kv1[t] : 64) << 16);
+                    it.n_tiles = nt;
+                }
+                if (lane == 0) *dst = it;
+            } else if (lane == 0) {
+                dst->valid = 0;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->item_full[k & 1]);
+            if (!live) break;
+        }
+        // after an abort: draw on to this CTA's last draw (the counter resets itself)
+        if (a.sched)
+            while (!drawn_last) drawn_last = next_item(a, 0) >= a.n_items;
+    } else if (warp == 0) {
         // ================= TMA producer (whole warp; one elected lane issues)
-        if (n_tiles > 0) {
-            int last_it[4] = {-1, -1, -1, -1};
-            if (load_q && !early_q) issue_q();
-            bool ok = true;
-            // paged: lane j holds the cache row of box j (page_box tokens) of the
-            // item after the one being issued; boxes cover the item's 128 keys.
-            const int n_box = MODE == kCausalPaged ? BN / a.page_box : 0;
-            auto page_row = [&](int item) -> int {
-                if (MODE != kCausalPaged || lane >= n_box || item >= 2 * n_tiles) return 0;
-                int t, k0, k1;
-                bool iv;
-                ring_item(item, n_tiles, C::NSB, t, iv);
-                tile_keys(t, k0, k1);
-                const int tok = k0 + lane * a.page_box;
-                const int b = kv_bh / a.hkv;
-                int page = tok < a.seq_k ? a.page_table[static_cast<long long>(b) * a.max_pages +
-                                                        tok / a.page_size]
-                                         : 0;
-                if (page < 0 || page >= a.num_phys) {
-                    atomicOr(a.status, kDevBadPage);
-                    page = 0;
-                }
-                return page * a.page_size + tok % a.page_size;
-            };
-            int prow_next = page_row(0);
-            for (int it = 0; it < 2 * n_tiles; ++it) {
-                if (a.fault == 2 && it >= 2 * C::NS) {   // test hook: stop mid-stream, drain, leave
-                    ok = false;
-                    break;
-                }
-                const int slot = it % C::NS;
-                const int prow_cur = prow_next;
-                if (MODE == kCausalPaged) prow_next = page_row(it + 1);
-                if (!wait_warp(&ctrl->empty[slot], ((it / C::NS) & 1) ^ 1u, w)) { ok = false; break; }
-                int t;
-                bool is_v;
-                ring_item(it, n_tiles, C::NSB, t, is_v);
-                int k0, k1;
-                tile_keys(t, k0, k1);
-                const CUtensorMap* m = is_v ? &tmV : &tmK;
-                uint8_t* dst = sKV + slot * C::SLOT_BYTES;
-                if (MODE == kCausalPaged) {
-                    // E4M3 rows of the item (128 keys x D bytes) into the slot's upper half,
-                    // laid out [key half][column half][64 rows][128 bytes], 128-byte swizzle.
-                    uint8_t* stage = dst + C::SLOT_BYTES / 2;
-                    const int hk = kv_bh % a.hkv;
-                    const int rows_per_box = a.page_box;
-                    int rows[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) rows[j] = __shfl_sync(0xffffffffu, prow_cur, j);
+        int last_it[4] = {-1, -1, -1, -1};   // last ring position issued into each slot
+        int last_q[2] = {-1, -1};            // last use issued into each query buffer
+        int ring = 0, qu = 0;
+        bool ok = true;
+        // paged: lane j holds the cache row of box j (page_box tokens) of the
+        // item after the one being issued; boxes cover the item's 128 keys.
+        const int n_box = MODE == kCausalPaged ? BN / a.page_box : 0;
+        for (int k = 0; ok && (kPersist || k < 1); ++k) {
+            Item cur;
+            ok = get_item(k, cur);
+            if (!ok) break;
+            if (!cur.valid) break;
+            const SparseSlot* sl = slots + (k & 1);
+            const int n = cur.n_tiles;
+            const int qb = cur.bh / a.hq, qh = cur.bh - qb * a.hq;
+            const int kvb = cur.kv_bh / a.hkv, kvh = cur.kv_bh - kvb * a.hkv;
+            if (n > 0) {
+                const int qbuf = qu % C::QB;
+                if (qu >= C::QB) ok = wait_warp(&ctrl->q_empty[qbuf], ((qu / C::QB) - 1) & 1, w);
+                if (!ok) break;
+                if (load_q) {
+                    uint8_t* dq = sQ + qbuf * C::Q_BYTES;
                     if (elect_one()) {
-                        mbar_arrive_expect_tx(&ctrl->raw_full[slot], BN * D);
-                        for (int j = 0; j < n_box; ++j) {
-                            const int key = j * rows_per_box;   // 0..127 within the item
-                            const int kh = key >> 6, r = key & 63;
+                        mbar_arrive_expect_tx(&ctrl->q_full[qbuf], C::Q_BYTES);
+                        if (is_sparse(MODE)) {   // two 64-row halves; tmM has 64-row boxes
+                            const int r1 = cur.rbase1 >= 0 ? cur.rbase1 : cur.rbase0;
 #pragma unroll
-                            for (int ch = 0; ch < D / 128; ++ch)
-                                tma_load_3d(stage + (kh * (D / 128) + ch) * 8192 + r * 128, m,
-                                            &ctrl->raw_full[slot], 128 * ch, hk, rows[j]);
+                            for (int c = 0; c < C::KCH; ++c) {
+                                tma_load_4d(dq + c * C::CHUNK, &tmM, &ctrl->q_full[qbuf], c * 64, cur.rbase0, qh, qb);
+                                tma_load_4d(dq + c * C::CHUNK + C::HALF, &tmM, &ctrl->q_full[qbuf], c * 64, r1, qh, qb);
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < C::KCH; ++c)
+                                tma_load_4d(dq + c * C::CHUNK, &tmQ, &ctrl->q_full[qbuf], c * 64, cur.q_row0, qh, qb);
                         }
                     }
                     __syncwarp();
-                    last_it[slot] = it;
-                    continue;
+                    last_q[qbuf] = qu;
                 }
-                if (elect_one()) {
-                    mbar_arrive_expect_tx(&ctrl->full[slot], C::SLOT_BYTES);
-#pragma unroll
-                    for (int c = 0; c < C::KCH; ++c) {
-                        tma_load_4d(dst + c * C::CHUNK, m, &ctrl->full[slot], c * 64, k0, kvh, kvb);
-                        tma_load_4d(dst + c * C::CHUNK + C::HALF, m, &ctrl->full[slot], c * 64, k1,
-                                    kvh, kvb);
+                ++qu;
+                auto page_row = [&](int item) -> int {
+                    if (MODE != kCausalPaged || lane >= n_box || item >= 2 * n) return 0;
+                    int t, k0, k1;
+                    bool iv;
+                    ring_item(item, n, C::NSB, t, iv);
+                    tile_keys(cur, sl, t, k0, k1);
+                    const int tok = k0 + lane * a.page_box;
+                    const int b = cur.kv_bh / a.hkv;
+                    int page = tok < a.seq_k ? a.page_table[static_cast<long long>(b) * a.max_pages +
+                                                            tok / a.page_size]
+                                             : 0;
+                    if (page < 0 || page >= a.num_phys) {
+                        atomicOr(a.status, kDevBadPage);
+                        page = 0;
                     }
+                    return page * a.page_size + tok % a.page_size;
+                };
+                int prow_next = page_row(0);
+                for (int it = 0; it < 2 * n; ++it) {
+                    const int gi = ring + it;
+                    if (a.fault == 2 && gi >= 2 * C::NS) {   // test hook: stop mid-stream, drain, leave
+                        ok = false;
+                        break;
+                    }
+                    const int slot = slot_of<C::NS>(gi);
+                    const int prow_cur = prow_next;
+                    if (MODE == kCausalPaged) prow_next = page_row(it + 1);
+                    if (!wait_warp(&ctrl->empty[slot], phase_of<C::NS>(gi) ^ 1u, w)) { ok = false; break; }
+                    int t;
+                    bool is_v;
+                    ring_item(it, n, C::NSB, t, is_v);
+                    int k0, k1;
+                    tile_keys(cur, sl, t, k0, k1);
+                    const CUtensorMap* m = is_v ? &tmV : &tmK;
+                    uint8_t* dst = sKV + slot * C::SLOT_BYTES;
+                    if (MODE == kCausalPaged) {
+                        // E4M3 rows of the ring item (128 keys x D bytes) into the slot's upper
+                        // half, laid out [key half][column half][64 rows][128 bytes], 128-byte swizzle.
+                        uint8_t* stage = dst + C::SLOT_BYTES / 2;
+                        const int hk = cur.kv_bh % a.hkv;
+                        const int rows_per_box = a.page_box;
+                        int rows[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) rows[j] = __shfl_sync(0xffffffffu, prow_cur, j);
+                        if (elect_one()) {
+                            mbar_arrive_expect_tx(&ctrl->raw_full[slot], BN * D);
+                            for (int j = 0; j < n_box; ++j) {
+                                const int key = j * rows_per_box;   // 0..127 within the ring item
+                                const int kh = key >> 6, r = key & 63;
+#pragma unroll
+                                for (int ch = 0; ch < D / 128; ++ch)
+                                    tma_load_3d(stage + (kh * (D / 128) + ch) * 8192 + r * 128, m,
+                                                &ctrl->raw_full[slot], 128 * ch, hk, rows[j]);
+                            }
+                        }
+                        __syncwarp();
+                        last_it[slot] = gi;
+                        continue;
+                    }
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(&ctrl->full[slot], C::SLOT_BYTES);
+#pragma unroll
+                        for (int c = 0; c < C::KCH; ++c) {
+                            tma_load_4d(dst + c * C::CHUNK, m, &ctrl->full[slot], c * 64, k0, kvh, kvb);
+                            tma_load_4d(dst + c * C::CHUNK + C::HALF, m, &ctrl->full[slot], c * 64, k1,
+                                        kvh, kvb);
+                        }
+                    }
+                    __syncwarp();
+                    last_it[slot] = gi;
                 }
-                __syncwarp();
-                last_it[slot] = it;
+                ring += 2 * n;
             }
-            if (!ok && lane == 0) {   // let copies in flight land before the CTA exits
-                if (load_q) drain_wait(&ctrl->q_full, 0);
-                for (int s = 0; s < C::NS; ++s)
-                    if (last_it[s] >= 0)
-                        drain_wait(MODE == kCausalPaged ? &ctrl->raw_full[s] : &ctrl->full[s],
-                                   (last_it[s] / C::NS) & 1);
-            }
-        } else if (early_q) {   // an empty key list (bad indices): nobody waits for Q
-            if (lane == 0) drain_wait(&ctrl->q_full, 0);
-            __syncwarp();
+            if (!ok) break;
+            item_release(k);
         }
+        if (!ok && lane == 0) {   // let copies in flight land before the CTA exits
+            for (int b = 0; b < C::QB; ++b)
+                if (last_q[b] >= 0) drain_wait(&ctrl->q_full[b], (last_q[b] / C::QB) & 1);
+            for (int s = 0; s < C::NS; ++s)
+                if (last_it[s] >= 0)
+                    drain_wait(MODE == kCausalPaged ? &ctrl->raw_full[s] : &ctrl->full[s],
+                               phase_of<C::NS>(last_it[s]));
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ================= MMA issuer (whole warp waits; one elected lane issues
         // each group of MMAs and its commits)
-        if (n_tiles > 0) {
-            bool ok = wait_warp(&ctrl->q_full, 0, w);
+        int tb = 0, qu = 0, o_uses = 0;
+        Cursor<C::NSB> sb;   // S buffer and phase of tile tb + t (QK order = PV order)
+        bool ok = true;
+        for (int k = 0; ok && (kPersist || k < 1); ++k) {
+            Item cur;
+            ok = get_item(k, cur);
+            if (!ok) break;
+            const int valid = cur.valid, n = cur.n_tiles;
+            item_release(k);
+            if (!valid) break;
+            if (n == 0) continue;
+            const int qbuf = qu % C::QB;
+            ok = wait_warp(&ctrl->q_full[qbuf], (qu / C::QB) & 1, w);
+            ++qu;
+            if (!ok) break;
             if (dual_issue(MODE)) {
-                // QK only (warp 10 issues PV).  QK_t overwrites the S buffer that
-                // PV_{t-NSB} read P_{t-NSB} from, so it waits for that PV to finish.
+                // QK only (warp 10 issues PV).  QK_g overwrites the S buffer that
+                // PV_{g-NSB} read P_{g-NSB} from, so it waits for that PV to finish.
                 // A parity wait on a slot is unambiguous only if the slot's previous
-                // item is known to have landed: here it is either an earlier K (this
-                // warp waited for it) or a V_i that precedes K_t in the ring, so
-                // i <= t-NSB (K_t follows V_{t-NSB}) and PV_i finished with PV_{t-NSB}.
-                for (int t = 0; ok && t < n_tiles; ++t) {
-                    const int pos = pos_k(t);
-                    const int slot = pos % C::NS;
-                    const int buf = t % C::NSB;
-                    if (t >= C::NSB) ok = wait_warp(&ctrl->pv_done[buf], ((t - C::NSB) / C::NSB) & 1, w);
-                    ok = ok && wait_warp(&ctrl->full[slot], (pos / C::NS) & 1, w);
+                // ring item is known to have landed: here it is either an earlier K
+                // (this warp waited for it) or a V_i that precedes K_g in the ring,
+                // so i <= g-NSB (within an item K_t follows V_{t-NSB}; the first
+                // NSB K of an item follow every V of the items before) and PV_i
+                // finished with PV_{g-NSB}.
+                for (int t = 0; t < n; ++t) {
+                    const int g = tb + t;
+                    const int pos = 2 * tb + pos_k(t);
+                    const int slot = slot_of<C::NS>(pos);
+                    const int buf = sb.idx;
+                    // PV_{g-NSB}: same buffer, previous phase
+                    if (g >= C::NSB) ok = wait_warp(&ctrl->pv_done[buf], sb.phase ^ 1u, w);
+                    ok = ok && wait_warp(&ctrl->full[slot], phase_of<C::NS>(pos), w);
+                    sb.step();
                     if (!ok) break;
                     tc_fence_after();
                     if (elect_one()) {
-                        issue_qk(slot, buf);
+                        issue_qk(qbuf, slot, buf);
                         mma_commit(&ctrl->s_full[buf]);
                         mma_commit(&ctrl->empty[slot]);
+                        if (t == n - 1) mma_commit(&ctrl->q_empty[qbuf]);
                     }
                     __syncwarp();
                 }
             } else {
-                int it = 0;
-                // S_0 .. S_{L-1} up front, then per tile: PV_j, and QK_{j+L} into the
-                // buffer P_j has just been read from (in order on the tensor pipe).
-                for (int t = 0; ok && t < min(n_tiles, C::NSB); ++t) {
-                    const int slot = it % C::NS;
-                    ok = wait_warp(&ctrl->full[slot], (it / C::NS) & 1, w);
+                int it = 2 * tb;
+                // S_0 .. S_{L-1} of the item up front (into buffers whose previous
+                // PV this thread issued earlier: in order on the tensor pipe), then
+                // per tile: PV_j, and QK_{j+L} into the buffer P_j has just been
+                // read from.
+                for (int t = 0; ok && t < min(n, C::NSB); ++t) {
+                    const int slot = slot_of<C::NS>(it);
+                    ok = wait_warp(&ctrl->full[slot], phase_of<C::NS>(it), w);
                     if (!ok) break;
+                    const int buf = (sb.idx + t) % C::NSB;
                     tc_fence_after();
                     if (elect_one()) {
-                        issue_qk(slot, t);
-                        mma_commit(&ctrl->s_full[t]);
+                        issue_qk(qbuf, slot, buf);
+                        mma_commit(&ctrl->s_full[buf]);
                         mma_commit(&ctrl->empty[slot]);
+                        if (t == n - 1) mma_commit(&ctrl->q_empty[qbuf]);
                     }
                     __syncwarp();
                     ++it;
                 }
-                for (int j = 0; ok && j < n_tiles; ++j) {
-                    const int buf = j % C::NSB;
-                    const int vslot = it % C::NS;
-                    ok = wait_warp(&ctrl->p_full[buf], (j / C::NSB) & 1, w) &&
-                         wait_warp(&ctrl->full[vslot], (it / C::NS) & 1, w);
+                for (int j = 0; ok && j < n; ++j) {
+                    const int buf = sb.idx;
+                    const int vslot = slot_of<C::NS>(it);
+                    ok = wait_warp(&ctrl->p_full[buf], sb.phase, w) &&
+                         wait_warp(&ctrl->full[vslot], phase_of<C::NS>(it), w);
+                    sb.step();
+                    // the item's first PV overwrites O: the previous item's O must be read
+                    if (ok && j == 0 && o_uses > 0) ok = wait_warp(&ctrl->o_free, (o_uses - 1) & 1, w);
                     if (!ok) break;
                     ++it;
                     tc_fence_after();
@@ -727,51 +925,69 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                         mma_commit(&ctrl->pv_done[buf]);
                     }
                     __syncwarp();
-                    if (j + C::NSB < n_tiles) {
-                        const int kslot = it % C::NS;
-                        ok = wait_warp(&ctrl->full[kslot], (it / C::NS) & 1, w);
+                    if (j + C::NSB < n) {
+                        const int kslot = slot_of<C::NS>(it);
+                        ok = wait_warp(&ctrl->full[kslot], phase_of<C::NS>(it), w);
                         if (!ok) break;
                         ++it;
                         tc_fence_after();
                         if (elect_one()) {
-                            issue_qk(kslot, buf);
+                            issue_qk(qbuf, kslot, buf);
                             mma_commit(&ctrl->s_full[buf]);
                             mma_commit(&ctrl->empty[kslot]);
+                            if (j + C::NSB == n - 1) mma_commit(&ctrl->q_empty[qbuf]);
                         }
                         __syncwarp();
                     }
                 }
+                ++o_uses;
             }
-            if (!ok) {   // wait for issued MMAs before tensor memory is freed
-                if (elect_one()) mma_commit(&ctrl->drain);
-                __syncwarp();
-                if (lane == 0) drain_wait(&ctrl->drain, 0);
-            }
+            tb += n;
+        }
+        if (!ok) {   // wait for issued MMAs before tensor memory is freed
+            if (elect_one()) mma_commit(&ctrl->drain);
+            __syncwarp();
+            if (lane == 0) drain_wait(&ctrl->drain, 0);
         }
     } else if (dual_issue(MODE) && warp == kPvWarp) {
         // ================= PV issuer (D=128 modes; whole warp waits, one elected
-        // lane issues).  PV_j waits for P_j (the softmax is done with S_j, so
-        // every QK_t with t <= j has finished) and for V_j in the ring.  A parity
-        // wait on a slot is unambiguous only if the slot's previous item is known
-        // to have landed: an earlier V (this warp waited for it) or a K_t with
-        // t <= j is; a K_t with t > j (a 3-slot ring: t = j+1) is first awaited
-        // through its QK.  That QK wait is itself unambiguous: K_t precedes V_j in
-        // the ring, so t <= j+NSB-1 and QK_{t-NSB} finished before S_j was read.
-        if (n_tiles > 0) {
-            bool ok = true;
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int pos = pos_v(j);
-                const int slot = pos % C::NS;
-                const int buf = j % C::NSB;
-                ok = wait_warp(&ctrl->p_full[buf], (j / C::NSB) & 1, w);
-                if (ok && pos >= C::NS) {
+        // lane issues).  PV_g waits for P_g (the softmax is done with S_g, so
+        // every QK up to g has finished) and for V_g in the ring.  A parity wait
+        // on a slot is unambiguous only if the slot's previous ring item is known
+        // to have landed: an earlier V (this warp waited for it), a K_t with
+        // t <= g, or a K of an earlier item is; a K_t of the same item with t > j
+        // (a 3-slot ring: t = j+1) is first awaited through its QK.  That QK wait
+        // is itself unambiguous: K_t precedes V_j in the ring, so t <= j+NSB-1
+        // and QK_{t-NSB} finished before S_j was read.
+        int tb = 0, o_uses = 0;
+        Cursor<C::NSB> sb;   // S buffer and phase of tile tb + j
+        bool ok = true;
+        for (int k = 0; ok && (kPersist || k < 1); ++k) {
+            Item cur;
+            ok = get_item(k, cur);
+            if (!ok) break;
+            const int valid = cur.valid, n = cur.n_tiles;
+            item_release(k);
+            if (!valid) break;
+            if (n == 0) continue;
+            // the item's first PV overwrites O: the previous item's O must be read
+            if (o_uses > 0) ok = wait_warp(&ctrl->o_free, (o_uses - 1) & 1, w);
+            ++o_uses;
+            for (int j = 0; ok && j < n; ++j) {
+                const int rpos = pos_v(j, n);
+                const int pos = 2 * tb + rpos;
+                const int slot = slot_of<C::NS>(pos);
+                const int buf = sb.idx;
+                ok = wait_warp(&ctrl->p_full[buf], sb.phase, w);
+                sb.step();
+                if (ok && rpos >= C::NS) {
                     int pt;
                     bool pv;
-                    ring_item(pos - C::NS, n_tiles, C::NSB, pt, pv);
+                    ring_item(rpos - C::NS, n, C::NSB, pt, pv);
                     if (!pv && pt > j)
-                        ok = wait_warp(&ctrl->s_full[pt % C::NSB], (pt / C::NSB) & 1, w);
+                        ok = wait_warp(&ctrl->s_full[(tb + pt) % C::NSB], ((tb + pt) / C::NSB) & 1, w);
                 }
-                ok = ok && wait_warp(&ctrl->full[slot], (pos / C::NS) & 1, w);
+                ok = ok && wait_warp(&ctrl->full[slot], phase_of<C::NS>(pos), w);
                 if (!ok) break;
                 tc_fence_after();
                 if (elect_one()) {
@@ -781,105 +997,126 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                 }
                 __syncwarp();
             }
-            if (!ok) {   // wait for issued MMAs before tensor memory is freed
-                if (elect_one()) mma_commit(&ctrl->drain_pv);
-                __syncwarp();
-                if (lane == 0) drain_wait(&ctrl->drain_pv, 0);
-            }
+            tb += n;
+        }
+        if (!ok) {   // wait for issued MMAs before tensor memory is freed
+            if (elect_one()) mma_commit(&ctrl->drain_pv);
+            __syncwarp();
+            if (lane == 0) drain_wait(&ctrl->drain_pv, 0);
         }
     } else if (MODE == kCausalPaged && warp >= 10) {
         // ================= E4M3 -> FP16 converters (warps 10..13, paged mode)
-        // Thread ct owns key row ct of every item: it reads the row's D E4M3 bytes
-        // from the slot's upper half into registers, waits for the other
+        // Thread ct owns key row ct of every ring item: it reads the row's D E4M3
+        // bytes from the slot's upper half into registers, waits for the other
         // converters (the FP16 tile overwrites that half), then writes the FP16
         // row into the 128-byte-swizzled K-major layout TMA would have produced.
         const int ct = threadIdx.x - 320;
         const int kh = ct >> 6, rr = ct & 63;
         bool ok = true;
-        for (int it = 0; it < 2 * n_tiles; ++it) {
-            const int slot = it % C::NS;
-            ok = wait_warp(&ctrl->raw_full[slot], (it / C::NS) & 1, w);
+        int ring = 0;
+        for (int k = 0; ok && (kPersist || k < 1); ++k) {
+            Item cur;
+            ok = get_item(k, cur);
             if (!ok) break;
-            int t;
-            bool is_v;
-            ring_item(it, n_tiles, C::NSB, t, is_v);
-            uint8_t* dst = sKV + slot * C::SLOT_BYTES;
-            const uint8_t* stage = dst + C::SLOT_BYTES / 2;
-            uint4 raw[D / 16];
+            if (!cur.valid) break;
+            const int n = cur.n_tiles;
+            for (int it = 0; it < 2 * n; ++it) {
+                const int gi = ring + it;
+                const int slot = slot_of<C::NS>(gi);
+                ok = wait_warp(&ctrl->raw_full[slot], phase_of<C::NS>(gi), w);
+                if (!ok) break;
+                int t;
+                bool is_v;
+                ring_item(it, n, C::NSB, t, is_v);
+                uint8_t* dst = sKV + slot * C::SLOT_BYTES;
+                const uint8_t* stage = dst + C::SLOT_BYTES / 2;
+                uint4 raw[D / 16];
 #pragma unroll
-            for (int ch = 0; ch < D / 128; ++ch)
+                for (int ch = 0; ch < D / 128; ++ch)
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    raw[ch * 8 + u] = *reinterpret_cast<const uint4*>(
-                        stage + (kh * (D / 128) + ch) * 8192 + rr * 128 + ((u ^ (rr & 7)) << 4));
-            // all converters must hold their bytes before any FP16 lands on the bytes
-            // (a time-bounded barrier wait, like every other wait of the kernel)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->conv_read[slot]);
-            ok = wait_warp(&ctrl->conv_read[slot], (it / C::NS) & 1, w);
-            if (!ok) break;
-            const float sc = is_v ? a.vs : a.ks;
-            const __half2 sc2 = is_v ? a.vs2 : a.ks2;
-            int k0, k1;
-            tile_keys(t, k0, k1);
-            const bool live_key = k0 + ct < a.seq_k;   // rows past the cache end become zeros
+                    for (int u = 0; u < 8; ++u)
+                        raw[ch * 8 + u] = *reinterpret_cast<const uint4*>(
+                            stage + (kh * (D / 128) + ch) * 8192 + rr * 128 + ((u ^ (rr & 7)) << 4));
+                // all converters must hold their bytes before any FP16 lands on the bytes
+                // (a time-bounded barrier wait, like every other wait of the kernel)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->conv_read[slot]);
+                ok = wait_warp(&ctrl->conv_read[slot], phase_of<C::NS>(gi), w);
+                if (!ok) break;
+                const float sc = is_v ? a.vs : a.ks;
+                const __half2 sc2 = is_v ? a.vs2 : a.ks2;
+                const int k0 = (cur.tile0 + t) * BN;
+                const bool live_key = k0 + ct < a.seq_k;   // rows past the cache end become zeros
 #pragma unroll
-            for (int q = 0; q < D / 16; ++q) {   // 16 E4M3 bytes -> 16 halves (2 units)
-                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                if (live_key) {
-                    if (a.scale_mode == 2) {
-                        convert16<false>(raw[q], sc2, sc, lo, hi);
-                    } else if (a.scale_mode == 1) {
-                        convert16<true>(raw[q], sc2, sc, lo, hi);
-                    } else {   // power-of-two scale: applied to the scores and outputs instead
-                        const uint32_t w4[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
-                        uint32_t h[8];
+                for (int q = 0; q < D / 16; ++q) {   // 16 E4M3 bytes -> 16 halves (2 units)
+                    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+                    if (live_key) {
+                        if (a.scale_mode == 2) {
+                            convert16<false>(raw[q], sc2, sc, lo, hi);
+                        } else if (a.scale_mode == 1) {
+                            convert16<true>(raw[q], sc2, sc, lo, hi);
+                        } else {   // power-of-two scale: applied to the scores and outputs instead
+                            const uint32_t w4[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+                            uint32_t h[8];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            h[2 * i] = e4m3x2_to_f16x2(w4[i] & 0xFFFFu);
-                            h[2 * i + 1] = e4m3x2_to_f16x2(w4[i] >> 16);
+                            for (int i = 0; i < 4; ++i) {
+                                h[2 * i] = e4m3x2_to_f16x2(w4[i] & 0xFFFFu);
+                                h[2 * i + 1] = e4m3x2_to_f16x2(w4[i] >> 16);
+                            }
+                            lo = make_uint4(h[0], h[1], h[2], h[3]);
+                            hi = make_uint4(h[4], h[5], h[6], h[7]);
                         }
-                        lo = make_uint4(h[0], h[1], h[2], h[3]);
-                        hi = make_uint4(h[4], h[5], h[6], h[7]);
                     }
+                    const int d0 = q * 16;            // head-width position of the 16 values
+                    const int c = d0 >> 6, u0 = (d0 & 63) >> 3;
+                    uint8_t* row = dst + c * C::CHUNK + kh * C::HALF + rr * 128;
+                    *reinterpret_cast<uint4*>(row + ((u0 ^ (rr & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ (rr & 7)) << 4)) = hi;
                 }
-                const int d0 = q * 16;            // head-width position of the 16 values
-                const int c = d0 >> 6, u0 = (d0 & 63) >> 3;
-                uint8_t* row = dst + c * C::CHUNK + kh * C::HALF + rr * 128;
-                *reinterpret_cast<uint4*>(row + ((u0 ^ (rr & 7)) << 4)) = lo;
-                *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ (rr & 7)) << 4)) = hi;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the MMAs
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->full[slot]);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the MMAs
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->full[slot]);
+            if (!ok) break;
+            ring += 2 * n;
+            item_release(k);
         }
-        (void)ok;
     } else if (MODE == kMasked && warp == kMaskWarp) {
-        // ================= mask loader (masked mode): tile t's mask rows into slot
-        // t % 2 once every softmax warp has read tile t - 2 from it
-        const int mb_b = bh / a.hq, mb_h = bh - mb_b * a.hq;
+        // ================= mask loader (masked mode): tile g's mask rows into slot
+        // g % 2 once every softmax warp has read tile g - 2 from it
         bool ok = true;
-        int issued = 0;
-        for (int t = 0; t < n_tiles; ++t) {
-            if (t >= 2 && !wait_warp(&mbar[2 + (t & 1)], ((t >> 1) - 1) & 1, w)) {
-                ok = false;
-                break;
+        int tb = 0, issued = 0;
+        for (int k = 0; ok && (kPersist || k < 1); ++k) {
+            Item cur;
+            ok = get_item(k, cur);
+            if (!ok) break;
+            if (!cur.valid) break;
+            const int mb_b = cur.bh / a.hq, mb_h = cur.bh - mb_b * a.hq;
+            for (int t = 0; t < cur.n_tiles; ++t) {
+                const int g = tb + t;
+                if (g >= 2 && !wait_warp(&mbar[2 + (g & 1)], ((g >> 1) - 1) & 1, w)) {
+                    ok = false;
+                    break;
+                }
+                int f0, f1;
+                tile_keys(cur, nullptr, t, f0, f1);
+                if (elect_one()) {
+                    uint8_t* dst = sMask + (g & 1) * kMaskSlotBytes;
+                    mbar_arrive_expect_tx(&mbar[g & 1], kMaskSlotBytes);
+                    tma_load_4d(dst, &tmM, &mbar[g & 1], f0, cur.q_row0, a.mask_sh ? mb_h : 0,
+                                a.mask_sb ? mb_b : 0);
+                    tma_load_4d(dst + kMaskSlotBytes / 2, &tmM, &mbar[g & 1], f1, cur.q_row0,
+                                a.mask_sh ? mb_h : 0, a.mask_sb ? mb_b : 0);
+                }
+                __syncwarp();
+                issued = g + 1;
             }
-            int f0, f1;
-            tile_keys(t, f0, f1);
-            if (elect_one()) {
-                uint8_t* dst = sMask + (t & 1) * kMaskSlotBytes;
-                mbar_arrive_expect_tx(&mbar[t & 1], kMaskSlotBytes);
-                tma_load_4d(dst, &tmM, &mbar[t & 1], f0, q_row0, a.mask_sh ? mb_h : 0,
-                            a.mask_sb ? mb_b : 0);
-                tma_load_4d(dst + kMaskSlotBytes / 2, &tmM, &mbar[t & 1], f1, q_row0,
-                            a.mask_sh ? mb_h : 0, a.mask_sb ? mb_b : 0);
-            }
-            __syncwarp();
-            issued = t + 1;
+            if (!ok) break;
+            tb += cur.n_tiles;
+            item_release(k);
         }
         if (!ok && lane == 0)   // copies in flight must land before the CTA exits
-            for (int t = max(0, issued - 2); t < issued; ++t) drain_wait(&mbar[t & 1], (t >> 1) & 1);
+            for (int g = max(0, issued - 2); g < issued; ++g) drain_wait(&mbar[g & 1], (g >> 1) & 1);
         __syncwarp();
     } else {
         // ================= softmax / correction / epilogue (warps 2..9)
@@ -891,278 +1128,311 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         const int half = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        // token row of this thread's query row (a missing second cube: past the end)
-        const int rb = row < 64 ? rbase0 : rbase1;
-        const long long row_g = rb < 0 ? static_cast<long long>(a.seq_q) : static_cast<long long>(rb) + (row & 63);
         const int row_half = row >> 6;
         uint64_t* xbar = &ctrl->xchg[quarter];
-        bool pad_row = false;   // a padding query slot of a boundary cube, read before the loop
-        if (MODE == kSparseFull && a.cube_valid && row_g >= a.prefix && row_g < a.seq_q) {
-            const int vr = static_cast<int>(row_g - a.prefix);
-            pad_row = (vr & 63) >= cube_count(a, vr >> 6);
-        }
-        int lim = a.seq_k;   // keys >= lim are invisible to this row
-        if (is_causal(MODE))
-            lim = static_cast<int>(min(static_cast<long long>(a.seq_k), a.kv_prefix + row_g + 1));
-        const int lim0 = is_causal(MODE)
-                             ? static_cast<int>(min(static_cast<long long>(a.seq_k),
-                                                    static_cast<long long>(a.kv_prefix) + q_row0 + 1))
-                             : a.seq_k;
         // Exponent factor: scores arrive raw (scale*log2e applies), or in masked
         // mode as y = scale*s + mask (log2e applies).
         const float sl2 = MODE == kMasked ? 1.4426950408889634f : a.scale_log2;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
-        float m_run = -INFINITY, l = 0.0f;
         uint32_t xphase = 0;
+        Cursor<C::NSB> sc;   // S buffer and phase of the CTA's tile g
+        Cursor<2> gp;        // g & 1 and (g >> 1) & 1 (exchange buffer, mask slot)
+        int prev_buf = 0;    // S buffer and phase of tile g - 1
+        uint32_t prev_phase = 0;
         bool ok = true;
-        // Masked mode: tile t's mask arrives in slot t % 2, this thread's row of
-        // its half at [half][row][128 bytes] (staged by the mask warp).
-        for (int j = 0; j < n_tiles; ++j) {
-            const int buf = j % C::NSB;
-            const uint32_t sbuf = tl + buf * 128;
-            // Sparse modes: this half's visible-column limit (a hidden quadrant 0, a
-            // boundary cube its real-key count), read before S arrives so that its
-            // shared-memory latency stays off the path from S to P.
-            int lim_c = 64;
-            if (is_sparse(MODE)) {
-                const uint32_t ti = st->info[j];
-                const bool vis = (ti >> (row_half * 2 + half)) & 1u;
-                // plain VSA: all 64 keys or none (a limit the compiler can see)
-                lim_c = !vis ? 0 : MODE == kSparseFull ? static_cast<int>((ti >> (8 + 8 * half)) & 0xFFu) : 64;
-            }
-            ok = wait_warp(&ctrl->s_full[buf], (j / C::NSB) & 1, w);
+        for (int k = 0; ok && (kPersist || k < 1); ++k) {
+            Item cur;
+            ok = get_item(k, cur);
             if (!ok) break;
-            tc_fence_after();
-            uint32_t s[64];
-            tmem_ld32(sbuf + half * 64, s);
-            tmem_ld32(sbuf + half * 64 + 32, s + 32);
-            tmem_ld_wait();
-
-            int k0, k1;
-            tile_keys(j, k0, k1);
-            if (MODE == kMasked) {
-                // y = scale * s + mask, then hidden keys -> -inf.
-                ok = wait_warp(&mbar[j & 1], (j >> 1) & 1, w);
+            if (!cur.valid) break;
+            const SparseSlot* sl = slots + (k & 1);
+            const int n_tiles = cur.n_tiles;
+            // token row of this thread's query row (a missing second cube: past the end)
+            const int rb = row < 64 ? cur.rbase0 : cur.rbase1;
+            const long long row_g =
+                rb < 0 ? static_cast<long long>(a.seq_q) : static_cast<long long>(rb) + (row & 63);
+            bool pad_row = false;   // a padding query slot of a boundary cube, read before the loop
+            if (MODE == kSparseFull && a.cube_valid && row_g >= a.prefix && row_g < a.seq_q) {
+                const int vr = static_cast<int>(row_g - a.prefix);
+                pad_row = (vr & 63) >= cube_count(a, vr >> 6);
+            }
+            int lim = a.seq_k;   // keys >= lim are invisible to this row
+            if (is_causal(MODE))
+                lim = static_cast<int>(min(static_cast<long long>(a.seq_k), a.kv_prefix + row_g + 1));
+            const int lim0 = is_causal(MODE)
+                                 ? static_cast<int>(min(static_cast<long long>(a.seq_k),
+                                                        static_cast<long long>(a.kv_prefix) + cur.q_row0 + 1))
+                                 : a.seq_k;
+            float m_run = -INFINITY, l = 0.0f;
+            // Masked mode: tile g's mask arrives in slot g % 2, this thread's row of
+            // its half at [half][row][128 bytes] (staged by the mask warp).
+            for (int j = 0; j < n_tiles; ++j) {
+                const int buf = sc.idx;
+                const uint32_t sphase = sc.phase;
+                const int gb = gp.idx;               // g & 1
+                const uint32_t gph = gp.phase;       // (g >> 1) & 1
+                const uint32_t sbuf = tl + buf * 128;
+                // Sparse modes: this half's visible-column limit (a hidden quadrant 0, a
+                // boundary cube its real-key count), read before S arrives so that its
+                // shared-memory latency stays off the path from S to P.
+                int lim_c = 64;
+                if (is_sparse(MODE)) {
+                    const uint32_t ti = sl->info[j];
+                    const bool vis = (ti >> (row_half * 2 + half)) & 1u;
+                    // plain VSA: all 64 keys or none (a limit the compiler can see)
+                    lim_c = !vis ? 0 : MODE == kSparseFull ? static_cast<int>((ti >> (8 + 8 * half)) & 0xFFu) : 64;
+                }
+                ok = wait_warp(&ctrl->s_full[buf], sphase, w);
                 if (!ok) break;
-                const uint64_t sc2 = f2_pack(a.scale, a.scale);
-                const uint8_t* mrow =
-                    sMask + (j & 1) * kMaskSlotBytes + half * (kMaskSlotBytes / 2) + row * 128;
+                tc_fence_after();
+                uint32_t s[64];
+                tmem_ld32(sbuf + half * 64, s);
+                tmem_ld32(sbuf + half * 64 + 32, s + 32);
+                tmem_ld_wait();
+
+                int k0, k1;
+                tile_keys(cur, sl, j, k0, k1);
+                if (MODE == kMasked) {
+                    // y = scale * s + mask, then hidden keys -> -inf.
+                    ok = wait_warp(&mbar[gb], gph, w);
+                    if (!ok) break;
+                    const uint64_t sc2 = f2_pack(a.scale, a.scale);
+                    const uint8_t* mrow =
+                        sMask + gb * kMaskSlotBytes + half * (kMaskSlotBytes / 2) + row * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 mv = *reinterpret_cast<const uint4*>(mrow + ((c ^ (lane & 7)) << 4));
-                    const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 mv = *reinterpret_cast<const uint4*>(mrow + ((c ^ (lane & 7)) << 4));
+                        const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = 4 * c + e;   // key pair 2i, 2i+1
-                        const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mw[e]));
-                        float x0, x1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
-                                         sc2, f2_pack(mf.x, mf.y)),
-                                  x0, x1);
-                        s[2 * i] = __float_as_uint(x0);
-                        s[2 * i + 1] = __float_as_uint(x1);
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 4 * c + e;   // key pair 2i, 2i+1
+                            const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mw[e]));
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                             sc2, f2_pack(mf.x, mf.y)),
+                                      x0, x1);
+                            s[2 * i] = __float_as_uint(x0);
+                            s[2 * i + 1] = __float_as_uint(x1);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&mbar[2 + gb]);   // this warp is done with the slot
+                    // keys past the end and rows past the end hidden through one column limit
+                    const int kh = half ? k1 : k0;
+                    const int lim_m = row_g >= a.seq_q ? 0 : a.seq_k - kh;
+                    if (lim_m < 64) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (c >= lim_m) s[c] = __float_as_uint(-INFINITY);
+                    }
+                } else if (is_sparse(MODE)) {
+                    // One column limit per tile half (read above): a quadrant hidden from
+                    // this row's cube hides all 64 keys, a boundary cube its padding keys.
+                    // (Two separate masking loops here had cost the full-layout kernel 45
+                    // registers and a quarter of its speed.)
+                    if (lim_c < 64) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (c >= lim_c) s[c] = __float_as_uint(-INFINITY);
+                    }
+                } else {
+                    const int kh = half ? k1 : k0;
+                    if (kh + 64 > lim0) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (kh + c >= lim) s[c] = __float_as_uint(-INFINITY);
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&mbar[2 + (j & 1)]);   // this warp is done with the slot
-                // keys past the end and rows past the end hidden through one column limit
-                const int kh = half ? k1 : k0;
-                const int lim_c = row_g >= a.seq_q ? 0 : a.seq_k - kh;
-                if (lim_c < 64) {
+                // row max of the 64 values with four independent chains (short latency):
+                // s[0..3] start the chains, s[4..59] in seven steps of eight, s[60..63] last
+                float m4[4];
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (c >= lim_c) s[c] = __float_as_uint(-INFINITY);
-                }
-            } else if (is_sparse(MODE)) {
-                // One column limit per tile half (read above): a quadrant hidden from
-                // this row's cube hides all 64 keys, a boundary cube its padding keys.
-                // (Two separate masking loops here had cost the full-layout kernel 45
-                // registers and a quarter of its speed.)
-                if (lim_c < 64) {
+                for (int q = 0; q < 4; ++q) m4[q] = __uint_as_float(s[q]);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (c >= lim_c) s[c] = __float_as_uint(-INFINITY);
-                }
-            } else {
-                const int kh = half ? k1 : k0;
-                if (kh + 64 > lim0) {
+                for (int c = 4; c < 60; c += 8) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (kh + c >= lim) s[c] = __float_as_uint(-INFINITY);
+                    for (int q = 0; q < 4; ++q)
+                        m4[q] = max3f(m4[q], __uint_as_float(s[c + q]), __uint_as_float(s[c + 4 + q]));
                 }
+                m4[0] = max3f(m4[0], __uint_as_float(s[60]), __uint_as_float(s[61]));
+                m4[1] = max3f(m4[1], __uint_as_float(s[62]), __uint_as_float(s[63]));
+                const float pm = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
+                ex->mx[gb][half][row] = pm;
+                tc_fence_before();   // our S loads are ordered before the partner's P stores
+                mbar_arrive(xbar);
+                ok = wait_warp(xbar, xphase, w);
+                xphase ^= 1u;
+                if (!ok) break;
+                tc_fence_after();
+                const float mx = fmaxf(pm, ex->mx[gb][half ^ 1][row]);
+                const float m_new = fmaxf(m_run, mx * sl2);
+                const bool need = m_new > m_run + 8.0f;
+                float alpha = 1.0f;
+                if (need) {
+                    alpha = fast_exp2(m_run - m_new);
+                    m_run = m_new;
+                }
+                const bool warp_need = __any_sync(0xffffffffu, need);
+                const float m_use = m_run == -INFINITY ? 0.0f : m_run;
+                const uint64_t negm = f2_pack(-m_use, -m_use);
+                uint64_t rs[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) rs[q] = f2_pack(0.0f, 0.0f);
+                uint32_t p2[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                     sl2x2, negm),
+                              x0, x1);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    rs[i & 3] = f2_add(rs[i & 3], f2_pack(p0, p1));   // four independent sums
+                    p2[i] = pack_half2(p0, p1);
+                    if (PS) {   // keep p for its low half
+                        s[2 * i] = __float_as_uint(p0);
+                        s[2 * i + 1] = __float_as_uint(p1);
+                    }
+                }
+                float r0, r1, r2, r3, r4, r5, r6, r7;
+                f2_unpack(rs[0], r0, r1);
+                f2_unpack(rs[1], r2, r3);
+                f2_unpack(rs[2], r4, r5);
+                f2_unpack(rs[3], r6, r7);
+                l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
+                // P_g over the first 64 columns of its S buffer; both threads of the
+                // row have loaded their S halves (they passed the exchange above).
+                tmem_st32(sbuf + half * 32, p2);
+                if (PS) {   // lo = RNE(p - hi); p - hi is exact in FP32
+                    uint32_t lo2[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&p2[i]));
+                        lo2[i] = pack_half2(__uint_as_float(s[2 * i]) - h.x, __uint_as_float(s[2 * i + 1]) - h.y);
+                    }
+                    tmem_st32(sbuf + 64 + half * 32, lo2);
+                }
+                tmem_st_wait();
+                if (warp_need && j > 0) {   // rescale this thread's half of O after PV_{g-1}
+                    ok = wait_warp(&ctrl->pv_done[prev_buf], prev_phase, w);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        const uint32_t col = tl + C::T_O + half * (D / 2) + cc * 32;
+                        uint32_t o[32];
+                        tmem_ld32(col, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            float y0, y1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), a2),
+                                      y0, y1);
+                            o[2 * e] = __float_as_uint(y0);
+                            o[2 * e + 1] = __float_as_uint(y1);
+                        }
+                        tmem_st32(col, o);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                mbar_arrive(&ctrl->p_full[buf]);
+                prev_buf = buf;
+                prev_phase = sphase;
+                sc.step();
+                gp.step();
             }
-            // row max of the 64 values with four independent chains (short latency):
-            // s[0..3] start the chains, s[4..59] in seven steps of eight, s[60..63] last
-            float m4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) m4[k] = __uint_as_float(s[k]);
-#pragma unroll
-            for (int c = 4; c < 60; c += 8) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    m4[k] = max3f(m4[k], __uint_as_float(s[c + k]), __uint_as_float(s[c + 4 + k]));
+            if (!ok) break;
+            if (n_tiles > 0) {   // PV of the item's last tile
+                ok = wait_warp(&ctrl->pv_done[prev_buf], prev_phase, w);
+                tc_fence_after();
             }
-            m4[0] = max3f(m4[0], __uint_as_float(s[60]), __uint_as_float(s[61]));
-            m4[1] = max3f(m4[1], __uint_as_float(s[62]), __uint_as_float(s[63]));
-            const float pm = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
-            ex->mx[j & 1][half][row] = pm;
-            tc_fence_before();   // our S loads are ordered before the partner's P stores
+            if (!ok) break;
+            // combine the two partial row sums
+            ex->l[half][row] = l;
             mbar_arrive(xbar);
             ok = wait_warp(xbar, xphase, w);
             xphase ^= 1u;
             if (!ok) break;
-            tc_fence_after();
-            const float mx = fmaxf(pm, ex->mx[j & 1][half ^ 1][row]);
-            const float m_new = fmaxf(m_run, mx * sl2);
-            const bool need = m_new > m_run + 8.0f;
-            float alpha = 1.0f;
-            if (need) {
-                alpha = fast_exp2(m_run - m_new);
-                m_run = m_new;
-            }
-            const bool warp_need = __any_sync(0xffffffffu, need);
-            const float m_use = m_run == -INFINITY ? 0.0f : m_run;
-            const uint64_t negm = f2_pack(-m_use, -m_use);
-            uint64_t rs[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) rs[k] = f2_pack(0.0f, 0.0f);
-            uint32_t p2[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
-                                 sl2x2, negm),
-                          x0, x1);
-                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                rs[i & 3] = f2_add(rs[i & 3], f2_pack(p0, p1));   // four independent sums
-                p2[i] = pack_half2(p0, p1);
-                if (PS) {   // keep p for its low half
-                    s[2 * i] = __float_as_uint(p0);
-                    s[2 * i + 1] = __float_as_uint(p1);
-                }
-            }
-            float r0, r1, r2, r3, r4, r5, r6, r7;
-            f2_unpack(rs[0], r0, r1);
-            f2_unpack(rs[1], r2, r3);
-            f2_unpack(rs[2], r4, r5);
-            f2_unpack(rs[3], r6, r7);
-            l = l * alpha + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
-            // P_j over the first 64 columns of its S buffer; both threads of the
-            // row have loaded their S halves (they passed the exchange above).
-            tmem_st32(sbuf + half * 32, p2);
-            if (PS) {   // lo = RNE(p - hi); p - hi is exact in FP32
-                uint32_t lo2[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&p2[i]));
-                    lo2[i] = pack_half2(__uint_as_float(s[2 * i]) - h.x, __uint_as_float(s[2 * i + 1]) - h.y);
-                }
-                tmem_st32(sbuf + 64 + half * 32, lo2);
-            }
-            tmem_st_wait();
-            if (warp_need && j > 0) {   // rescale this thread's half of O after PV_{j-1}
-                ok = wait_warp(&ctrl->pv_done[(j - 1) % C::NSB], ((j - 1) / C::NSB) & 1, w);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-                for (int cc = 0; cc < D / 64; ++cc) {
-                    const uint32_t col = tl + C::T_O + half * (D / 2) + cc * 32;
-                    uint32_t o[32];
-                    tmem_ld32(col, o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float y0, y1;
-                        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), a2),
-                                  y0, y1);
-                        o[2 * e] = __float_as_uint(y0);
-                        o[2 * e + 1] = __float_as_uint(y1);
-                    }
-                    tmem_st32(col, o);
-                }
-                tmem_st_wait();
-            }
-            tc_fence_before();
-            mbar_arrive(&ctrl->p_full[buf]);
-        }
-        if (ok && n_tiles > 0) {
-            ok = wait_warp(&ctrl->pv_done[(n_tiles - 1) % C::NSB], ((n_tiles - 1) / C::NSB) & 1, w);
-            tc_fence_after();
-        }
-        if (ok) {   // combine the two partial row sums
-            ex->l[half][row] = l;
-            mbar_arrive(xbar);
-            ok = wait_warp(xbar, xphase, w);
-            if (ok) l += ex->l[half ^ 1][row];
-        }
-        if (ok) {
+            l += ex->l[half ^ 1][row];
+            // O out of tensor memory 32 columns at a time; once the last chunk is in
+            // registers the next item's first PV may overwrite O.
+            item_release(k);
             const bool row_ok = row_g < a.seq_q;
             const bool zero_row = (is_causal(MODE) && row_g >= a.q_real) || pad_row;
             const float inv_l = (l > 0.0f && !zero_row) ? (MODE == kCausalPaged ? a.out_mul : 1.0f) / l : 0.0f;
             const float lse2 = (l > 0.0f && !zero_row) ? m_run + __log2f(l) : -INFINITY;
             const bool partial = is_causal(MODE) && a.n_chunks > 1;
-            const long long orow = static_cast<long long>(bh) * a.seq_q + row_g;
+            const int qb = cur.bh / a.hq, qh = cur.bh - qb * a.hq;
+            const long long orow = static_cast<long long>(cur.bh) * a.seq_q + row_g;
 #pragma unroll 1
             for (int cc = 0; cc < D / 64; ++cc) {
-                const int c0 = half * (D / 2) + cc * 32;   // first output column of this chunk
                 uint32_t o[32];
                 if (n_tiles > 0) {
-                    tmem_ld32(tl + C::T_O + c0, o);
+                    tmem_ld32(tl + C::T_O + half * (D / 2) + cc * 32, o);
                     tmem_ld_wait();
+                    if (kPersist && cc == D / 64 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctrl->o_free);
+                    }
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
                 if (!row_ok) continue;
-                if (partial) {
-                    float4* dst = reinterpret_cast<float4*>(
-                        a.part_o + ((static_cast<long long>(chunk) * a.heads_q * a.seq_q + orow) * D + c0));
+                {
+                    const int c0 = half * (D / 2) + cc * 32;   // first output column of this chunk
+                    const uint32_t* oc32 = o;
+                    if (partial) {
+                        float4* dst = reinterpret_cast<float4*>(
+                            a.part_o + ((static_cast<long long>(cur.chunk) * a.heads_q * a.seq_q + orow) * D + c0));
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l,
-                                             __uint_as_float(o[4 * e + 1]) * inv_l,
-                                             __uint_as_float(o[4 * e + 2]) * inv_l,
-                                             __uint_as_float(o[4 * e + 3]) * inv_l);
-                } else {
-                    uint4* dst = reinterpret_cast<uint4*>(a.o + qb * a.o_sb + qh * a.o_sh +
-                                                          row_g * a.o_sr + c0);
-                    float y[32];
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(oc32[4 * e]) * inv_l,
+                                                 __uint_as_float(oc32[4 * e + 1]) * inv_l,
+                                                 __uint_as_float(oc32[4 * e + 2]) * inv_l,
+                                                 __uint_as_float(oc32[4 * e + 3]) * inv_l);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(a.o + qb * a.o_sb + qh * a.o_sh +
+                                                              row_g * a.o_sr + c0);
+                        float y[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) y[e] = __uint_as_float(o[e]) * inv_l;
-                    if (is_sparse(MODE) && a.coarse && row_g >= a.prefix && !pad_row) {
-                        // coarse branch: o += gate * o_coarse[cube of the row]
-                        const int cube = static_cast<int>((row_g - a.prefix) >> 6);
-                        const float4* oc = reinterpret_cast<const float4*>(
-                            a.coarse + (static_cast<long long>(bh) * a.n_cubes + cube) * D + c0);
-                        const uint4* gt = reinterpret_cast<const uint4*>(
-                            a.gate + (static_cast<long long>(bh) * a.seq_q + row_g) * D + c0);
+                        for (int e = 0; e < 32; ++e) y[e] = __uint_as_float(oc32[e]) * inv_l;
+                        if (is_sparse(MODE) && a.coarse && row_g >= a.prefix && !pad_row) {
+                            // coarse branch: o += gate * o_coarse[cube of the row]
+                            const int cube = static_cast<int>((row_g - a.prefix) >> 6);
+                            const float4* ocv = reinterpret_cast<const float4*>(
+                                a.coarse + (static_cast<long long>(cur.bh) * a.n_cubes + cube) * D + c0);
+                            const uint4* gt = reinterpret_cast<const uint4*>(
+                                a.gate + (static_cast<long long>(cur.bh) * a.seq_q + row_g) * D + c0);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint4 gw = gt[e];
-                            const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w};
-                            const float4 c0v = oc[2 * e], c1v = oc[2 * e + 1];
-                            const float cv[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
+                            for (int e = 0; e < 4; ++e) {
+                                const uint4 gw = gt[e];
+                                const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w};
+                                const float4 c0v = ocv[2 * e], c1v = ocv[2 * e + 1];
+                                const float cv[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
 #pragma unroll
-                            for (int f = 0; f < 4; ++f) {
-                                const float2 g2 = __half22float2(*reinterpret_cast<const __half2*>(&gv[f]));
-                                y[8 * e + 2 * f] = fmaf(g2.x, cv[2 * f], y[8 * e + 2 * f]);
-                                y[8 * e + 2 * f + 1] = fmaf(g2.y, cv[2 * f + 1], y[8 * e + 2 * f + 1]);
+                                for (int f = 0; f < 4; ++f) {
+                                    const float2 g2 = __half22float2(*reinterpret_cast<const __half2*>(&gv[f]));
+                                    y[8 * e + 2 * f] = fmaf(g2.x, cv[2 * f], y[8 * e + 2 * f]);
+                                    y[8 * e + 2 * f + 1] = fmaf(g2.y, cv[2 * f + 1], y[8 * e + 2 * f + 1]);
+                                }
                             }
                         }
-                    }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint32_t hw[4];
+                        for (int e = 0; e < 4; ++e) {
+                            uint32_t hw[4];
 #pragma unroll
-                        for (int f = 0; f < 4; ++f) hw[f] = pack_half2(y[8 * e + 2 * f], y[8 * e + 2 * f + 1]);
-                        dst[e] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            for (int f = 0; f < 4; ++f) hw[f] = pack_half2(y[8 * e + 2 * f], y[8 * e + 2 * f + 1]);
+                            dst[e] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        }
                     }
                 }
             }
             if (row_ok && half == 0) {
                 if (partial)
-                    a.part_lse[static_cast<long long>(chunk) * a.heads_q * a.seq_q + orow] = lse2;
+                    a.part_lse[static_cast<long long>(cur.chunk) * a.heads_q * a.seq_q + orow] = lse2;
                 else if (a.lse)
                     a.lse[orow] = lse2 * 0.69314718055994531f;
             }
@@ -1246,9 +1516,15 @@ int set_smem_attr() {
 
 template <int D, int MODE, bool PS = false>
 int launch_attn(const void* q, const void* k, const void* v, int seq_q, int seq_k, int heads_q,
-                const Strides& qs, const Strides& kvs, dim3 grid, AttnArgs args,
-                cudaStream_t stream, const CUtensorMap* mask_map = nullptr,
+                const Strides& qs, const Strides& kvs, long long n_items, int items_x,
+                AttnArgs args, cudaStream_t stream, const CUtensorMap* mask_map = nullptr,
                 const CUtensorMap* kv_maps = nullptr) {
+    // Persistent modes: one CTA per SM (never more than items); otherwise one CTA
+    // per item.  Item numbers and the counter's draws stay in int.
+    if (n_items <= 0 || n_items > 0x7FFFFFFFLL - args.nsm) return GBATTN_ERR_SHAPE;
+    args.n_items = static_cast<int>(n_items);
+    args.items_x = items_x;
+    const dim3 grid(static_cast<unsigned>(persistent(MODE) ? std::min<long long>(n_items, args.nsm) : n_items));
     // 4-D maps (D, S, heads, batch) with the callers' strides; boxes past a head's
     // last row read zeros and never cross into another head
     const int batch = heads_q / args.hq;
@@ -1283,6 +1559,7 @@ AttnArgs base_args(const DeviceState& dev, float scale) {
     a.scale_log2 = scale * 1.4426950408889634f;
     a.scale = scale;
     a.status = dev.status;
+    a.nsm = dev.num_sms > 0 ? dev.num_sms : 148;
     a.wait_limit = wait_limit_ns();
     a.group = 1;
     return a;
@@ -1382,8 +1659,9 @@ extern "C" int attn_dense_fwd(const void* q, const void* k, const void* v, void*
     a.o = static_cast<__half*>(o);
     set_out_strides(a, os);
     a.lse = lse;
-    dim3 grid((Sq + BM - 1) / BM, B * H);
-    return launch_attn<128, kDense>(q, k, v, Sq, Skv, B * H, qs, kvs, grid, a,
+    const int n_qt = (Sq + BM - 1) / BM;
+    return launch_attn<128, kDense>(q, k, v, Sq, Skv, B * H, qs, kvs,
+                                    static_cast<long long>(n_qt) * B * H, n_qt, a,
                                     static_cast<cudaStream_t>(stream));
 }
 
@@ -1438,10 +1716,10 @@ extern "C" int attn_dense_mask_fwd(const void* q, const void* k, const void* v, 
     CUtensorMap tm;
     if (encode_tmap_f16_mask(&tm, mask, Skv, Sq, hm, bm, sh, sb) != GBATTN_OK)
         return GBATTN_ERR_CUDA;
-    dim3 grid(B * H, (Sq + BM - 1) / BM);
     set_out_strides(a, dense_strides(H, Sq, D));
     return launch_attn<128, kMasked>(q, k, v, Sq, Skv, B * H, dense_strides(H, Sq, D),
-                                     dense_strides(H, Skv, D), grid, a,
+                                     dense_strides(H, Skv, D),
+                                     static_cast<long long>((Sq + BM - 1) / BM) * B * H, B * H, a,
                                      static_cast<cudaStream_t>(stream), &tm);
 }
 
@@ -1513,10 +1791,11 @@ extern "C" int attn_causal_prefill_fwd(const void* q, const void* k, const void*
         a.part_lse = a.part_o + static_cast<size_t>(chunks) * rows * D;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    dim3 grid(((Q_pad + BM - 1) / BM) * chunks, B * Hq);
+    const int ix = ((Q_pad + BM - 1) / BM) * chunks;
+    const long long ni = static_cast<long long>(ix) * B * Hq;
     rc = (flags & GBATTN_PROB_SPLIT)
-             ? launch_attn<256, kCausal, true>(q, k, v, Q_pad, KV, B * Hq, qs, kvs, grid, a, s)
-             : launch_attn<256, kCausal>(q, k, v, Q_pad, KV, B * Hq, qs, kvs, grid, a, s);
+             ? launch_attn<256, kCausal, true>(q, k, v, Q_pad, KV, B * Hq, qs, kvs, ni, ix, a, s)
+             : launch_attn<256, kCausal>(q, k, v, Q_pad, KV, B * Hq, qs, kvs, ni, ix, a, s);
     if (rc != GBATTN_OK || chunks == 1) return rc;
     const long long threads = rows * 32;
     attn_merge_kernel<256><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
@@ -1620,12 +1899,13 @@ extern "C" int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pag
         a.part_lse = a.part_o + static_cast<size_t>(chunks) * rows * D;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    dim3 grid(((Q_pad + BM - 1) / BM) * chunks, B * Hq);
+    const int ix = ((Q_pad + BM - 1) / BM) * chunks;
+    const long long ni = static_cast<long long>(ix) * B * Hq;
     rc = (flags & GBATTN_PROB_SPLIT)
              ? launch_attn<256, kCausalPaged, true>(q, nullptr, nullptr, Q_pad, KV, B * Hq, qs, qs,
-                                                    grid, a, s, nullptr, kv)
-             : launch_attn<256, kCausalPaged>(q, nullptr, nullptr, Q_pad, KV, B * Hq, qs, qs, grid,
-                                              a, s, nullptr, kv);
+                                                    ni, ix, a, s, nullptr, kv)
+             : launch_attn<256, kCausalPaged>(q, nullptr, nullptr, Q_pad, KV, B * Hq, qs, qs, ni,
+                                              ix, a, s, nullptr, kv);
     if (rc != GBATTN_OK || chunks == 1) return rc;
     const long long threads = rows * 32;
     attn_merge_kernel<256><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
@@ -1638,7 +1918,8 @@ extern "C" int attn_causal_prefill_paged_fwd(const void* q, const uint8_t* k_pag
 extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
                               const int32_t* pairs, int prefix, const int32_t* cube_valid,
                               const float* o_coarse, const void* gate, void* o, float* lse, int B,
-                              int H, int S, int D, int block, int topk, float scale, void* stream) {
+                              int H, int S, int D, int block, int topk, float scale,
+                              void* workspace, size_t workspace_bytes, void* stream) {
     CallRange nvtx_range("vsa_sparse_fwd");
     if (!q || !k || !v || !idx || !o || (!o_coarse) != (!gate)) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || S <= 0 || topk <= 0 || prefix < 0 || prefix >= S)
@@ -1653,9 +1934,10 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
         return GBATTN_ERR_ALIGN;
     if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
     if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace) ||
         (reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
         return GBATTN_ERR_ALIGN;
+    if (workspace && workspace_bytes < kSparseWorkspaceBytes) return GBATTN_ERR_WORKSPACE;
     const size_t xb = static_cast<size_t>(B) * H * S * D * 2;
     const size_t ib = static_cast<size_t>(B) * H * nc * topk * 4;
     const size_t lb = static_cast<size_t>(B) * H * S * 4;
@@ -1666,10 +1948,19 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
         overlaps(o, xb, o_coarse, cb) || overlaps(o, xb, gate, xb) || overlaps(lse, lb, o_coarse, cb) ||
         overlaps(lse, lb, gate, xb))
         return GBATTN_ERR_ALIAS;
+    const size_t wb = kSparseWorkspaceBytes, pb = static_cast<size_t>(B) * H * ((nc + 1) / 2) * 8;
+    const size_t vb = static_cast<size_t>(nc) * 4;   // cube_valid: one count per cube
+    if (workspace && (overlaps(workspace, wb, q, xb) || overlaps(workspace, wb, k, xb) ||
+                      overlaps(workspace, wb, v, xb) || overlaps(workspace, wb, o, xb) ||
+                      overlaps(workspace, wb, idx, ib) || overlaps(workspace, wb, lse, lb) ||
+                      overlaps(workspace, wb, pairs, pb) || overlaps(workspace, wb, cube_valid, vb) ||
+                      overlaps(workspace, wb, o_coarse, cb) || overlaps(workspace, wb, gate, xb)))
+        return GBATTN_ERR_ALIAS;
     DeviceState dev;
     int rc = current_device(&dev);
     if (rc != GBATTN_OK) return rc;
     AttnArgs a = base_args(dev, scale);
+    a.sched = static_cast<int*>(workspace);
     a.seq_q = S;
     a.seq_k = S;
     a.heads_q = B * H;
@@ -1686,12 +1977,17 @@ extern "C" int vsa_sparse_fwd(const void* q, const void* k, const void* v, const
     a.pairs = pairs;
     a.o = static_cast<__half*>(o);
     a.lse = lse;
-    dim3 grid(prefix / BM + (nc + 1) / 2, B * H);
+    const int ix = prefix / BM + (nc + 1) / 2;
+    const long long ni = static_cast<long long>(ix) * B * H;
     const Strides ds = dense_strides(H, S, D);
     set_out_strides(a, ds);
     if (prefix > 0 || cube_valid)
-        return launch_attn<128, kSparseFull>(q, k, v, S, S, B * H, ds, ds, grid, a,
+        return launch_attn<128, kSparseFull>(q, k, v, S, S, B * H, ds, ds, ni, ix, a,
                                              static_cast<cudaStream_t>(stream));
-    return launch_attn<128, kSparse>(q, k, v, S, S, B * H, ds, ds, grid, a,
+    return launch_attn<128, kSparse>(q, k, v, S, S, B * H, ds, ds, ni, ix, a,
                                      static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t vsa_sparse_workspace_size(void) {
+    return kSparseWorkspaceBytes;
 }

@@ -106,6 +106,32 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// wait_warp for a waiter with time to spare: it sleeps sleep_ns between polls,
+// so that it takes no issue slots from the warps on its SM sub-partition.
+__device__ __forceinline__ bool wait_warp_sleep(uint64_t* bar, uint32_t parity, const WaitCtl& w,
+                                                uint32_t sleep_ns) {
+    const uint32_t lane = threadIdx.x & 31u;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        bool ok = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        __nanosleep(sleep_ns);
+        int stop = 0;
+        if (lane == 0) {
+            uint64_t t = global_timer_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > w.limit_ns) {
+                atomicOr(w.status, kDevWaitTimeout);
+                *w.abort = 1;
+                stop = 1;
+            }
+            if (*w.abort) stop = 1;
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
+
 // One lane of a converged warp (elect.sync).  Issue tcgen05.mma / TMA from a
 // converged warp through one elected lane per group of instructions: a lone
 // diverged lane issuing them makes every later shared-memory wait of the warp

@@ -369,11 +369,23 @@ int vsa_select_blocks_noalloc(const void* q, const void* k, int B, int H, int S,
  *   the fine branch's).  Prefix tokens and padding slots are unchanged.
  *   block == 64, D == 128, prefix % 128 == 0, (S - prefix) % block == 0,
  *   1 <= topk <= min((S-prefix)/block, 512), prefix/128 + ceil(cubes/2) <= 512.
+ *   workspace: NULL, or vsa_sparse_workspace_size() bytes of device memory, 16-byte aligned,
+ *   overlapping no other argument, that hold zeros before the first call using them.  The
+ *   work items (query-cube pairs, prefix query tiles) are then handed to the GPU's persistent
+ *   CTAs by a counter in it, whichever CTA is free first, and every call leaves it at zero
+ *   again, an aborted one (GBATTN_DEV_WAIT_TIMEOUT) included.  Calls that may run at the
+ *   same time (two streams, concurrent graph launches) need separate workspaces.  NULL:
+ *   CTA c of the G persistent CTAs takes items c, c + G, c + 2G, ... (slower when the
+ *   items' key lists differ in length).  Too small: GBATTN_ERR_WORKSPACE.
  */
 int vsa_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
                    const int32_t* pairs, int prefix, const int32_t* cube_valid,
                    const float* o_coarse, const void* gate, void* o, float* lse, int B, int H,
-                   int S, int D, int block, int topk, float scale, void* stream);
+                   int S, int D, int block, int topk, float scale, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Bytes of vsa_sparse_fwd's optional workspace (16). */
+size_t vsa_sparse_workspace_size(void);
 
 /*
  * Pairs the video query cubes of every head for vsa_sparse_fwd, which runs two query cubes per

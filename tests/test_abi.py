@@ -226,22 +226,32 @@ def test_select_and_sparse_validation(lib):
     assert f(P, P2, 1, 24, 32768, 128, 64, 64, 0, None, P3, P4, ws, None) in (CUDA, OK)
     g = lib.vsa_sparse_fwd
     # q, k, v, idx, pairs, prefix, cube_valid, coarse, gate, o, lse, B, H, S, D, block, topk,
-    # scale, stream
+    # scale, workspace, workspace_bytes, stream
     I = ctypes.c_void_p(0x70000000)
     N = None
-    assert g(P, P2, P3, P4, N, 0, N, N, N, None, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == NULL
-    assert g(P, P2, P3, I, N, 0, N, N, N, P, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == ALIAS
-    assert g(P, P2, P3, I, N, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 600, 0.08, None) == SHAPE
-    assert g(P, P2, P3, I, N, 64, N, N, N, P4, None, 1, 24, 32768 + 64, 128, 64, 64, 0.08,
+    assert g(P, P2, P3, P4, N, 0, N, N, N, None, None, 1, 24, 32768, 128, 64, 64, 0.08, N, 0, None) == NULL
+    assert g(P, P2, P3, I, N, 0, N, N, N, P, None, 1, 24, 32768, 128, 64, 64, 0.08, N, 0, None) == ALIAS
+    assert g(P, P2, P3, I, N, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 600, 0.08, N, 0, None) == SHAPE
+    assert g(P, P2, P3, I, N, 64, N, N, N, P4, None, 1, 24, 32768 + 64, 128, 64, 64, 0.08, N, 0,
              None) == SHAPE                        # prefix must be whole 128-row query tiles
-    assert g(P, P2, P3, I, N, 128, MIS2, N, N, P4, None, 1, 24, 32768 + 128, 128, 64, 64, 0.08,
+    assert g(P, P2, P3, I, N, 128, MIS2, N, N, P4, None, 1, 24, 32768 + 128, 128, 64, 64, 0.08, N, 0,
              None) == ALIGN
-    assert g(P, P2, P3, I, MIS2, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, None) == ALIGN
+    assert g(P, P2, P3, I, MIS2, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, N, 0, None) == ALIGN
     C = ctypes.c_void_p(0x78000000)
-    assert g(P, P2, P3, I, N, 0, N, C, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08,
+    assert g(P, P2, P3, I, N, 0, N, C, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, N, 0,
              None) == NULL                         # coarse without a gate
-    assert g(P, P2, P3, I, N, 0, N, C, P4, P4, None, 1, 24, 32768, 128, 64, 64, 0.08,
+    assert g(P, P2, P3, I, N, 0, N, C, P4, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, N, 0,
              None) == ALIAS                        # output over the gate
+    W = ctypes.c_void_p(0x7C000000)
+    assert lib.vsa_sparse_workspace_size() == 16
+    assert g(P, P2, P3, I, N, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, W, 15,
+             None) == WORKSPACE                    # too small a counter
+    assert g(P, P2, P3, I, N, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08,
+             ctypes.c_void_p(0x7C000004), 16, None) == ALIGN
+    assert g(P, P2, P3, I, N, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, P4, 16,
+             None) == ALIAS                        # counter inside the output
+    assert g(P, P2, P3, I, N, 0, N, N, N, P4, None, 1, 24, 32768, 128, 64, 64, 0.08, I, 16,
+             None) == ALIAS                        # counter inside idx
     c = lib.vsa_select_blocks_coarse
     ws = lib.vsa_select_coarse_workspace_size(1, 24, 32768, 128, 64)
     assert ws == lib.vsa_select_workspace_size(1, 24, 32768, 128, 64) + 24 * 512 * 128 * 4
