@@ -50,7 +50,8 @@ _SIGNATURES = {
     "vsa_select_coarse_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "vsa_select_blocks_coarse": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _f, _vp, _vp,
                                       _vp, _sz, _vp]),
-    "vsa_pair_query_cubes": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
+    "vsa_pair_workspace_size": (_sz, [_i, _i, _i]),
+    "vsa_pair_query_cubes": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
 }
 
 PROB_SPLIT = 1          # flags of the causal prefill calls (GBATTN_PROB_SPLIT)
@@ -420,16 +421,22 @@ def vsa_select_blocks_coarse(q, k, v, topk, block=64, prefix=0, cube_valid=None,
     return idx, coarse
 
 
-def vsa_pair_query_cubes(idx, pairs=None, stream=None):
+def vsa_pair_query_cubes(idx, pairs=None, workspace=None, stream=None):
     """Query-cube pairs for vsa_sparse_fwd.  idx int32 [B,H,cubes,topk] ->
-    pairs int32 [B,H,ceil(cubes/2),2] (second entry -1 for a lone cube)."""
+    pairs int32 [B,H,ceil(cubes/2),2] (second entry -1 for a lone cube), greedy by selection
+    overlap, longest union first.  workspace: vsa_pair_workspace_size bytes (allocated here
+    when None)."""
     import torch
     _need(idx, "idx", torch.int32, 4)
     B, H, nc, topk = idx.shape
     if pairs is None:
         pairs = torch.empty((B, H, (nc + 1) // 2, 2), dtype=torch.int32, device=idx.device)
     _need(pairs, "pairs", torch.int32)
-    rc = load().vsa_pair_query_cubes(_ptr(idx), B, H, nc, topk, _ptr(pairs), _stream(stream))
+    if workspace is None:
+        workspace = torch.empty(int(load().vsa_pair_workspace_size(B, H, nc)), dtype=torch.uint8,
+                                device=idx.device)
+    rc = load().vsa_pair_query_cubes(_ptr(idx), B, H, nc, topk, _ptr(pairs), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
     _check("vsa_pair_query_cubes", rc)
     return pairs
 

@@ -976,37 +976,76 @@ extern "C" int vsa_select_blocks_coarse(const void* q, const void* k, const void
 
 // ------------------------------------------------------------------ query-cube pairing
 //
-// The sparse attention kernel processes two query cubes per CTA over the union
+// The sparse attention kernel processes two query cubes per item over the union
 // of their selected key cubes; every key cube only one of the two selected is
-// wasted work for the other.  Pairing cubes whose selections overlap most
-// cuts that waste.  One CTA per head:
-//   1. each cube's selection as a bitset over key cubes;
-//   2. the overlap of every cube with the cubes up to kPairWindow index
-//      positions away (neighbours in the cube grid are close in cube index);
-//   3. kPairRounds rounds of "mutual best": every unpaired cube picks its
-//      unpaired window partner of largest overlap (ties to the lower index);
-//      two cubes that pick each other are paired;
-//   4. the cubes still unpaired are paired in index order.
-// The pairs are written in order of their first cube.  Any pairing gives the
-// same attention result (up to summation order); this one only saves work.
+// wasted work for the other.  The pairing is the greedy one: the pair of
+// largest selection overlap first (ties: the lower cube indices), then the
+// largest among the cubes left, and so on.  Three kernels compute it:
+//   vsa_pair_bits_kernel (a warp per cube): every cube's selection as a bitset
+//     over key cubes, into the workspace;
+//   vsa_pair_cand_kernel (a warp per four cubes): every cube's kPairCand (32)
+//     best partners over all cubes of the head, by overlap then index, into the
+//     workspace;
+//   vsa_pair_kernel (a CTA per head): rounds of "mutual best": each unpaired
+//     cube takes the first unpaired cube of its list, and two cubes that take
+//     each other pair up.  Such a pair is the heaviest one left at both its
+//     cubes, so the greedy order pairs it too.  A cube whose list has run out
+//     waits for the second phase: rounds of mutual best over all cubes still
+//     unpaired (full overlap scans), which complete the greedy pairing.  A
+//     lone cube of an odd count stays alone.
+// The pairs are written longest union first (ties: lower first cube): the
+// persistent sparse kernel hands its items out in this order, so the long
+// ones do not end the launch.  Any pairing gives the same attention result
+// (up to summation order); this one only saves work.
 namespace gbattn {
 namespace {
-constexpr int kPairThreads = 1024;   // one thread per cube
-constexpr int kPairWindow = 32;
-constexpr int kPairRounds = 4;
+constexpr int kPairThreads = 1024;   // vsa_pair_kernel: one thread per cube
 constexpr int kPairMaxCubes = 1024;
 constexpr int kPairMaxWords = kPairMaxCubes / 32;
+constexpr int kPairCand = 32;        // candidates kept per cube (one per lane)
+constexpr int kCandThreads = 128;    // vsa_pair_cand_kernel: four warps
 
-size_t pair_smem_bytes(int nc) {
-    const int words = (nc + 31) / 32;
-    return static_cast<size_t>(nc) * words * 4 + static_cast<size_t>(nc) * kPairWindow +
-           static_cast<size_t>(nc) * 2 * 3 + 64 * 4;
+__host__ __device__ inline int pair_words(int nc) { return (nc + 31) / 32; }
+// selection bitsets padded to whole 16-byte rows (vector loads)
+__host__ __device__ inline int pair_row_words(int nc) { return (pair_words(nc) + 3) & ~3; }
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+// Cubes per warp of vsa_pair_cand_kernel: four when a lane's share of the
+// partners (one in 32) fits 16 registers per cube, else two.
+inline int cand_cubes_per_warp(int nc) { return nc <= 512 ? 4 : 2; }
+
+size_t cand_smem_bytes(int nc) {
+    return static_cast<size_t>(nc) * pair_row_words(nc) * 4 + kCandThreads * 4;
+}
+
+// vsa_pair_kernel's shared memory: bitset rows, candidate lists, then int16
+// arrays (partner, best, list, first cube of each pair) and the pairs' tiles.
+__host__ __device__ inline size_t pair_lists_offset(int nc) {
+    return static_cast<size_t>(nc) * pair_row_words(nc) * 4;
+}
+__host__ __device__ inline size_t pair_arrays_offset(int nc) {
+    return pair_lists_offset(nc) + static_cast<size_t>(nc) * kPairCand * 2;
+}
+__host__ __device__ inline size_t pair_tiles_offset(int nc) {
+    return pair_arrays_offset(nc) + align16(static_cast<size_t>(nc) * 2 * 4);
+}
+size_t pair_smem_bytes(int nc) { return pair_tiles_offset(nc) + align16(static_cast<size_t>(nc + 8) * 2); }
+
+// Workspace: the bitset rows, then the candidate lists.
+size_t pair_bits_bytes(int B, int H, int nc) {
+    return static_cast<size_t>(B) * H * nc * pair_row_words(nc) * 4;
+}
+
+// Candidate key: overlap in the high half, then the lower index first.
+__device__ __forceinline__ uint32_t cand_key(int overlap, int b) {
+    return (static_cast<uint32_t>(overlap) << 16) | static_cast<uint32_t>(0xFFFF - b);
 }
 
 // Exclusive prefix sum of v over the block (one value per thread); returns the
 // total through *total.
 __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n_warps = static_cast<int>(blockDim.x) >> 5;
     int x = v;
 #pragma unroll
     for (int sh = 1; sh < 32; sh <<= 1) {
@@ -1016,7 +1055,7 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
     if (lane == 31) warp_tot[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int t = lane < kPairThreads / 32 ? warp_tot[lane] : 0;
+        int t = lane < n_warps ? warp_tot[lane] : 0;
 #pragma unroll
         for (int sh = 1; sh < 32; sh <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, t, sh);
@@ -1026,128 +1065,361 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
     }
     __syncthreads();
     const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
-    *total = warp_tot[kPairThreads / 32 - 1];
+    *total = warp_tot[n_warps - 1];
     __syncthreads();
     return before;
 }
 
-__global__ void __launch_bounds__(kPairThreads) vsa_pair_kernel(const int32_t* __restrict__ idx,
-                                                                int nc, int topk,
+// Every cube's selection as a bitset over key cubes (one warp per cube): lane i
+// takes entries i, i + 32, ...; each word of the row is the OR over the lanes of
+// the bits that fall in it, and lane w stores word w.  Entries out of range are
+// skipped.  Rows are row_words long (whole 16-byte units).
+__global__ void __launch_bounds__(256) vsa_pair_bits_kernel(const int32_t* __restrict__ idx,
+                                                            long long rows, int nc, int topk,
+                                                            uint32_t* __restrict__ bits) {
+    const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;   // warp-uniform
+    const int rw = pair_row_words(nc);
+    const int32_t* sel = idx + r * topk;
+    uint32_t mine = 0u;   // word `lane` of the row
+    for (int base = 0; base < topk; base += 32) {
+        const int kc = base + lane < topk ? sel[base + lane] : -1;
+        const bool ok = kc >= 0 && kc < nc;
+        const int w = ok ? (kc >> 5) : -1;
+        const uint32_t bit = ok ? 1u << (kc & 31) : 0u;
+        for (int ww = 0; ww < rw; ++ww) {
+            const uint32_t v = __reduce_or_sync(0xffffffffu, w == ww ? bit : 0u);
+            if (lane == ww) mine |= v;
+        }
+    }
+    if (lane < rw) bits[r * rw + lane] = mine;
+}
+
+// 16-byte chunk q and word w of bitset row b (rows of rw words).
+__device__ __forceinline__ uint4 row_chunk(const uint32_t* bits, int rw, int b, int q) {
+    return reinterpret_cast<const uint4*>(bits + b * rw)[q];
+}
+__device__ __forceinline__ uint32_t row_word(const uint32_t* bits, int rw, int b, int w) {
+    return bits[b * rw + w];
+}
+
+// Copy a head's bitset rows (nc rows of row_words words) into shared memory.
+__device__ void load_rows(const uint32_t* __restrict__ src, int nc, int rw, uint32_t* dst) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (int i = threadIdx.x; i < nc * (rw >> 2); i += blockDim.x) d4[i] = s4[i];
+    __syncthreads();
+}
+
+__device__ __forceinline__ int popc_and4(uint4 x, uint4 y) {
+    return __popc(x.x & y.x) + __popc(x.y & y.y) + __popc(x.z & y.z) + __popc(x.w & y.w);
+}
+
+// Each warp takes CPW cubes a; lane l holds the overlaps of those cubes with the
+// partners b = l + 32 i (i < CPL), each partner row read once for all CPW cubes.
+// A cube's kPairCand best partners (overlap, then the lower index) come from a
+// bitwise search for the overlap threshold tau (the largest value that at least
+// kPairCand partners reach), every partner above tau, the lowest-index partners
+// at tau, and a 32-lane bitonic sort of their keys.
+template <int CPL, int CPW>
+__global__ void __launch_bounds__(kCandThreads) vsa_pair_cand_kernel(const uint32_t* __restrict__ gbits,
+                                                                     int nc, int top_bit,
+                                                                     int16_t* __restrict__ cand) {
+    extern __shared__ uint32_t csm[];
+    const int rw = pair_row_words(nc);
+    uint32_t* bits = csm;                                   // [nc][rw]
+    uint32_t* stage = csm + static_cast<size_t>(nc) * rw;   // [warps][32] keys
+    const long long bh = blockIdx.y;
+    load_rows(gbits + bh * nc * static_cast<long long>(rw), nc, rw, bits);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int a0 = (static_cast<int>(blockIdx.x) * (kCandThreads / 32) + warp) * CPW;
+    if (a0 >= nc) return;   // warp-uniform; no block barrier follows
+    int acc[CPW][CPL];
+#pragma unroll
+    for (int c = 0; c < CPW; ++c)
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) acc[c][i] = 0;
+    for (int q = 0; q < (rw >> 2); ++q) {
+        uint4 A[CPW];
+#pragma unroll
+        for (int c = 0; c < CPW; ++c)
+            A[c] = a0 + c < nc ? row_chunk(bits, rw, a0 + c, q) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            const int b = lane + 32 * i;
+            if (b < nc) {
+                const uint4 Bv = row_chunk(bits, rw, b, q);
+#pragma unroll
+                for (int c = 0; c < CPW; ++c) acc[c][i] += popc_and4(A[c], Bv);
+            }
+        }
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t* st = stage + warp * 32;
+    const int want = min(kPairCand, nc - 1);
+#pragma unroll
+    for (int c = 0; c < CPW; ++c) {
+        const int a = a0 + c;
+        if (a >= nc) break;   // warp-uniform
+        // -1 marks no partner (past the end, or the cube itself)
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            const int b = lane + 32 * i;
+            if (b >= nc || b == a) acc[c][i] = -1;
+        }
+        int tau = 0;
+        for (int bit = top_bit; bit >= 0; --bit) {   // overlaps are at most topk < 2^(top_bit+1)
+            const int trial = tau | (1 << bit);
+            int n = 0;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) n += acc[c][i] >= trial;
+            if (static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(n))) >= want) tau = trial;
+        }
+        int need = want;   // partners at tau still to take
+        {
+            int above = 0;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) above += acc[c][i] > tau;
+            need -= static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(above)));
+        }
+        int slot = 0;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {   // index order: i, then lane
+            const int v = acc[c][i];
+            const unsigned meq = __ballot_sync(0xffffffffu, v == tau);
+            const bool take = v > tau || (v == tau && __popc(meq & lt) < need);
+            need -= min(need, __popc(meq));
+            const unsigned mt = __ballot_sync(0xffffffffu, take);
+            const int at = slot + __popc(mt & lt);   // below want by the choice of tau
+            if (take && at < 32) st[at] = cand_key(v, lane + 32 * i);
+            slot += __popc(mt);
+        }
+        __syncwarp();
+        uint32_t k = lane < want ? st[lane] : 0u;
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                const uint32_t o = __shfl_xor_sync(0xffffffffu, k, stride);
+                k = (((lane & stride) == 0) == ((lane & size) == 0)) ? max(k, o) : min(k, o);
+            }
+        cand[(bh * nc + a) * kPairCand + lane] =
+            static_cast<int16_t>(k == 0u ? -1 : 0xFFFF - static_cast<int>(k & 0xFFFFu));
+        __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(kPairThreads) vsa_pair_kernel(const uint32_t* __restrict__ gbits,
+                                                                const int16_t* __restrict__ cand,
+                                                                int nc,
                                                                 int32_t* __restrict__ pairs) {
     extern __shared__ uint32_t psm[];
     __shared__ int warp_tot[32];
-    const int words = (nc + 31) / 32;
-    uint32_t* bits = psm;                                            // [words][nc] (transposed)
-    uint8_t* ov = reinterpret_cast<uint8_t*>(bits + static_cast<size_t>(nc) * words);  // [W][nc]
-    int16_t* partner = reinterpret_cast<int16_t*>(ov + static_cast<size_t>(nc) * kPairWindow);
+    const int words = pair_row_words(nc);
+    uint8_t* base = reinterpret_cast<uint8_t*>(psm);
+    uint32_t* bits = psm;                                                         // [nc][words]
+    int16_t* cl = reinterpret_cast<int16_t*>(base + pair_lists_offset(nc));       // [nc][kPairCand]
+    int16_t* partner = reinterpret_cast<int16_t*>(base + pair_arrays_offset(nc));
     int16_t* best = partner + nc;
     int16_t* list = best + nc;
+    int16_t* p_first = list + nc;
+    int16_t* p_tiles = reinterpret_cast<int16_t*>(base + pair_tiles_offset(nc));  // 16-byte aligned
     const long long bh = blockIdx.x;
-    const int32_t* sel = idx + bh * nc * static_cast<long long>(topk);
     const int a = threadIdx.x;
+    const int lane = a & 31, warp = a >> 5;
     const bool live = a < nc;
-
-    for (int i = a; i < nc * words; i += kPairThreads) bits[i] = 0u;
+    load_rows(gbits + bh * nc * static_cast<long long>(words), nc, words, bits);
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(cand + bh * nc * kPairCand);
+        uint4* dst = reinterpret_cast<uint4*>(cl);
+        for (int i = a; i < nc * kPairCand / 8; i += kPairThreads) dst[i] = src[i];
+    }
     if (live) partner[a] = -1;
+    for (int i = a; i < nc + 8; i += kPairThreads) p_tiles[i] = -1;
     __syncthreads();
-    for (int e = a; e < nc * topk; e += kPairThreads) {
-        const int c = e / topk;
-        const int kc = sel[e];
-        if (kc >= 0 && kc < nc) atomicOr(&bits[(kc >> 5) * nc + c], 1u << (kc & 31));
-    }
-    __syncthreads();
-    // overlap of a and a + d (d = 1..W) at ov[(d - 1) * nc + a]
-    if (live) {
-        uint32_t mine[kPairMaxWords];
-#pragma unroll
-        for (int w = 0; w < kPairMaxWords; ++w) mine[w] = w < words ? bits[w * nc + a] : 0u;
-        for (int d = 1; d <= kPairWindow; ++d) {
-            const int b = a + d;
-            int n = 0;
-            if (b < nc) {
-#pragma unroll
-                for (int w = 0; w < kPairMaxWords; ++w)
-                    if (w < words) n += __popc(mine[w] & bits[w * nc + b]);
-            }
-            ov[(d - 1) * nc + a] = static_cast<uint8_t>(n > 255 ? 255 : n);
-        }
-    }
-    __syncthreads();
-    for (int r = 0; r < kPairRounds; ++r) {
+    // phase 1: mutual best over the candidate lists (each round pairs at least one
+    // pair or ends the phase); a list is read eight entries at a time, the eight
+    // partner lookups together
+    for (int r = 0; r < nc; ++r) {
         int bb = -1;
         if (live && partner[a] < 0) {
-            int bw = -1;
-            for (int d = kPairWindow; d >= 1; --d) {      // b = a - d, ascending b
-                const int b = a - d;
-                if (b < 0 || partner[b] >= 0) continue;
-                const int w = ov[(d - 1) * nc + b];
-                if (w > bw) { bw = w; bb = b; }
-            }
-            for (int d = 1; d <= kPairWindow; ++d) {      // b = a + d, ascending b
-                const int b = a + d;
-                if (b >= nc) break;
-                if (partner[b] >= 0) continue;
-                const int w = ov[(d - 1) * nc + a];
-                if (w > bw) { bw = w; bb = b; }
+            const uint4* L = reinterpret_cast<const uint4*>(cl + a * kPairCand);
+            for (int q = 0; q < kPairCand / 8 && bb < 0; ++q) {
+                const uint4 v = L[q];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                int c8[8], p8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) c8[e] = static_cast<int16_t>((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) p8[e] = (c8[e] >= 0 && c8[e] < nc) ? partner[c8[e]] : 0;
+                bool end = false;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (bb >= 0 || end) continue;
+                    if (c8[e] < 0 || c8[e] >= nc) end = true;
+                    else if (p8[e] < 0) bb = c8[e];
+                }
+                if (end) break;
             }
         }
         if (live) best[a] = static_cast<int16_t>(bb);
         __syncthreads();
-        if (live && partner[a] < 0 && bb >= 0 && best[bb] == a) partner[a] = static_cast<int16_t>(bb);
+        const bool pair_now = live && partner[a] < 0 && bb >= 0 && best[bb] == a;
+        if (pair_now) partner[a] = static_cast<int16_t>(bb);
+        if (!__syncthreads_or(pair_now)) break;
+    }
+    // phase 2: mutual best over all cubes still unpaired (the heaviest pair left
+    // is always mutual, so each round pairs at least one pair); a warp scans the
+    // partners of one unpaired cube at a time, a lane every 32nd of them
+    for (int r = 0; r < nc; ++r) {
+        int n_left = 0;
+        const bool left = live && partner[a] < 0;
+        const int lr = block_exclusive_scan(left ? 1 : 0, warp_tot, &n_left);
+        if (left) list[lr] = static_cast<int16_t>(a);
+        __syncthreads();
+        if (n_left < 2) break;
+        for (int li = warp; li < n_left; li += kPairThreads / 32) {
+            const int me = list[li];
+            uint32_t bk = 0u;
+            int bb = -1;
+            for (int j = lane; j < n_left; j += 32) {
+                const int b = list[j];
+                if (b == me) continue;
+                int n = 0;
+                for (int q = 0; q < (words >> 2); ++q)
+                    n += popc_and4(row_chunk(bits, words, me, q), row_chunk(bits, words, b, q));
+                const uint32_t k = cand_key(n, b);
+                if (k > bk) {
+                    bk = k;
+                    bb = b;
+                }
+            }
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+            const unsigned who = __ballot_sync(0xffffffffu, mk != 0u && bk == mk);
+            const int win = who ? __shfl_sync(0xffffffffu, bb, __ffs(who) - 1) : -1;
+            if (lane == 0) best[me] = static_cast<int16_t>(win);
+        }
+        __syncthreads();
+        const int me = a < n_left ? list[a] : -1;
+        const int bb = me >= 0 ? best[me] : -1;
+        const bool pair_now = me >= 0 && bb >= 0 && best[bb] == me;
+        if (pair_now) partner[me] = static_cast<int16_t>(bb);
+        if (!__syncthreads_or(pair_now)) break;
+    }
+    // (phase 2 leaves at most one cube; should any more be left, they pair up in
+    // index order, so that the output is always a pairing)
+    {
+        int n_left = 0;
+        const bool left = live && partner[a] < 0;
+        const int lr = block_exclusive_scan(left ? 1 : 0, warp_tot, &n_left);
+        if (left) list[lr] = static_cast<int16_t>(a);
+        __syncthreads();
+        if (left && (lr & 1) == 0 && lr + 1 < n_left) {
+            const int b = list[lr + 1];
+            partner[a] = static_cast<int16_t>(b);
+            partner[b] = static_cast<int16_t>(a);
+        }
         __syncthreads();
     }
-    // the cubes still unpaired pair up in index order
-    int n_left = 0;
-    const bool left = live && partner[a] < 0;
-    const int lr = block_exclusive_scan(left ? 1 : 0, warp_tot, &n_left);
-    if (left) list[lr] = static_cast<int16_t>(a);
-    __syncthreads();
-    if (left && (lr & 1) == 0 && lr + 1 < n_left) {
-        const int b = list[lr + 1];
-        partner[a] = static_cast<int16_t>(b);
-        partner[b] = static_cast<int16_t>(a);
-    }
-    __syncthreads();
-    // pairs in order of their first cube
+    // every pair once (by its lower cube; a lone cube by itself) with its union's tiles
     const int pb = live ? partner[a] : 0;
     const bool first = live && (pb > a || pb < 0);
-    int n_out = 0;
-    const int p = block_exclusive_scan(first ? 1 : 0, warp_tot, &n_out);
+    int n_pairs = 0;
+    const int slot = block_exclusive_scan(first ? 1 : 0, warp_tot, &n_pairs);
+    int tiles = 0;
     if (first) {
-        int32_t* out = pairs + (bh * static_cast<long long>((nc + 1) / 2) + p) * 2;
-        out[0] = a;
-        out[1] = pb > a ? pb : -1;
+        int u = 0;
+        for (int w = 0; w < words; ++w)
+            u += __popc(row_word(bits, words, a, w) | (pb >= 0 ? row_word(bits, words, pb, w) : 0u));
+        tiles = (u + 1) / 2;
+        p_first[slot] = static_cast<int16_t>(a);
+        p_tiles[slot] = static_cast<int16_t>(tiles);
+    }
+    __syncthreads();
+    // rank: more tiles first, then the lower first cube (slots are in cube order);
+    // the padding past the last pair holds -1
+    if (first) {
+        int rank = 0;
+        const uint4* t8 = reinterpret_cast<const uint4*>(p_tiles);
+        for (int j8 = 0; j8 < (n_pairs + 7) / 8; ++j8) {
+            const uint4 v = t8[j8];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int tj = static_cast<int16_t>((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+                const int j = j8 * 8 + e;
+                rank += (tj > tiles) || (tj == tiles && j < slot);
+            }
+        }
+        if (rank < (nc + 1) / 2) {   // always true for a pairing
+            int32_t* out = pairs + (bh * static_cast<long long>((nc + 1) / 2) + rank) * 2;
+            out[0] = a;
+            out[1] = pb > a ? pb : -1;
+        }
     }
 }
 
 }  // namespace
 }  // namespace gbattn
 
+using namespace gbattn;
+
+extern "C" size_t vsa_pair_workspace_size(int B, int H, int n_cubes) {
+    if (B <= 0 || H <= 0 || n_cubes <= 0) return 0;
+    return pair_bits_bytes(B, H, n_cubes) +
+           ((static_cast<size_t>(B) * H * n_cubes * kPairCand * 2 + 15) & ~static_cast<size_t>(15));
+}
+
 extern "C" int vsa_pair_query_cubes(const int32_t* idx, int B, int H, int n_cubes, int topk,
-                                    int32_t* pairs, void* stream) {
+                                    int32_t* pairs, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
     CallRange nvtx_range("vsa_pair_query_cubes");
     if (!idx || !pairs) return GBATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || n_cubes <= 0 || topk <= 0 || topk > n_cubes) return GBATTN_ERR_SHAPE;
-    if (n_cubes > kPairMaxCubes || static_cast<long long>(B) * H > 0x7FFFFFFFLL)
-        return GBATTN_ERR_SHAPE;
-    if ((reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(pairs) & 3u))
+    if (n_cubes > kPairMaxCubes || static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(pairs) & 3u) ||
+        !aligned16(workspace))
         return GBATTN_ERR_ALIGN;
+    const size_t wb = vsa_pair_workspace_size(B, H, n_cubes);
+    if (!workspace || workspace_bytes < wb) return GBATTN_ERR_WORKSPACE;
     const size_t ib = static_cast<size_t>(B) * H * n_cubes * topk * 4;
     const size_t pb = static_cast<size_t>(B) * H * ((n_cubes + 1) / 2) * 2 * 4;
-    if (overlaps(pairs, pb, idx, ib)) return GBATTN_ERR_ALIAS;
+    if (overlaps(pairs, pb, idx, ib) || overlaps(workspace, wb, idx, ib) ||
+        overlaps(workspace, wb, pairs, pb))
+        return GBATTN_ERR_ALIAS;
     DeviceState dev;
     int rc = current_device(&dev);
     if (rc != GBATTN_OK) return rc;
-    const size_t smem = pair_smem_bytes(n_cubes);
     static std::once_flag once[64];
     if (dev.device >= 0 && dev.device < 64)
         std::call_once(once[dev.device], [] {
+            cudaFuncSetAttribute(vsa_pair_cand_kernel<16, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(cand_smem_bytes(kPairMaxCubes)));
+            cudaFuncSetAttribute(vsa_pair_cand_kernel<32, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(cand_smem_bytes(kPairMaxCubes)));
             cudaFuncSetAttribute(vsa_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(pair_smem_bytes(kPairMaxCubes)));
         });
-    vsa_pair_kernel<<<static_cast<unsigned>(static_cast<long long>(B) * H), kPairThreads, smem,
-                      static_cast<cudaStream_t>(stream)>>>(idx, n_cubes, topk, pairs);
-    count_launches(1);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* gbits = static_cast<uint32_t*>(workspace);
+    int16_t* cand = reinterpret_cast<int16_t*>(static_cast<uint8_t*>(workspace) +
+                                               pair_bits_bytes(B, H, n_cubes));
+    const long long rows = static_cast<long long>(B) * H * n_cubes;
+    vsa_pair_bits_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(
+        idx, rows, n_cubes, topk, gbits);
+    const int cpw = cand_cubes_per_warp(n_cubes);
+    const int per_cta = (kCandThreads / 32) * cpw;
+    const dim3 cgrid((n_cubes + per_cta - 1) / per_cta, static_cast<unsigned>(B * H));
+    int top_bit = 0;   // the highest bit an overlap (at most topk) can have
+    while ((2 << top_bit) <= topk) ++top_bit;
+    if (cpw == 4)
+        vsa_pair_cand_kernel<16, 4><<<cgrid, kCandThreads, cand_smem_bytes(n_cubes), s>>>(gbits, n_cubes, top_bit, cand);
+    else
+        vsa_pair_cand_kernel<32, 2><<<cgrid, kCandThreads, cand_smem_bytes(n_cubes), s>>>(gbits, n_cubes, top_bit, cand);
+    vsa_pair_kernel<<<static_cast<unsigned>(B * H), kPairThreads, pair_smem_bytes(n_cubes), s>>>(
+        gbits, cand, n_cubes, pairs);
+    count_launches(3);
     return launch_status();
 }
 

@@ -110,6 +110,10 @@ class Workload:
                                      device=dev)
             ws = gb.vsa_select_workspace_size(w["B"], w["H"], S, w["D"], 64)
             self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+            self.pair_ws = torch.empty(gb.load().vsa_pair_workspace_size(w["B"], w["H"], nc),
+                                       dtype=torch.uint8, device=dev)
+            self.counter = torch.zeros(gb.load().vsa_sparse_workspace_size(), dtype=torch.uint8,
+                                       device=dev)
             self.o = torch.empty_like(self.q)
             self.flops = vsa_flops(w["B"], w["H"], S, w["D"], w["topk"])
         elif w["kind"] == "paged":
@@ -137,10 +141,11 @@ class Workload:
                      lambda: gb.vsa_select_blocks(self.q, self.k, w["topk"], idx=self.idx,
                                                   workspace=self.ws)),
                     ("vsa_pair_query_cubes",
-                     lambda: gb.vsa_pair_query_cubes(self.idx, pairs=self.pairs)),
+                     lambda: gb.vsa_pair_query_cubes(self.idx, pairs=self.pairs,
+                                                     workspace=self.pair_ws)),
                     ("vsa_sparse_fwd",
                      lambda: gb.vsa_sparse_fwd(self.q, self.k, self.v, self.idx, pairs=self.pairs,
-                                               o=self.o))]
+                                               o=self.o, workspace=self.counter))]
         return [("e4m3_paged_to_fp16",
                  lambda: gb.e4m3_paged_to_fp16(self.kp, self.vp, self.table, w["KV"], w["k_scale"],
                                                w["v_scale"], k_out=self.kf, v_out=self.vf)),

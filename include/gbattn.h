@@ -396,12 +396,18 @@ size_t vsa_sparse_workspace_size(void);
  *   idx   : int32 [B][H][n_cubes][topk] from vsa_select_blocks.
  *   pairs : int32 [B][H][ceil(n_cubes/2)][2], every cube exactly once; the second entry of a
  *           pair is -1 for the one unpaired cube of an odd count.
- *   Each head: overlaps of every cube with the cubes up to 32 index positions away, 4 rounds of
- *   mutual best partners (ties to the lower index), the rest paired in index order; pairs are
- *   listed by their first cube.  n_cubes <= 1024.
+ *   workspace: vsa_pair_workspace_size(B, H, n_cubes) bytes of device memory, 16-byte aligned,
+ *           overlapping neither idx nor pairs (each cube's selection as a bitset and its 32 best
+ *           partners); its contents need no initial value.  NULL or smaller: GBATTN_ERR_WORKSPACE.
+ *   Each head is paired greedily: the two cubes whose selections share the most key cubes first
+ *   (ties: the lower cube indices), then the most overlapping two of the cubes left, and so on;
+ *   a lone cube of an odd count stays alone.  The pairs are listed longest union first (ties:
+ *   the lower first cube), the order in which the sparse kernel hands out its items.
+ *   n_cubes <= 1024, B * H <= 65535.  Three kernel launches.
  */
+size_t vsa_pair_workspace_size(int B, int H, int n_cubes);
 int vsa_pair_query_cubes(const int32_t* idx, int B, int H, int n_cubes, int topk, int32_t* pairs,
-                         void* stream);
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

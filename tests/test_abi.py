@@ -260,11 +260,17 @@ def test_select_and_sparse_validation(lib):
     assert c(P, P2, I, 1, 24, 32768, 128, 64, 64, 0, N, 0.08, P3, C, P4, ws - 1, None) == WORKSPACE
     assert c(P, P2, I, 1, 24, 32768, 128, 64, 64, 0, N, 0.08, P3, P, P4, ws, None) == ALIAS
     h = lib.vsa_pair_query_cubes
-    assert h(None, 1, 24, 512, 64, P4, None) == NULL
-    assert h(I, 1, 24, 2048, 64, P4, None) == SHAPE     # more cubes than the pairing takes
-    assert h(I, 1, 24, 512, 600, P4, None) == SHAPE
-    assert h(I, 1, 24, 512, 64, I, None) == ALIAS
-    assert h(I, 1, 24, 512, 64, P4, None) in (CUDA, OK)
+    pw = lib.vsa_pair_workspace_size(1, 24, 512)
+    assert pw == 24 * 512 * 16 * 4 + 24 * 512 * 32 * 2  # bitset rows, 32 int16 candidates per cube
+    assert h(None, 1, 24, 512, 64, P4, W, pw, None) == NULL
+    assert h(I, 1, 24, 2048, 64, P4, W, pw, None) == SHAPE   # more cubes than the pairing takes
+    assert h(I, 1, 24, 512, 600, P4, W, pw, None) == SHAPE
+    assert h(I, 1, 24, 512, 64, I, W, pw, None) == ALIAS
+    assert h(I, 1, 24, 512, 64, P4, W, pw - 1, None) == WORKSPACE
+    assert h(I, 1, 24, 512, 64, P4, None, pw, None) == WORKSPACE
+    assert h(I, 1, 24, 512, 64, P4, ctypes.c_void_p(0x7C000008), pw, None) == ALIGN
+    assert h(I, 1, 24, 512, 64, P4, P4, pw, None) == ALIAS   # workspace over the pairs
+    assert h(I, 1, 24, 512, 64, P4, W, pw, None) in (CUDA, OK)
 
 
 def test_product_package_does_not_import_oracle():

@@ -27,14 +27,40 @@ def assert_close(got, ref, what=""):
     assert bad == 0, f"{what}: {bad} of {excess.size} outside tolerance, max excess {excess.max():.3e}"
 
 
-def check_pairing(pairs, nc):
-    for row in pairs.reshape(-1, (nc + 1) // 2, 2):
+def union_tiles(sel, a, b):
+    u = set(sel[a].tolist()) | (set(sel[b].tolist()) if b >= 0 else set())
+    return (len(u) + 1) // 2
+
+
+def check_pairing(pairs, nc, idx=None):
+    """Every cube exactly once, the lower cube first, pairs longest union first (ties: the
+    lower first cube)."""
+    rows = pairs.reshape(-1, (nc + 1) // 2, 2)
+    sels = None if idx is None else idx.reshape(-1, nc, idx.shape[-1])
+    for h, row in enumerate(rows):
         seen = row.reshape(-1)
         real = seen[seen >= 0]
         assert np.array_equal(np.sort(real), np.arange(nc))        # every cube exactly once
         assert (seen < 0).sum() == nc % 2
         assert np.all(row[:, 0] >= 0)
-        assert np.all(np.diff(row[:, 0]) > 0)                       # listed by first cube
+        assert np.all((row[:, 1] < 0) | (row[:, 1] > row[:, 0]))
+        if sels is not None:
+            keys = [(-union_tiles(sels[h], a, b), a) for a, b in row]
+            assert keys == sorted(keys)
+
+
+def greedy_pairs(sel, nc):
+    """The greedy pairing by selection overlap (ties: the lower cube indices), listed longest
+    union first: a plain restatement for the test."""
+    sets = [set(r.tolist()) for r in sel]
+    cand = sorted((-len(sets[a] & sets[b]), a, b) for a in range(nc) for b in range(a + 1, nc))
+    used, out = set(), []
+    for _, a, b in cand:
+        if a not in used and b not in used:
+            used |= {a, b}
+            out.append((a, b))
+    out += [(a, -1) for a in range(nc) if a not in used]
+    return sorted(out, key=lambda p: (-union_tiles(sel, p[0], p[1]), p[0]))
 
 
 @pytest.mark.parametrize("B,grid,topk", [(1, (8, 32, 32), 16), (1, (4, 16, 20), 9),
@@ -46,7 +72,7 @@ def test_pairing_valid_and_sparse_matches(gb, B, grid, topk):
     pairs = gb.vsa_pair_query_cubes(idx)
     torch.cuda.synchronize()
     nc = idx.shape[2]
-    check_pairing(pairs.cpu().numpy(), nc)
+    check_pairing(pairs.cpu().numpy(), nc, idx.cpu().numpy())
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
     o = gb.vsa_sparse_fwd(tq, tk, tv, idx, pairs=pairs, lse=lse)
     torch.cuda.synchronize()
@@ -98,10 +124,24 @@ def test_pairing_full_workload(gb):
     torch.cuda.synchronize()
     assert gb.device_status() == 0
     nc = idx.shape[2]
-    check_pairing(pairs.cpu().numpy(), nc)
+    check_pairing(pairs.cpu().numpy(), nc, idx.cpu().numpy())
     S = q.shape[2]
     rows = inputs.sample_rows(w["B"] * w["H"], S, 4096, w["seed"])
     ridx = idx.cpu().numpy()          # the selection itself is checked bit-exact elsewhere
     ro, _ = OA.vsa_sparse_attention(q, k, v, ridx, 64, inputs.softmax_scale(w["D"]), rows=rows)
     fo = o.float().cpu().numpy().reshape(-1, S, w["D"])[rows[:, 0], rows[:, 1]]
     assert_close(fo, ro, "o")
+
+
+@pytest.mark.parametrize("grid,topk,seed", [((4, 12, 12), 4, 71), ((4, 12, 20), 7, 72),
+                                            ((8, 32, 32), 16, 73)])
+def test_pairing_is_the_greedy_pairing(gb, grid, topk, seed):
+    """Bit-exact against the greedy pairing written out on the CPU (odd and even cube counts,
+    many tied overlaps with few selected cubes)."""
+    q, k, _ = inputs.vsa_inputs(1, 2, 128, seed=seed, grid=grid)
+    idx = gb.vsa_select_blocks(t(q), t(k), topk)
+    pairs = gb.vsa_pair_query_cubes(idx).cpu().numpy()
+    sel = idx.cpu().numpy()
+    nc = sel.shape[2]
+    for h in range(2):
+        assert [tuple(p) for p in pairs[0, h].tolist()] == greedy_pairs(sel[0, h], nc)
