@@ -1631,51 +1631,6 @@ using namespace gbattn;
 
 
 
-extern "C" int attn_dense_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                              int B, int H, int Sq, int Skv, int D, const int64_t* q_strides,
-                              const int64_t* kv_strides, const int64_t* o_strides, float scale,
-                              void* stream) {
-    CallRange nvtx_range("attn_dense_fwd");
-    if (!q || !k || !v || !o) return GBATTN_ERR_NULL;
-    if (B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0) return GBATTN_ERR_SHAPE;
-    if (static_cast<long long>(B) * H > 65535) return GBATTN_ERR_SHAPE;
-    if (D != 128) return GBATTN_ERR_UNSUPPORTED;
-    Strides qs, kvs, os;
-    if (!make_strides(q_strides, B, H, Sq, D, false, &qs) ||
-        !make_strides(kv_strides, B, H, Skv, D, false, &kvs) ||
-        !make_strides(o_strides, B, H, Sq, D, true, &os))
-        return GBATTN_ERR_SHAPE;
-    if (!finite_positive(scale)) return GBATTN_ERR_SCALE;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-        (reinterpret_cast<uintptr_t>(lse) & 3u))
-        return GBATTN_ERR_ALIGN;
-    const size_t qb = strided_bytes(qs, B, H, Sq, D);
-    const size_t kb = strided_bytes(kvs, B, H, Skv, D);
-    const size_t ob = strided_bytes(os, B, H, Sq, D);
-    const size_t lb = static_cast<size_t>(B) * H * Sq * 4;
-    if (overlaps(o, ob, q, qb) || overlaps(o, ob, k, kb) || overlaps(o, ob, v, kb) ||
-        overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
-        overlaps(lse, lb, o, ob))
-        return GBATTN_ERR_ALIAS;
-    DeviceState dev;
-    int rc = current_device(&dev);
-    if (rc != GBATTN_OK) return rc;
-    AttnArgs a = base_args(dev, scale);
-    a.seq_q = Sq;
-    a.seq_k = Skv;
-    a.heads_q = B * H;
-    a.hq = H;
-    a.hkv = H;
-    a.n_chunks = 1;
-    a.o = static_cast<__half*>(o);
-    set_out_strides(a, os);
-    a.lse = lse;
-    const int n_qt = (Sq + BM - 1) / BM;
-    return launch_attn<128, kDense>(q, k, v, Sq, Skv, B * H, qs, kvs,
-                                    static_cast<long long>(n_qt) * B * H, n_qt, a,
-                                    static_cast<cudaStream_t>(stream));
-}
-
 extern "C" int attn_dense_mask_fwd(const void* q, const void* k, const void* v, const void* mask,
                                    long long mask_stride_b, long long mask_stride_h, void* o,
                                    float* lse, int B, int H, int Sq, int Skv, int D, float scale,
