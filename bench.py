@@ -266,7 +266,7 @@ def peaks():
 
 
 KERNEL_SOURCES = {
-    "attn_fwd_kernel<128,dense>": ("attn.cu", "ptx.cuh", "host.h"),
+    "attn_dense_kernel": ("attn_dense.cu", "ptx.cuh", "host.h"),
     "attn_fwd_kernel<128,sparse>": ("attn.cu", "ptx.cuh", "host.h"),
     "attn_fwd_kernel<256,causal>+merge": ("attn.cu", "ptx.cuh", "host.h"),
     "e4m3_bridge_kernel": ("bridge.cu", "e4m3.cuh", "ptx.cuh", "host.h"),
@@ -960,7 +960,7 @@ def main():
     dom = max(attn_calls, key=attn_calls.get)
     dom_w = next(w for w in wls if dom.startswith(w.name + ":"))
     achieved = dom_w.flops / (attn_calls[dom] * 1e-3) / 1e12
-    kernel_name = {"dense": "attn_fwd_kernel<128,dense>", "vsa": "attn_fwd_kernel<128,sparse>",
+    kernel_name = {"dense": "attn_dense_kernel", "vsa": "attn_fwd_kernel<128,sparse>",
                    "paged": "attn_fwd_kernel<256,causal>+merge",
                    "causal": "attn_fwd_kernel<256,causal>+merge"}[dom_w.w["kind"]]
     peak_tc = pk["tc_sust"] or pk["tc"]
