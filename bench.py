@@ -991,8 +991,8 @@ def main():
             gbs = sel_bytes / (t * 1e-3) / 1e9
             extra["select"] = {"ms": t, "achieved": gbs, "unit": "GB/s", "peak": pk["hbm"],
                                "frac": gbs / pk["hbm"], "bytes_per_call": sel_bytes,
-                               "kernels": "vsa_pool_kernel + vsa_score_select_kernel + "
-                                          "vsa_select_fallback_kernel",
+                               "kernels": "vsa_pool_kernel + vsa_score_kernel + vsa_topk_kernel "
+                                          "(+ its fallback form for rows with many undecided keys)",
                                "timing": "CUDA events around the call inside the step"}
     per_variant = {}
     for w in wls:
