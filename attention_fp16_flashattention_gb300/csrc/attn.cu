@@ -132,8 +132,8 @@ constexpr int kSmemMax = 232448;   // dynamic shared memory a CTA may opt into (
 struct Ctrl {
     uint64_t q_full[2];    // query buffer b loaded
     uint64_t q_empty[2];   // the last QK of the item that used query buffer b is done
-    uint64_t full[4];
-    uint64_t empty[4];
+    uint64_t full[5];
+    uint64_t empty[5];
     uint64_t s_full[3];    // QK_g done (buffer g % NSB), g counting every tile of the CTA
     uint64_t p_full[3];    // P_g written (buffer g % NSB)
     uint64_t pv_done[3];   // PV_g done (barrier g % NSB).  QK_g is issued after
@@ -204,8 +204,10 @@ constexpr int kMaskStageBytes = 2 * kMaskSlotBytes + 4 * 8;
 
 template <int D, int MODE>
 struct Cfg {
-    // K/V ring slots (the masked mode gives one D=128 slot to its mask stages)
-    static constexpr int NS = D == 128 ? (MODE == 3 ? 3 : 4) : 2;
+    // K/V ring slots (the masked mode gives one D=128 slot to its mask stages; the
+    // VSA modes, whose key cubes are gathered from across the head and miss L2
+    // more often, take a fifth in place of a second query buffer)
+    static constexpr int NS = D == 128 ? (MODE == 3 ? 3 : is_sparse(MODE) ? 5 : 4) : 2;
     static constexpr int NSB = D == 128 ? 3 : 2;         // S buffers in TMEM (QK lookahead)
     static constexpr int CHUNK = 128 * 128;               // 128 rows x 64 FP16 columns
     static constexpr int HALF = 64 * 128;                 // 64 rows x 64 columns
@@ -218,7 +220,7 @@ struct Cfg {
                                 (MODE == kMasked ? kMaskStageBytes : 0);
     // Two query buffers where they fit: the next item's query tile then loads
     // while the last QKs of the current item still read theirs.
-    static constexpr int QB = persistent(MODE) && REST + 2 * Q_BYTES <= kSmemMax ? 2 : 1;
+    static constexpr int QB = persistent(MODE) && !is_sparse(MODE) && REST + 2 * Q_BYTES <= kSmemMax ? 2 : 1;
     static constexpr int SMEM = REST + QB * Q_BYTES;
     static_assert(SMEM <= kSmemMax, "shared memory budget");
     // TMEM columns: S buffer b at b*128 (P of that tile overwrites its first 64
@@ -716,7 +718,9 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             while (!drawn_last) drawn_last = next_item(a, 0) >= a.n_items;
     } else if (warp == 0) {
         // ================= TMA producer (whole warp; one elected lane issues)
-        int last_it[4] = {-1, -1, -1, -1};   // last ring position issued into each slot
+        int last_it[C::NS];                  // last ring position issued into each slot
+#pragma unroll
+        for (int s = 0; s < C::NS; ++s) last_it[s] = -1;
         int last_q[2] = {-1, -1};            // last use issued into each query buffer
         int ring = 0, qu = 0;
         bool ok = true;
