@@ -2,19 +2,23 @@
 // FP16 Q/K/V/P/O, FP32 accumulation in tensor memory and an FP32 online softmax
 // ("Integrate FP32 v37 prefill and exact E4M3 bridge", Implementation: FP32
 // QK/PV accumulation, FP32 prefix/tail state and final merge, FP16
-// probabilities and output).
+// probabilities and output).  This file holds the causal (plain and paged
+// E4M3), masked and VSA modes; dense attention has its own copy of the
+// pipeline in attn_dense.cu.
 //
-// One CTA owns a 128-row query tile and walks a list of 128-key tiles.  Each
-// key tile is two 64-key halves; for dense and causal attention the halves are
+// A work item is a 128-row query tile with a list of 128-key tiles.  Each key
+// tile is two 64-key halves; for causal and masked attention the halves are
 // adjacent, for VSA they are two selected 64-token cubes (the two-query-half x
 // two-key-half blocks with a 4-bit quadrant mask of block_lists.py in the
-// FastVideo compare view).
+// FastVideo compare view).  Causal and masked launches run one CTA per item;
+// the VSA modes run persistent CTAs (one per SM) whose scheduler warp draws
+// items from a counter and builds their tile lists one item ahead.
 //
-// Warp roles (352 threads at D=128, 384 with the mask warp, 320 at D=256, 448 with
-// the paged converters):
-//   warp 0      TMA producer: Q once, then K and V tiles through an NS-slot ring
-//               in the order the MMAs consume them (K0 .. K_{NSB-1}, V0, K_NSB,
-//               V1, ...).
+// Warp roles (320 threads at D=256, 384 with the mask warp or the VSA scheduler,
+// 448 with the paged converters):
+//   warp 0      TMA producer: each item's Q, then K and V tiles through an
+//               NS-slot ring in the order the MMAs consume them (K0 .. K_{NSB-1},
+//               V0, K_NSB, V1, ...); items follow each other in the ring.
 //   warp 1      allocates tensor memory and issues S = Q K_t^T (SMEM x SMEM);
 //               at D=128 only these, at D=256 also every PV, in order.
 //   warp 10     (D=128) issues O += P_j V_j (P from TMEM), so that neither MMA
@@ -25,7 +29,8 @@
 //               exp2 with packed FP32 pairs, row sum, P -> FP16 into TMEM; lazy
 //               O rescaling (only when the running max grows by more than 2^8),
 //               each thread on its half of O; epilogue O / l.
-//   warp 11     (masked) loads each tile's 128 x 128 mask block two tiles ahead.
+//   warp 11     (masked) loads each tile's 128 x 128 mask block two tiles ahead;
+//               (VSA) the scheduler.
 //   warps 10..13 (paged causal) convert E4M3 page rows to FP16 in shared memory.
 // Tensor memory (512 columns): NSB S buffers of 128 FP32 columns (3 for D=128,
 // 2 for D=256); P_j overwrites the first 64 columns of its S buffer as FP16
