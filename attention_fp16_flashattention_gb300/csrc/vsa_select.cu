@@ -601,11 +601,14 @@ constexpr int kTopkWarps = 8;
 constexpr int kFbWarps = 2;
 constexpr float kErrScale = 1.0f / 32768.0f;
 
-template <int CH, int CAP, bool FALLBACK>
+// NCF: the cube count as a compile-time constant (a row of exactly CH chunks,
+// so every per-key bounds test folds away), or 0 to take it from nc_arg.
+template <int CH, int CAP, bool FALLBACK, int NCF = 0>
 __global__ void __launch_bounds__(FALLBACK ? kFbWarps * 32 : kTopkWarps * 32, FALLBACK ? 1 : (CH > 16 ? 2 : 3)) vsa_topk_kernel(
     float* __restrict__ S, const float* __restrict__ qm, const float* __restrict__ km,
-    const float* __restrict__ qn, const float* __restrict__ kn, int NC, int topk, long long rows,
+    const float* __restrict__ qn, const float* __restrict__ kn, int nc_arg, int topk, long long rows,
     int32_t* __restrict__ deferred, int32_t* __restrict__ idx, uint32_t* status, float coarse_l2) {
+    const int NC = NCF ? NCF : nc_arg;
     extern __shared__ __align__(16) uint8_t topk_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int kWarps = FALLBACK ? kFbWarps : kTopkWarps;
@@ -925,12 +928,20 @@ int select_impl(const void* q, const void* k, const void* v, int B, int H, int S
     cudaError_t e;
     if (NC <= 512) {
         cfg.dynamicSmemBytes = topk_smem_bytes<16, kCap, kTopkWarps>();
-        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<16, kCap, false>, scores, cqm, ckm, cqn, ckn, NC,
-                               topk, rows, deferred, idx, dev.status, coarse_l2);
+        e = NC == 512 ? cudaLaunchKernelEx(&cfg, vsa_topk_kernel<16, kCap, false, 512>, scores, cqm,
+                                           ckm, cqn, ckn, NC, topk, rows, deferred, idx, dev.status,
+                                           coarse_l2)
+                      : cudaLaunchKernelEx(&cfg, vsa_topk_kernel<16, kCap, false>, scores, cqm, ckm,
+                                           cqn, ckn, NC, topk, rows, deferred, idx, dev.status,
+                                           coarse_l2);
     } else {
         cfg.dynamicSmemBytes = topk_smem_bytes<32, kCap, kTopkWarps>();
-        e = cudaLaunchKernelEx(&cfg, vsa_topk_kernel<32, kCap, false>, scores, cqm, ckm, cqn, ckn, NC,
-                               topk, rows, deferred, idx, dev.status, coarse_l2);
+        e = NC == 1024 ? cudaLaunchKernelEx(&cfg, vsa_topk_kernel<32, kCap, false, 1024>, scores, cqm,
+                                            ckm, cqn, ckn, NC, topk, rows, deferred, idx, dev.status,
+                                            coarse_l2)
+                       : cudaLaunchKernelEx(&cfg, vsa_topk_kernel<32, kCap, false>, scores, cqm, ckm,
+                                            cqn, ckn, NC, topk, rows, deferred, idx, dev.status,
+                                            coarse_l2);
     }
     if (!launched(e)) return GBATTN_ERR_CUDA;
     const long long fb_ctas = std::min<long long>((rows + 32 * kFbWarps - 1) / (32 * kFbWarps),
