@@ -1138,10 +1138,13 @@ __device__ __forceinline__ int popc_and4(uint4 x, uint4 y) {
 // bitwise search for the overlap threshold tau (the largest value that at least
 // kPairCand partners reach), every partner above tau, the lowest-index partners
 // at tau, and a 32-lane bitonic sort of their keys.
-template <int CPL, int CPW>
+// NCF: the cube count as a compile-time constant (every bounds test and the
+// row length fold away), or 0 to take it from nc_arg.
+template <int CPL, int CPW, int NCF = 0>
 __global__ void __launch_bounds__(kCandThreads) vsa_pair_cand_kernel(const uint32_t* __restrict__ gbits,
-                                                                     int nc, int top_bit,
+                                                                     int nc_arg, int top_bit,
                                                                      int16_t* __restrict__ cand) {
+    const int nc = NCF ? NCF : nc_arg;
     extern __shared__ uint32_t csm[];
     const int rw = pair_row_words(nc);
     uint32_t* bits = csm;                                   // [nc][rw]
@@ -1412,6 +1415,9 @@ extern "C" int vsa_pair_query_cubes(const int32_t* idx, int B, int H, int n_cube
         std::call_once(once[dev.device], [] {
             cudaFuncSetAttribute(vsa_pair_cand_kernel<16, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(cand_smem_bytes(kPairMaxCubes)));
+            cudaFuncSetAttribute(vsa_pair_cand_kernel<16, 4, 512>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(cand_smem_bytes(kPairMaxCubes)));
             cudaFuncSetAttribute(vsa_pair_cand_kernel<32, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(cand_smem_bytes(kPairMaxCubes)));
             cudaFuncSetAttribute(vsa_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1429,7 +1435,10 @@ extern "C" int vsa_pair_query_cubes(const int32_t* idx, int B, int H, int n_cube
     const dim3 cgrid((n_cubes + per_cta - 1) / per_cta, static_cast<unsigned>(B * H));
     int top_bit = 0;   // the highest bit an overlap (at most topk) can have
     while ((2 << top_bit) <= topk) ++top_bit;
-    if (cpw == 4)
+    if (n_cubes == 512)
+        vsa_pair_cand_kernel<16, 4, 512><<<cgrid, kCandThreads, cand_smem_bytes(n_cubes), s>>>(
+            gbits, n_cubes, top_bit, cand);
+    else if (cpw == 4)
         vsa_pair_cand_kernel<16, 4><<<cgrid, kCandThreads, cand_smem_bytes(n_cubes), s>>>(gbits, n_cubes, top_bit, cand);
     else
         vsa_pair_cand_kernel<32, 2><<<cgrid, kCandThreads, cand_smem_bytes(n_cubes), s>>>(gbits, n_cubes, top_bit, cand);

@@ -134,10 +134,11 @@ def test_pairing_full_workload(gb):
 
 
 @pytest.mark.parametrize("grid,topk,seed", [((4, 12, 12), 4, 71), ((4, 12, 20), 7, 72),
-                                            ((8, 32, 32), 16, 73)])
+                                            ((8, 32, 32), 16, 73), ((8, 64, 64), 64, 74)])
 def test_pairing_is_the_greedy_pairing(gb, grid, topk, seed):
     """Bit-exact against the greedy pairing written out on the CPU (odd and even cube counts,
-    many tied overlaps with few selected cubes)."""
+    many tied overlaps with few selected cubes, and the workload's 512 cubes at top-64, which
+    take the candidate kernel's fixed-size instance)."""
     q, k, _ = inputs.vsa_inputs(1, 2, 128, seed=seed, grid=grid)
     idx = gb.vsa_select_blocks(t(q), t(k), topk)
     pairs = gb.vsa_pair_query_cubes(idx).cpu().numpy()
