@@ -495,16 +495,17 @@ __device__ __forceinline__ void write_row(const RowClass<CH>& rc, const Cands<CA
 // Batched FP32 product S[bh] = Qm[bh] Km[bh]^T of the cube means ([NC][128]
 // each), one 128 x 128 tile of S per CTA.  256 threads, each an 8 x 8 register
 // tile (rows 4ty.., 64+4ty.., columns 4tx.., 64+4tx..); the two operand tiles
-// pass through shared memory eight dims at a time, stored dim-major so that
-// every operand read is a 16-byte load, with the next eight dims loaded into
-// registers (one 16-byte load per operand per thread) while the current ones
+// pass through shared memory sixteen dims at a time, stored dim-major so that
+// every operand read is a 16-byte load, with the next sixteen dims loaded into
+// registers (two 16-byte loads per operand per thread) while the current ones
 // are multiplied.  Every score is a sequence of FFMAs over d = 0..127, issued
 // two scores at a time as packed FP32 pair FMAs (each lane an IEEE FMA with
 // round to nearest, so the scores are those of scalar FFMAs).
 // (Two CTAs fit on an SM.  A 4 x 8 thread tile with three CTAs per SM, for
 // fewer idle SMs in the last wave, measured slower: 54 against 47 us.)
 constexpr int kGT = 128;          // tile edge (query cubes x key cubes)
-constexpr int kGK = 8;            // dims per stage
+constexpr int kGK = 8;            // keys per stage of the coarse product
+constexpr int kSK = 16;           // dims per stage of the score product
 constexpr int kGThreads = 256;
 constexpr int kGP = kGT + 4;      // shared-memory pitch (conflict-free transposing stores)
 constexpr int kSelD = 128;
@@ -514,8 +515,8 @@ __host__ __device__ constexpr int score_ld(int NC) { return (NC + kGT - 1) / kGT
 __global__ void __launch_bounds__(kGThreads, 2) vsa_score_kernel(const float* __restrict__ qm,
                                                                  const float* __restrict__ km,
                                                                  int NC, float* __restrict__ S) {
-    __shared__ __align__(16) float As[2][kGK][kGP];
-    __shared__ __align__(16) float Bs[2][kGK][kGP];
+    __shared__ __align__(16) float As[2][kSK][kGP];
+    __shared__ __align__(16) float Bs[2][kSK][kGP];
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the means come from the pool kernel
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int t = threadIdx.x;
@@ -524,19 +525,31 @@ __global__ void __launch_bounds__(kGThreads, 2) vsa_score_kernel(const float* __
     const int LD = score_ld(NC);
     const float* A = qm + bh * NC * kSelD;
     const float* B = km + bh * NC * kSelD;
-    const int lr = t >> 1, lk = (t & 1) * 4;   // staging: row lr, dims lk..lk+3 of a stage
+    // staging: thread t loads row lr, dims lk..lk+3 and lk+8..lk+11 of each stage
+    constexpr int J = kSK / 8;
+    const int lr = t >> 1, lk = (t & 1) * 4;
     const bool a_live = m0 + lr < NC, b_live = n0 + lr < NC;
     const float* a_src = A + static_cast<long long>(m0 + lr) * kSelD + lk;
     const float* b_src = B + static_cast<long long>(n0 + lr) * kSelD + lk;
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 ra = a_live ? *reinterpret_cast<const float4*>(a_src) : zero;
-    float4 rb = b_live ? *reinterpret_cast<const float4*>(b_src) : zero;
-    auto stage = [&](int buf) {
-        As[buf][lk + 0][lr] = ra.x; As[buf][lk + 1][lr] = ra.y;
-        As[buf][lk + 2][lr] = ra.z; As[buf][lk + 3][lr] = ra.w;
-        Bs[buf][lk + 0][lr] = rb.x; Bs[buf][lk + 1][lr] = rb.y;
-        Bs[buf][lk + 2][lr] = rb.z; Bs[buf][lk + 3][lr] = rb.w;
+    float4 ra[J], rb[J];
+    auto load = [&](int d0) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            ra[j] = a_live ? *reinterpret_cast<const float4*>(a_src + d0 + 8 * j) : zero;
+            rb[j] = b_live ? *reinterpret_cast<const float4*>(b_src + d0 + 8 * j) : zero;
+        }
     };
+    auto stage = [&](int buf) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            As[buf][lk + 8 * j + 0][lr] = ra[j].x; As[buf][lk + 8 * j + 1][lr] = ra[j].y;
+            As[buf][lk + 8 * j + 2][lr] = ra[j].z; As[buf][lk + 8 * j + 3][lr] = ra[j].w;
+            Bs[buf][lk + 8 * j + 0][lr] = rb[j].x; Bs[buf][lk + 8 * j + 1][lr] = rb[j].y;
+            Bs[buf][lk + 8 * j + 2][lr] = rb[j].z; Bs[buf][lk + 8 * j + 3][lr] = rb[j].w;
+        }
+    };
+    load(0);
     stage(0);
     __syncthreads();
     const int ty = t >> 4, tx = t & 15;
@@ -545,16 +558,13 @@ __global__ void __launch_bounds__(kGThreads, 2) vsa_score_kernel(const float* __
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int p = 0; p < 4; ++p) acc[i][p] = 0ull;
-    constexpr int NCH = kSelD / kGK;
+    constexpr int NCH = kSelD / kSK;
 #pragma unroll 1
     for (int ch = 0; ch < NCH; ++ch) {
         const int buf = ch & 1;
-        if (ch + 1 < NCH) {
-            ra = a_live ? *reinterpret_cast<const float4*>(a_src + (ch + 1) * kGK) : zero;
-            rb = b_live ? *reinterpret_cast<const float4*>(b_src + (ch + 1) * kGK) : zero;
-        }
+        if (ch + 1 < NCH) load((ch + 1) * kSK);
 #pragma unroll
-        for (int kk = 0; kk < kGK; ++kk) {
+        for (int kk = 0; kk < kSK; ++kk) {
             const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][4 * ty]);
             const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + 4 * ty]);
             const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][4 * tx]);
