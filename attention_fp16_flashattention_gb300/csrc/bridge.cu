@@ -57,15 +57,17 @@ __device__ __forceinline__ void chunk_place(long long g, const BridgeGeom& q, lo
     }
 }
 
-// Each thread takes chunks g, g + stride, g + 2 stride, g + 3 stride of the grid
-// stride loop together: their eight loads are in flight before the first store.
+// Each thread takes chunks g and g + stride of the grid stride loop together:
+// their four loads are in flight before the first store.  (Four chunks per
+// thread kept more loads in flight but ran 5% slower: 41.6 against 39.6 us per
+// call, 37.3 against 35.5 us back to back; eight chunks 45.7 us.)
 template <bool kHalfScale, bool kPow2>
 __global__ void __launch_bounds__(256) e4m3_bridge_kernel(
     const uint8_t* __restrict__ kp, const uint8_t* __restrict__ vp,
     const int32_t* __restrict__ table, int num_phys, int kv_len, BridgeGeom q,
     float ks, float vs, __half2 ks2, __half2 vs2, __half* __restrict__ ko,
     __half* __restrict__ vo, uint32_t* status) {
-    constexpr int U = 4;
+    constexpr int U = 2;
     const long long per_token = static_cast<long long>(q.hkv) * (q.D >> 3);
     const long long total = static_cast<long long>(kv_len) * per_token;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
