@@ -1027,7 +1027,6 @@ namespace gbattn {
 namespace {
 constexpr int kPairThreads = 1024;   // vsa_pair_kernel: one thread per cube
 constexpr int kPairMaxCubes = 1024;
-constexpr int kPairMaxWords = kPairMaxCubes / 32;
 constexpr int kPairCand = 32;        // candidates kept per cube (one per lane)
 constexpr int kCandThreads = 128;    // vsa_pair_cand_kernel: four warps
 
