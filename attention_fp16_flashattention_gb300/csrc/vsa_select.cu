@@ -614,7 +614,7 @@ constexpr float kErrScale = 1.0f / 32768.0f;
 // NCF: the cube count as a compile-time constant (a row of exactly CH chunks,
 // so every per-key bounds test folds away), or 0 to take it from nc_arg.
 template <int CH, int CAP, bool FALLBACK, int NCF = 0>
-__global__ void __launch_bounds__(FALLBACK ? kFbWarps * 32 : kTopkWarps * 32, FALLBACK ? 1 : (CH > 16 ? 2 : 3)) vsa_topk_kernel(
+__global__ void __launch_bounds__(FALLBACK ? kFbWarps * 32 : kTopkWarps * 32, FALLBACK ? 1 : (CH > 16 ? 2 : 4)) vsa_topk_kernel(
     float* __restrict__ S, const float* __restrict__ qm, const float* __restrict__ km,
     const float* __restrict__ qn, const float* __restrict__ kn, int nc_arg, int topk, long long rows,
     int32_t* __restrict__ deferred, int32_t* __restrict__ idx, uint32_t* status, float coarse_l2) {
