@@ -613,6 +613,8 @@ constexpr float kErrScale = 1.0f / 32768.0f;
 
 // NCF: the cube count as a compile-time constant (a row of exactly CH chunks,
 // so every per-key bounds test folds away), or 0 to take it from nc_arg.
+// Rows of 16 chunks run four CTAs per SM (64 registers, a few spilled): the
+// selection is issue-bound and the extra warps measured faster than three CTAs.
 template <int CH, int CAP, bool FALLBACK, int NCF = 0>
 __global__ void __launch_bounds__(FALLBACK ? kFbWarps * 32 : kTopkWarps * 32, FALLBACK ? 1 : (CH > 16 ? 2 : 4)) vsa_topk_kernel(
     float* __restrict__ S, const float* __restrict__ qm, const float* __restrict__ km,
